@@ -1,0 +1,151 @@
+/*
+ * nvfp4moe.h -- C ABI of the GB300 (sm_103a) routed NVFP4 SiTU MoE forward.
+ *
+ * The operation ("Cake SiTU backend", FlashInfer tutorial, intro): BF16 x is
+ * routed to top-k experts, quantized to group-16 NVFP4, run through FC1 (gate
+ * and up), SiTU = (beta*tanh(g/beta)*sigmoid(g)) * (lambda*tanh(u/lambda))
+ * (defaults 4 and 25), requantized to NVFP4, run through FC2 and combined with
+ * the BF16 route weights into a BF16 output.  Init-routing follows the
+ * torch_npu page "npu_moe_init_routing_v2", section 计算公式 (formulas 1-5).
+ *
+ * Conventions for every entry point:
+ *  - Pointers are DEVICE pointers owned by the caller unless marked "host".
+ *  - The library allocates no memory, never synchronizes the stream (except
+ *    moe_read_status, a test helper), and never reads routing values on the
+ *    host ("Cake SiTU backend", section "Caller-owned execution": routing
+ *    values never participate in host dispatch; submission makes no CUDA
+ *    allocation).  All work is enqueued on `stream` in order, so a complete
+ *    call can be captured in a CUDA graph and replayed.
+ *  - Host-side validation failures return a status synchronously and launch
+ *    nothing.  Device-side anomalies (an expert id outside [0, E), a bounded
+ *    wait that gave up) never trap: they are OR-ed into a status word in the
+ *    workspace, read by moe_read_status.
+ *  - Concurrent calls need separate workspace and output buffers.
+ */
+#ifndef NVFP4MOE_H_
+#define NVFP4MOE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,          /* null pointer, bad size, bad option, misaligned pointer */
+  MOE_ERR_UNSUPPORTED = 2,          /* shape or option outside what the kernels implement */
+  MOE_ERR_WORKSPACE_TOO_SMALL = 3,  /* ws_bytes below moe_workspace_size for this call */
+  MOE_ERR_NOT_PREPARED = 4,         /* token count not passed to moe_prepare_workspace on this ws */
+  MOE_ERR_CUDA = 5,                 /* a CUDA runtime/driver call failed (launch, tensor map) */
+  MOE_ERR_DEVICE_STATUS = 6         /* moe_read_status found a non-zero device status */
+} moe_status_t;
+
+/* H (hidden), I (intermediate), E (local experts), k (top-k).
+ * Supported: H % 256 == 0, I % 128 == 0, 1 <= E <= 1024, 1 <= k <= min(32, E).
+ * The pages' shape is H=3584, I=384, E=896, k=16 ("Cake SiTU backend", intro). */
+typedef struct {
+  int32_t hidden, inter, num_experts, top_k;
+} moe_shape_t;
+
+/* Device status word bits (moe_read_status). */
+#define MOE_DEVSTAT_INVALID_EXPERT 1  /* an expert id outside [0, E) was skipped */
+#define MOE_DEVSTAT_TIMEOUT 2         /* a bounded wait inside a kernel gave up */
+#define MOE_DEVSTAT_BAD_TILE 4        /* a tile descriptor failed a bounds check */
+
+/* Workspace bytes for any token count 1..max_tokens ("Cake SiTU backend",
+ * "The size query uses host metadata only").  *bytes is a HOST pointer.
+ * The workspace holds the routing arrays, the quantized activations, the
+ * quantized intermediate, an fp32 output accumulator and the default SiTU
+ * constants.  Its carve-up depends only on the shape and its byte size, so
+ * a maximum-size workspace serves every smaller token count. */
+moe_status_t moe_workspace_size(const moe_shape_t* shape, int64_t max_tokens, size_t* bytes);
+
+/* Bytes of each prepared weight buffer.  They equal the canonical sizes
+ * ("Cake SiTU backend", "Prepared weights and scales": uint8 [E,2I,H/2] and
+ * [E,H,I/2], block scales [E,2I,H/16] and [E,H,I/16]).  Host out pointers. */
+moe_status_t moe_prepared_weight_bytes(const moe_shape_t* shape, size_t* w13_bytes, size_t* sf13_bytes,
+                                       size_t* w2_bytes, size_t* sf2_bytes);
+
+/* Weight preparation, run once per model ("Cake SiTU backend", "Prepared
+ * weights and scales": prepare once, scales carried with the packed bytes).
+ * Input is the canonical layout: w13 [E, 2I, H/2] packed E2M1 with the even
+ * element in the low nibble, rows 0..I-1 the gate (w1) and I..2I-1 the up
+ * projection (w3); sf13 [E, 2I, H/16] E4M3 row-major; w2 [E, H, I/2];
+ * sf2 [E, H, I/16].  Output is this library's private layout (same byte
+ * counts): codes tiled per MMA tile, gate and up tiles side by side, block
+ * scales in the 128x4 atom layout of the "Nvfp4 Tensor" page (block_scale).
+ * In and out must not overlap; outputs 256-byte aligned.  Asynchronous. */
+moe_status_t moe_prepare_weights(const moe_shape_t* shape, const uint8_t* w13, const uint8_t* sf13,
+                                 const uint8_t* w2, const uint8_t* sf2, uint8_t* w13_out, uint8_t* sf13_out,
+                                 uint8_t* w2_out, uint8_t* sf2_out, cudaStream_t stream);
+
+/* Per-token-count preparation ("Cake SiTU backend": "Prepare every token
+ * count before its first submission"; it initializes the default SiTU
+ * constants and allocates nothing).  Writes the default beta = 4 and
+ * lambda = 25 arrays and clears the status word in `ws` (256-byte aligned),
+ * and records (ws, ws_bytes, num_tokens) as prepared in a host-side table.
+ * Must be stream-ordered before the first moe_forward / moe_init_routing
+ * with this num_tokens. */
+moe_status_t moe_prepare_workspace(const moe_shape_t* shape, void* ws, size_t ws_bytes, int64_t num_tokens,
+                                   cudaStream_t stream);
+
+/* The forward ("Cake SiTU backend", whole page):
+ *   x [T, H] bf16; expert_ids [T, k] int32 in [0, E); route_weights [T, k] bf16;
+ *   w13, sf13, w2, sf2 prepared by moe_prepare_weights (w13, w2 256-byte aligned);
+ *   qX [1], dX_dW13 [E], qA [E], dA_dW2 [E] fp32 (the six quant_scales minus
+ *   the two block-scale tensors; qX = 1/dX, qA = 1/dA);
+ *   situ_beta, situ_linear_beta [E] fp32 or NULL (then 4 and 25);
+ *   out [T, H] bf16, written completely.
+ * T = num_tokens must be prepared on ws.  Ids outside [0, E) are skipped and
+ * flagged in the status word. */
+moe_status_t moe_forward(const moe_shape_t* shape, int64_t num_tokens, const void* x, const int32_t* expert_ids,
+                         const void* route_weights, const uint8_t* w13, const uint8_t* sf13, const uint8_t* w2,
+                         const uint8_t* sf2, const float* qX, const float* dX_dW13, const float* qA,
+                         const float* dA_dW2, const float* situ_beta, const float* situ_linear_beta, void* ws,
+                         size_t ws_bytes, void* out, cudaStream_t stream);
+
+/* Options of moe_init_routing (torch_npu "npu_moe_init_routing_v2",
+ * parameter list: drop_pad_mode, expert_capacity, row_idx_type,
+ * expert_tokens_num_type, quant_mode). */
+typedef struct {
+  int32_t drop_pad;         /* 0 dropless, 1 pad/drop every expert to expert_capacity rows */
+  int32_t expert_capacity;  /* C, used when drop_pad == 1 */
+  int32_t row_idx_type;     /* 0 gather form (default), 1 scatter form */
+  int32_t tokens_num_type;  /* 0 inclusive cumsum (default), 1 count; 2 (key_value) unsupported */
+  int32_t quant_mode;       /* -1 no quant (bf16 rows), 1 dynamic int8; 0 (static) unsupported */
+} moe_routing_opts_t;
+
+/* Init-routing alone ("npu_moe_init_routing_v2", formulas 1-5):
+ *   x [num_rows, hidden] bf16; expert_ids [num_rows, k] int32;
+ *   expanded_x: dropless [num_rows*k, hidden], drop/pad [E*C, hidden]
+ *     (int8 when quant_mode == 1, else bf16); rows of valid pairs in expert-
+ *     sorted order; drop/pad slots beyond an expert's count are zero;
+ *   expanded_row_idx [num_rows*k] int32: gather form out[sortedRowIdx[i]] = i
+ *     (drop/pad: e*C + rank, -1 for dropped or invalid pairs), or scatter form
+ *     out[i] = sortedRowIdx[i] (-1 past the valid count);
+ *   tokens_cumsum_or_count [E] int32 (not clipped by the capacity);
+ *   expanded_scale [rows of expanded_x] fp32 (quant_mode 1, else may be NULL):
+ *     row_max(|x|)/127 of the source row, 0 on unfilled slots.
+ * The sort is stable (ties by flat row index t*k+j).  ws: a workspace of
+ * moe_workspace_size(shape) for at least num_rows tokens (shape.inter is
+ * used only for that size), prepared for num_rows. */
+moe_status_t moe_init_routing(const moe_shape_t* shape, int64_t num_rows, const void* x, const int32_t* expert_ids,
+                              const moe_routing_opts_t* opts, void* expanded_x, int32_t* expanded_row_idx,
+                              int32_t* tokens_cumsum_or_count, float* expanded_scale, void* ws, size_t ws_bytes,
+                              cudaStream_t stream);
+
+/* Test helper: synchronizes `stream`, copies the device status word and the
+ * count of skipped expert ids to host_status[0..1] (HOST pointer) and clears
+ * them.  Returns MOE_ERR_DEVICE_STATUS if the status word was non-zero. */
+moe_status_t moe_read_status(const void* ws, int32_t* host_status, cudaStream_t stream);
+
+/* Human-readable name of a status code (static string). */
+const char* moe_status_string(moe_status_t status);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* NVFP4MOE_H_ */

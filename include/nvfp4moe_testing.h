@@ -1,0 +1,81 @@
+/*
+ * nvfp4moe_testing.h -- test and inspection entry points of libnvfp4moe.so.
+ *
+ * These run the same device functions as the forward (the NVFP4 group
+ * quantizer, the SiTU + requant epilogue, the hardware FP4/FP8 conversions,
+ * the block-scaled tcgen05 MMA with the forward's operand staging) on
+ * caller-given inputs, so that each step can be checked in isolation against
+ * an independent implementation.  Same conventions as nvfp4moe.h: device
+ * pointers unless marked "host", caller-owned memory, asynchronous on
+ * `stream`, host validation errors returned synchronously.
+ */
+#ifndef NVFP4MOE_TESTING_H_
+#define NVFP4MOE_TESTING_H_
+
+#include "nvfp4moe.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Hardware conversions over n consecutive fp32 bit patterns start..start+n-1:
+ *   e2m1_lo[i] = cvt.rn.satfinite.e2m1x2 with the value in the low nibble (4-bit code),
+ *   e2m1_hi[i] = the same conversion with the value in the high nibble (4-bit code),
+ *   e4m3[i]    = cvt.rn.satfinite.e4m3x2 of the value (byte).
+ * Any output may be NULL.  start + n <= 2^32. */
+moe_status_t moe_test_codec_sweep(uint32_t start, int64_t n, uint8_t* e2m1_lo, uint8_t* e2m1_hi, uint8_t* e4m3,
+                                  cudaStream_t stream);
+
+/* Group-16 NVFP4 quantization of fp32 rows ("Cake SiTU backend": group-16
+ * NVFP4 with an encode scale) with the device quantizer of the forward:
+ *   x [rows, cols] fp32 (cols % 16 == 0), q_per_row [rows] fp32 encode scales;
+ *   packed [rows, cols/2] (even element in the low nibble), sf [rows, cols/16]. */
+moe_status_t moe_test_quantize_rows(const float* x, int64_t rows, int32_t cols, const float* q_per_row,
+                                    uint8_t* packed, uint8_t* sf, cudaStream_t stream);
+
+/* The FC1 epilogue's SiTU + requant on given pre-activations ("Cake SiTU
+ * backend": SiTU, intermediate NVFP4 requantization):
+ *   z [rows, 2I] fp32 rows of [g | u] (already multiplied by dX*dW13);
+ *   a_out [rows, I] fp32 SiTU outputs; packed [rows, I/2]; sf [rows, I/16].
+ * I % 32 == 0. */
+moe_status_t moe_test_situ_requant(const float* z, int64_t rows, int32_t inter, float qA, float beta, float lam,
+                                   float* a_out, uint8_t* packed, uint8_t* sf, cudaStream_t stream);
+
+/* The FC1 epilogue's requant alone (one value per lane, 16-lane groups) on
+ * given activations act [rows, I] fp32 with encode scale qA:
+ * packed [rows, I/2], sf [rows, I/16].  I % 32 == 0. */
+moe_status_t moe_test_requant_lanes(const float* act, int64_t rows, int32_t inter, float qA, uint8_t* packed,
+                                    uint8_t* sf, cudaStream_t stream);
+
+/* One block-scaled FP4 tile product on tcgen05 with the operand staging of
+ * FC1 (kind::mxf4nvf4, 16-element E4M3 scales, 128B-swizzled K-major tiles):
+ *   a [128, k/2] packed E2M1 (even element in the low nibble), b [n, k/2];
+ *   sfa_atoms / sfb_atoms: their block scales in the 128x4 atom layout of
+ *   the "Nvfp4 Tensor" page (k/64 atoms of 512 B, rows padded to 128);
+ *   d [128, n] fp32 = sum_k a*sfa * b*sfb;  status [1] device status word.
+ * 1 <= n <= 128, k % 256 == 0; a, b 256-byte aligned. */
+moe_status_t moe_test_mma_fp4(const uint8_t* a, const uint8_t* sfa_atoms, const uint8_t* b, const uint8_t* sfb_atoms,
+                              int32_t n, int32_t k, float* d, int32_t* status, cudaStream_t stream);
+
+/* Byte offsets of the internal workspace regions of a workspace of ws_bytes
+ * (its carve-up depends only on the shape and its size), for inspection of
+ * intermediates in tests (host out struct).  Routing arrays are int32;
+ * xq/aq are packed codes of padded expanded rows ([rows, H/2] / [rows, I/2]);
+ * sfx/sfa are their block scales in the 128x4 atom layout; row_pos maps a
+ * flat pair t*k+j to its padded row. */
+typedef struct {
+  int64_t max_tokens, pairs_max, padded_rows_max, tiles_max;
+  int64_t header, count, cumsum, offs, poffs, sorted_row, gather, row_pos, prow_pair, tt_list;
+  int64_t xq, sfx, aq, sfa, out_f32, total;
+} moe_ws_layout_t;
+
+moe_status_t moe_workspace_layout(const moe_shape_t* shape, size_t ws_bytes, moe_ws_layout_t* layout);
+
+/* Number of kernel launches one moe_forward enqueues for this shape and T
+ * (host out). */
+moe_status_t moe_forward_launch_count(const moe_shape_t* shape, int64_t num_tokens, int32_t* launches);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* NVFP4MOE_TESTING_H_ */

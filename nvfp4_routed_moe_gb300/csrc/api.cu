@@ -1,0 +1,585 @@
+// api.cu -- the C ABI: host validation, workspace planning, tensor maps and
+// the launch sequence of the forward and of the standalone init-routing.
+#include <algorithm>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "nvfp4moe.h"
+#include "nvfp4moe_testing.h"
+#include "plan.h"
+#include "ptx.cuh"
+
+namespace moe {
+
+// launchers defined next to their kernels
+cudaError_t launch_routing(const RouteArgs& a, cudaStream_t st, int* launches);
+cudaError_t routing_set_attributes(int E);
+cudaError_t launch_init_move(const InitMoveArgs& a, cudaStream_t st);
+cudaError_t launch_init_finish(const InitFinishArgs& a, cudaStream_t st, int num_sms);
+cudaError_t launch_quant_x(const QuantXArgs& a, cudaStream_t st);
+cudaError_t launch_finalize(const float* acc, uint16_t* out, int64_t n, int num_sms, cudaStream_t st);
+cudaError_t launch_prep(const PrepArgs& a, cudaStream_t st, int num_sms);
+cudaError_t launch_codec_sweep(uint32_t start, int64_t n, uint8_t* lo, uint8_t* hi, uint8_t* e4, cudaStream_t st,
+                               int num_sms);
+cudaError_t launch_quant_rows(const float* x, int64_t rows, int cols, const float* qpr, uint8_t* packed, uint8_t* sf,
+                              cudaStream_t st, int num_sms);
+cudaError_t launch_situ_requant(const float* z, int64_t rows, int I, float qA, float beta, float lam, float* a_out,
+                                uint8_t* packed, uint8_t* sf, cudaStream_t st);
+cudaError_t launch_requant_lanes(const float* act, int64_t rows, int I, float qA, uint8_t* packed, uint8_t* sf,
+                                 cudaStream_t st);
+cudaError_t gemm_set_attributes();
+cudaError_t launch_fc1(const CUtensorMap& w13, const CUtensorMap& xq, const Fc1Args& a, int grid, cudaStream_t st);
+cudaError_t launch_fc2(const CUtensorMap& w2, const CUtensorMap& aq, const Fc2Args& a, int grid, cudaStream_t st);
+cudaError_t launch_mma_check(const CUtensorMap& a, const CUtensorMap& b, const uint8_t* sfa, const uint8_t* sfb,
+                             int N, int K, float* d, int32_t* status, cudaStream_t st);
+
+__global__ void fill_f32_kernel(float* p, int n, float v) {
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) p[i] = v;
+}
+
+// Programmatic dependent launch: a kernel may be scheduled while its
+// predecessor drains; every kernel of this library waits (griddepcontrol.wait)
+// before it touches memory the predecessor writes.  NVFP4MOE_PDL=0 turns the
+// attribute off.
+static bool pdl_enabled() {
+  static const bool on = [] {
+    const char* v = std::getenv("NVFP4MOE_PDL");
+    return !(v && v[0] == '0');
+  }();
+  return on;
+}
+
+cudaError_t launch_with_pdl(const void* fn, dim3 grid, dim3 block, size_t smem, cudaStream_t st, void** args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl_enabled() ? 1 : 0;
+  return cudaLaunchKernelExC(&cfg, fn, args);
+}
+
+// ------------------------------------------------------------ device state
+struct DeviceInfo {
+  int sms = 0;
+  bool attrs = false;
+};
+static std::mutex g_mu;
+static DeviceInfo g_dev[64];
+
+static cudaError_t device_ready(int* sms) {
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceInfo& d = g_dev[dev];
+  if (!d.attrs) {
+    err = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
+    if (err != cudaSuccess) return err;
+    err = routing_set_attributes(kMaxExperts);
+    if (err != cudaSuccess) return err;
+    err = gemm_set_attributes();
+    if (err != cudaSuccess) return err;
+    d.attrs = true;
+  }
+  *sms = d.sms;
+  return cudaSuccess;
+}
+
+// ------------------------------------------------------------ tensor maps
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+static bool make_map(CUtensorMap* m, const void* base, int rank, const uint64_t* dims, const uint64_t* strides,
+                     const uint32_t* box, CUtensorMapSwizzle sw) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t d[3], s[2];
+  cuuint32_t b[3], es[3] = {1, 1, 1};
+  for (int i = 0; i < rank; ++i) {
+    d[i] = dims[i];
+    b[i] = box[i];
+  }
+  for (int i = 0; i < rank - 1; ++i) s[i] = strides[i];
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, (cuuint32_t)rank, const_cast<void*>(base), d, s, b, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// ------------------------------------------------------------ validation
+static bool shape_ok(const moe_shape_t* s) {
+  return s && s->hidden > 0 && s->inter > 0 && s->num_experts > 0 && s->top_k > 0;
+}
+static moe_status_t shape_supported(const moe_shape_t* s) {
+  if (!shape_ok(s)) return MOE_ERR_INVALID_ARG;
+  if (s->hidden % 256 != 0 || s->inter % 128 != 0) return MOE_ERR_UNSUPPORTED;
+  if (s->num_experts > kMaxExperts || s->top_k > kMaxTopK || s->top_k > s->num_experts) return MOE_ERR_UNSUPPORTED;
+  if ((int64_t)s->hidden * s->top_k > (int64_t)1 << 30) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+static Shape to_shape(const moe_shape_t* s) { return Shape{s->hidden, s->inter, s->num_experts, s->top_k}; }
+
+// Largest token count whose layout fits in `bytes` (the carve-up of a
+// workspace is a function of its size, so every call on it agrees).
+static int64_t capacity_tokens(const Shape& s, size_t bytes) {
+  int64_t lo = 0, hi = 1;
+  while (hi < ((int64_t)1 << 31) / s.k && make_layout(s, hi).total <= bytes) {
+    lo = hi;
+    hi *= 2;
+  }
+  while (hi - lo > 1) {
+    const int64_t mid = (lo + hi) / 2;
+    if (make_layout(s, mid).total <= bytes) lo = mid;
+    else hi = mid;
+  }
+  return lo;
+}
+
+struct PreparedEntry {
+  const void* ws;
+  size_t bytes;
+  int64_t T;
+  Shape shape;
+};
+static std::vector<PreparedEntry> g_prepared;
+
+static bool is_prepared(const void* ws, size_t bytes, int64_t T, const Shape& s) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  for (const auto& p : g_prepared)
+    if (p.ws == ws && p.bytes == bytes && p.T == T && p.shape.H == s.H && p.shape.I == s.I && p.shape.E == s.E &&
+        p.shape.k == s.k)
+      return true;
+  return false;
+}
+
+static bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+#define MOE_CUDA(x)                              \
+  do {                                           \
+    if ((x) != cudaSuccess) return MOE_ERR_CUDA; \
+  } while (0)
+
+static RouteArgs route_args(const Shape& s, const WsLayout& L, uint8_t* ws, const int32_t* ids, int64_t T) {
+  RouteArgs a{};
+  a.ids = ids;
+  a.P = T * s.k;
+  a.k = s.k;
+  a.E = s.E;
+  a.hdr = reinterpret_cast<int32_t*>(ws + L.header);
+  a.count = reinterpret_cast<int32_t*>(ws + L.count);
+  a.cumsum = reinterpret_cast<int32_t*>(ws + L.cumsum);
+  a.offs = reinterpret_cast<int32_t*>(ws + L.offs);
+  a.poffs = reinterpret_cast<int32_t*>(ws + L.poffs);
+  a.ttoffs = reinterpret_cast<int32_t*>(ws + L.ttoffs);
+  a.sorted_row = reinterpret_cast<int32_t*>(ws + L.sorted_row);
+  a.gather = reinterpret_cast<int32_t*>(ws + L.gather);
+  a.row_pos = reinterpret_cast<int32_t*>(ws + L.row_pos);
+  a.prow_pair = reinterpret_cast<int32_t*>(ws + L.prow_pair);
+  a.tt_list = reinterpret_cast<int32_t*>(ws + L.tt_list);
+  a.blockhist = reinterpret_cast<int32_t*>(ws + L.blockhist);
+  a.nblk = (int32_t)((a.P + kRouteChunk - 1) / kRouteChunk);
+  return a;
+}
+
+static int forward_launches(int64_t P) { return (P <= kRouteSmallMax ? 1 : 2) + 4; }
+
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+const char* moe_status_string(moe_status_t st) {
+  switch (st) {
+    case MOE_OK: return "MOE_OK";
+    case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG";
+    case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED";
+    case MOE_ERR_WORKSPACE_TOO_SMALL: return "MOE_ERR_WORKSPACE_TOO_SMALL";
+    case MOE_ERR_NOT_PREPARED: return "MOE_ERR_NOT_PREPARED";
+    case MOE_ERR_CUDA: return "MOE_ERR_CUDA";
+    case MOE_ERR_DEVICE_STATUS: return "MOE_ERR_DEVICE_STATUS";
+  }
+  return "MOE_ERR_UNKNOWN";
+}
+
+moe_status_t moe_workspace_size(const moe_shape_t* shape, int64_t max_tokens, size_t* bytes) {
+  moe_status_t st = shape_supported(shape);
+  if (st != MOE_OK) return st;
+  if (!bytes || max_tokens < 1) return MOE_ERR_INVALID_ARG;
+  if (max_tokens * shape->top_k >= ((int64_t)1 << 31) - (int64_t)kTileRows * kMaxExperts)
+    return MOE_ERR_UNSUPPORTED;
+  *bytes = make_layout(to_shape(shape), max_tokens).total;
+  return MOE_OK;
+}
+
+moe_status_t moe_prepared_weight_bytes(const moe_shape_t* shape, size_t* w13_bytes, size_t* sf13_bytes,
+                                       size_t* w2_bytes, size_t* sf2_bytes) {
+  moe_status_t st = shape_supported(shape);
+  if (st != MOE_OK) return st;
+  if (!w13_bytes || !sf13_bytes || !w2_bytes || !sf2_bytes) return MOE_ERR_INVALID_ARG;
+  const size_t E = shape->num_experts, H = shape->hidden, I = shape->inter;
+  *w13_bytes = E * 2 * I * (H / 2);
+  *sf13_bytes = E * 2 * I * (H / 16);
+  *w2_bytes = E * H * (I / 2);
+  *sf2_bytes = E * H * (I / 16);
+  return MOE_OK;
+}
+
+moe_status_t moe_prepare_weights(const moe_shape_t* shape, const uint8_t* w13, const uint8_t* sf13,
+                                 const uint8_t* w2, const uint8_t* sf2, uint8_t* w13_out, uint8_t* sf13_out,
+                                 uint8_t* w2_out, uint8_t* sf2_out, cudaStream_t stream) {
+  moe_status_t st = shape_supported(shape);
+  if (st != MOE_OK) return st;
+  if (!w13 || !sf13 || !w2 || !sf2 || !w13_out || !sf13_out || !w2_out || !sf2_out) return MOE_ERR_INVALID_ARG;
+  if (!aligned(w13, 16) || !aligned(w2, 16) || !aligned(w13_out, 256) || !aligned(w2_out, 256) ||
+      !aligned(sf13_out, 16) || !aligned(sf2_out, 16))
+    return MOE_ERR_INVALID_ARG;
+  int sms = 0;
+  MOE_CUDA(device_ready(&sms));
+  PrepArgs a{w13, sf13, w2, sf2, w13_out, sf13_out, w2_out, sf2_out, shape->hidden, shape->inter,
+             shape->num_experts};
+  MOE_CUDA(launch_prep(a, stream, sms));
+  return MOE_OK;
+}
+
+moe_status_t moe_prepare_workspace(const moe_shape_t* shape, void* ws, size_t ws_bytes, int64_t num_tokens,
+                                   cudaStream_t stream) {
+  moe_status_t st = shape_supported(shape);
+  if (st != MOE_OK) return st;
+  if (!ws || num_tokens < 1 || !aligned(ws, 256)) return MOE_ERR_INVALID_ARG;
+  const Shape s = to_shape(shape);
+  const int64_t cap = capacity_tokens(s, ws_bytes);
+  if (cap < num_tokens) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  const WsLayout L = make_layout(s, cap);
+  int sms = 0;
+  MOE_CUDA(device_ready(&sms));
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  MOE_CUDA(cudaMemsetAsync(w + L.header, 0, HDR_WORDS * 4, stream));
+  fill_f32_kernel<<<4, 256, 0, stream>>>(reinterpret_cast<float*>(w + L.beta_def), s.E, 4.0f);
+  fill_f32_kernel<<<4, 256, 0, stream>>>(reinterpret_cast<float*>(w + L.lam_def), s.E, 25.0f);
+  MOE_CUDA(cudaGetLastError());
+  if (!is_prepared(ws, ws_bytes, num_tokens, s)) {
+    std::lock_guard<std::mutex> lock(g_mu);
+    g_prepared.push_back(PreparedEntry{ws, ws_bytes, num_tokens, s});
+  }
+  return MOE_OK;
+}
+
+moe_status_t moe_forward(const moe_shape_t* shape, int64_t num_tokens, const void* x, const int32_t* expert_ids,
+                         const void* route_weights, const uint8_t* w13, const uint8_t* sf13, const uint8_t* w2,
+                         const uint8_t* sf2, const float* qX, const float* dX_dW13, const float* qA,
+                         const float* dA_dW2, const float* situ_beta, const float* situ_linear_beta, void* ws,
+                         size_t ws_bytes, void* out, cudaStream_t stream) {
+  moe_status_t st = shape_supported(shape);
+  if (st != MOE_OK) return st;
+  if (!x || !expert_ids || !route_weights || !w13 || !sf13 || !w2 || !sf2 || !qX || !dX_dW13 || !qA || !dA_dW2 ||
+      !ws || !out || num_tokens < 1)
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(out, 16) || !aligned(ws, 256) || !aligned(w13, 256) || !aligned(w2, 256) ||
+      !aligned(sf13, 16) || !aligned(sf2, 16))
+    return MOE_ERR_INVALID_ARG;
+  const Shape s = to_shape(shape);
+  const int64_t cap = capacity_tokens(s, ws_bytes);
+  if (cap < num_tokens) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  if (!is_prepared(ws, ws_bytes, num_tokens, s)) return MOE_ERR_NOT_PREPARED;
+  const WsLayout L = make_layout(s, cap);
+  int sms = 0;
+  MOE_CUDA(device_ready(&sms));
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  const int64_t T = num_tokens, P = T * s.k;
+  const int NIT = s.I / 128, NKB = s.H / kFc1KBlock, NMT = s.H / 128, NKB2 = s.I / kFc2KBlock;
+
+  CUtensorMap tm_w13, tm_xq, tm_w2, tm_aq;
+  {
+    const uint64_t d[3] = {128, 256, (uint64_t)s.E * NIT * NKB};
+    const uint64_t str[2] = {128, 32768};
+    const uint32_t box[3] = {128, 256, 1};
+    if (!make_map(&tm_w13, w13, 3, d, str, box, CU_TENSOR_MAP_SWIZZLE_128B)) return MOE_ERR_CUDA;
+  }
+  {
+    const uint64_t d[2] = {(uint64_t)s.H / 2, (uint64_t)L.PpadMax};
+    const uint64_t str[1] = {(uint64_t)s.H / 2};
+    const uint32_t box[2] = {128, (uint32_t)kTokChunk};
+    if (!make_map(&tm_xq, w + L.xq, 2, d, str, box, CU_TENSOR_MAP_SWIZZLE_128B)) return MOE_ERR_CUDA;
+  }
+  {
+    const uint64_t d[3] = {64, 128, (uint64_t)s.E * NMT * NKB2};
+    const uint64_t str[2] = {64, 8192};
+    const uint32_t box[3] = {64, 128, 1};
+    if (!make_map(&tm_w2, w2, 3, d, str, box, CU_TENSOR_MAP_SWIZZLE_64B)) return MOE_ERR_CUDA;
+  }
+  {
+    const uint64_t d[2] = {(uint64_t)s.I / 2, (uint64_t)L.PpadMax};
+    const uint64_t str[1] = {(uint64_t)s.I / 2};
+    const uint32_t box[2] = {64, (uint32_t)kTokChunk};
+    if (!make_map(&tm_aq, w + L.aq, 2, d, str, box, CU_TENSOR_MAP_SWIZZLE_64B)) return MOE_ERR_CUDA;
+  }
+
+  // 1. routing
+  RouteArgs ra = route_args(s, L, w, expert_ids, T);
+  int nl = 0;
+  MOE_CUDA(launch_routing(ra, stream, &nl));
+
+  // 2. quantize X into the padded expanded rows, zero the fp32 accumulator
+  QuantXArgs qa{};
+  qa.x = static_cast<const uint16_t*>(x);
+  qa.row_pos = ra.row_pos;
+  qa.qX = qX;
+  qa.xq = w + L.xq;
+  qa.sfx = w + L.sfx;
+  qa.out_f32 = reinterpret_cast<float*>(w + L.out_f32);
+  qa.T = T;
+  qa.H = s.H;
+  qa.k = s.k;
+  qa.max_rows = L.PpadMax;
+  MOE_CUDA(launch_quant_x(qa, stream));
+
+  // 3. FC1 + SiTU + requant
+  const int64_t tt = tt_bound(P, s.E);
+  Fc1Args f1{};
+  f1.sf13p = sf13;
+  f1.sfx = w + L.sfx;
+  f1.tt_list = ra.tt_list;
+  f1.hdr = ra.hdr;
+  f1.dXdW13 = dX_dW13;
+  f1.qA = qA;
+  f1.beta = situ_beta ? situ_beta : reinterpret_cast<const float*>(w + L.beta_def);
+  f1.lam = situ_linear_beta ? situ_linear_beta : reinterpret_cast<const float*>(w + L.lam_def);
+  f1.aq = w + L.aq;
+  f1.sfa = w + L.sfa;
+  f1.status = ra.hdr + HDR_STATUS;
+  f1.H = s.H;
+  f1.I = s.I;
+  f1.E = s.E;
+  f1.max_tiles = (int32_t)L.TTmax;
+  f1.max_rows = L.PpadMax;
+  const int grid1 = (int)std::min<int64_t>(sms, tt * NIT);
+  MOE_CUDA(launch_fc1(tm_w13, tm_xq, f1, grid1, stream));
+
+  // 4. FC2 + weighted combine into the fp32 accumulator
+  Fc2Args f2{};
+  f2.sf2p = sf2;
+  f2.sfa = w + L.sfa;
+  f2.tt_list = ra.tt_list;
+  f2.hdr = ra.hdr;
+  f2.prow_pair = ra.prow_pair;
+  f2.route_w = static_cast<const uint16_t*>(route_weights);
+  f2.dAdW2 = dA_dW2;
+  f2.out_f32 = reinterpret_cast<float*>(w + L.out_f32);
+  f2.status = ra.hdr + HDR_STATUS;
+  f2.H = s.H;
+  f2.I = s.I;
+  f2.E = s.E;
+  f2.k = s.k;
+  f2.max_tiles = (int32_t)L.TTmax;
+  f2.max_rows = L.PpadMax;
+  f2.num_pairs = P;
+  const int grid2 = (int)std::min<int64_t>(sms, tt * NMT);
+  MOE_CUDA(launch_fc2(tm_w2, tm_aq, f2, grid2, stream));
+
+  // 5. BF16 finalize
+  MOE_CUDA(launch_finalize(reinterpret_cast<const float*>(w + L.out_f32), static_cast<uint16_t*>(out), T * s.H, sms,
+                           stream));
+  return MOE_OK;
+}
+
+moe_status_t moe_init_routing(const moe_shape_t* shape, int64_t num_rows, const void* x, const int32_t* expert_ids,
+                              const moe_routing_opts_t* opts, void* expanded_x, int32_t* expanded_row_idx,
+                              int32_t* tokens_cumsum_or_count, float* expanded_scale, void* ws, size_t ws_bytes,
+                              cudaStream_t stream) {
+  moe_status_t st = shape_supported(shape);
+  if (st != MOE_OK) return st;
+  if (!x || !expert_ids || !opts || !expanded_x || !expanded_row_idx || !tokens_cumsum_or_count || !ws ||
+      num_rows < 1)
+    return MOE_ERR_INVALID_ARG;
+  if (opts->drop_pad != 0 && opts->drop_pad != 1) return MOE_ERR_INVALID_ARG;
+  if (opts->drop_pad && opts->expert_capacity < 1) return MOE_ERR_INVALID_ARG;
+  if (opts->row_idx_type != 0 && opts->row_idx_type != 1) return MOE_ERR_INVALID_ARG;
+  if (opts->tokens_num_type == 2 || opts->quant_mode == 0) return MOE_ERR_UNSUPPORTED;
+  if (opts->tokens_num_type != 0 && opts->tokens_num_type != 1) return MOE_ERR_INVALID_ARG;
+  if (opts->quant_mode != -1 && opts->quant_mode != 1) return MOE_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(expanded_x, 16) || !aligned(ws, 256)) return MOE_ERR_INVALID_ARG;
+  const Shape s = to_shape(shape);
+  const int64_t cap = capacity_tokens(s, ws_bytes);
+  if (cap < num_rows) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  if (!is_prepared(ws, ws_bytes, num_rows, s)) return MOE_ERR_NOT_PREPARED;
+  const WsLayout L = make_layout(s, cap);
+  int sms = 0;
+  MOE_CUDA(device_ready(&sms));
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  RouteArgs ra = route_args(s, L, w, expert_ids, num_rows);
+  int nl = 0;
+  MOE_CUDA(launch_routing(ra, stream, &nl));
+  InitMoveArgs ma{};
+  ma.x = static_cast<const uint16_t*>(x);
+  ma.ids = expert_ids;
+  ma.gather = ra.gather;
+  ma.offs = ra.offs;
+  ma.T = num_rows;
+  ma.k = s.k;
+  ma.E = s.E;
+  ma.H = s.H;
+  ma.drop_pad = opts->drop_pad;
+  ma.C = opts->expert_capacity;
+  ma.quant_mode = opts->quant_mode;
+  ma.row_idx_type = opts->row_idx_type;
+  ma.expanded_x = expanded_x;
+  ma.expanded_scale = opts->quant_mode == 1 ? expanded_scale : nullptr;
+  ma.expanded_row_idx = expanded_row_idx;
+  MOE_CUDA(launch_init_move(ma, stream));
+  InitFinishArgs fa{};
+  fa.count = ra.count;
+  fa.cumsum = ra.cumsum;
+  fa.sorted_row = ra.sorted_row;
+  fa.P = ra.P;
+  fa.E = s.E;
+  fa.H = s.H;
+  fa.C = opts->expert_capacity;
+  fa.drop_pad = opts->drop_pad;
+  fa.row_idx_type = opts->row_idx_type;
+  fa.tokens_num_type = opts->tokens_num_type;
+  fa.esize = opts->quant_mode == 1 ? 1 : 2;
+  fa.expanded_x = expanded_x;
+  fa.expanded_scale = ma.expanded_scale;
+  fa.expanded_row_idx = expanded_row_idx;
+  fa.tokens_out = tokens_cumsum_or_count;
+  MOE_CUDA(launch_init_finish(fa, stream, sms));
+  return MOE_OK;
+}
+
+moe_status_t moe_read_status(const void* ws, int32_t* host_status, cudaStream_t stream) {
+  if (!ws || !host_status) return MOE_ERR_INVALID_ARG;
+  int32_t h[2] = {0, 0};
+  MOE_CUDA(cudaMemcpyAsync(h, ws, sizeof(h), cudaMemcpyDeviceToHost, stream));
+  MOE_CUDA(cudaStreamSynchronize(stream));
+  MOE_CUDA(cudaMemsetAsync(const_cast<void*>(ws), 0, sizeof(h), stream));
+  MOE_CUDA(cudaStreamSynchronize(stream));
+  host_status[0] = h[0];
+  host_status[1] = h[1];
+  return h[0] ? MOE_ERR_DEVICE_STATUS : MOE_OK;
+}
+
+moe_status_t moe_test_codec_sweep(uint32_t start, int64_t n, uint8_t* e2m1_lo, uint8_t* e2m1_hi, uint8_t* e4m3,
+                                  cudaStream_t stream) {
+  if (n < 0 || (uint64_t)start + (uint64_t)n > ((uint64_t)1 << 32)) return MOE_ERR_INVALID_ARG;
+  if (n == 0) return MOE_OK;
+  int sms = 0;
+  MOE_CUDA(device_ready(&sms));
+  MOE_CUDA(launch_codec_sweep(start, n, e2m1_lo, e2m1_hi, e4m3, stream, sms));
+  return MOE_OK;
+}
+
+moe_status_t moe_test_quantize_rows(const float* x, int64_t rows, int32_t cols, const float* q_per_row,
+                                    uint8_t* packed, uint8_t* sf, cudaStream_t stream) {
+  if (!x || !q_per_row || !packed || !sf || rows < 0 || cols <= 0 || cols % 16 != 0) return MOE_ERR_INVALID_ARG;
+  if (!aligned(packed, 8)) return MOE_ERR_INVALID_ARG;
+  if (rows == 0) return MOE_OK;
+  int sms = 0;
+  MOE_CUDA(device_ready(&sms));
+  MOE_CUDA(launch_quant_rows(x, rows, cols, q_per_row, packed, sf, stream, sms));
+  return MOE_OK;
+}
+
+moe_status_t moe_test_situ_requant(const float* z, int64_t rows, int32_t inter, float qA, float beta, float lam,
+                                   float* a_out, uint8_t* packed, uint8_t* sf, cudaStream_t stream) {
+  if (!z || !a_out || !packed || !sf || rows < 0 || inter <= 0 || inter % 32 != 0) return MOE_ERR_INVALID_ARG;
+  if (!aligned(packed, 4)) return MOE_ERR_INVALID_ARG;
+  if (rows == 0) return MOE_OK;
+  int sms = 0;
+  MOE_CUDA(device_ready(&sms));
+  MOE_CUDA(launch_situ_requant(z, rows, inter, qA, beta, lam, a_out, packed, sf, stream));
+  return MOE_OK;
+}
+
+moe_status_t moe_test_requant_lanes(const float* act, int64_t rows, int32_t inter, float qA, uint8_t* packed,
+                                    uint8_t* sf, cudaStream_t stream) {
+  if (!act || !packed || !sf || rows < 0 || inter <= 0 || inter % 32 != 0) return MOE_ERR_INVALID_ARG;
+  if (!aligned(packed, 4)) return MOE_ERR_INVALID_ARG;
+  if (rows == 0) return MOE_OK;
+  int sms = 0;
+  MOE_CUDA(device_ready(&sms));
+  MOE_CUDA(launch_requant_lanes(act, rows, inter, qA, packed, sf, stream));
+  return MOE_OK;
+}
+
+moe_status_t moe_test_mma_fp4(const uint8_t* a, const uint8_t* sfa_atoms, const uint8_t* b, const uint8_t* sfb_atoms,
+                              int32_t n, int32_t k, float* d, int32_t* status, cudaStream_t stream) {
+  if (!a || !sfa_atoms || !b || !sfb_atoms || !d || !status) return MOE_ERR_INVALID_ARG;
+  if (n < 1 || n > 128 || k < 256 || k % 256 != 0) return MOE_ERR_INVALID_ARG;
+  if (!aligned(a, 256) || !aligned(b, 256) || !aligned(sfa_atoms, 16) || !aligned(sfb_atoms, 16))
+    return MOE_ERR_INVALID_ARG;
+  int sms = 0;
+  MOE_CUDA(device_ready(&sms));
+  CUtensorMap ta, tb;
+  const uint64_t da[2] = {(uint64_t)k / 2, 128}, db[2] = {(uint64_t)k / 2, (uint64_t)n};
+  const uint64_t str[1] = {(uint64_t)k / 2};
+  const uint32_t ba[2] = {128, 128}, bb[2] = {128, 16};
+  if (!make_map(&ta, a, 2, da, str, ba, CU_TENSOR_MAP_SWIZZLE_128B)) return MOE_ERR_CUDA;
+  if (!make_map(&tb, b, 2, db, str, bb, CU_TENSOR_MAP_SWIZZLE_128B)) return MOE_ERR_CUDA;
+  MOE_CUDA(launch_mma_check(ta, tb, sfa_atoms, sfb_atoms, n, k, d, status, stream));
+  return MOE_OK;
+}
+
+moe_status_t moe_workspace_layout(const moe_shape_t* shape, size_t ws_bytes, moe_ws_layout_t* out) {
+  moe_status_t st = shape_supported(shape);
+  if (st != MOE_OK) return st;
+  if (!out) return MOE_ERR_INVALID_ARG;
+  const Shape s = to_shape(shape);
+  const int64_t cap = capacity_tokens(s, ws_bytes);
+  if (cap < 1) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  const WsLayout L = make_layout(s, cap);
+  out->max_tokens = L.max_tokens;
+  out->pairs_max = L.Pmax;
+  out->padded_rows_max = L.PpadMax;
+  out->tiles_max = L.TTmax;
+  out->header = (int64_t)L.header;
+  out->count = (int64_t)L.count;
+  out->cumsum = (int64_t)L.cumsum;
+  out->offs = (int64_t)L.offs;
+  out->poffs = (int64_t)L.poffs;
+  out->sorted_row = (int64_t)L.sorted_row;
+  out->gather = (int64_t)L.gather;
+  out->row_pos = (int64_t)L.row_pos;
+  out->prow_pair = (int64_t)L.prow_pair;
+  out->tt_list = (int64_t)L.tt_list;
+  out->xq = (int64_t)L.xq;
+  out->sfx = (int64_t)L.sfx;
+  out->aq = (int64_t)L.aq;
+  out->sfa = (int64_t)L.sfa;
+  out->out_f32 = (int64_t)L.out_f32;
+  out->total = (int64_t)L.total;
+  return MOE_OK;
+}
+
+moe_status_t moe_forward_launch_count(const moe_shape_t* shape, int64_t num_tokens, int32_t* launches) {
+  moe_status_t st = shape_supported(shape);
+  if (st != MOE_OK) return st;
+  if (!launches || num_tokens < 1) return MOE_ERR_INVALID_ARG;
+  *launches = forward_launches(num_tokens * shape->top_k);
+  return MOE_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,80 @@
+// nvfp4.cuh -- device-side NVFP4 group quantizer and SiTU, used by the X
+// quantization kernel, the FC1 epilogue and the test kernels alike.
+//
+// Group-16 quantization with encode scale q ("Cake SiTU backend": group-16
+// NVFP4, qX = 1/dX, qA = 1/dA; "Nvfp4 Tensor": the global scale is applied
+// after block dequantization):
+//   amax = max |v_j|;  sf = E4M3_rn_sat((amax * q) / 6);  S = value(sf);
+//   r = (S == 0) ? 0 : q / S;  code_j = E2M1_rn_sat(v_j * r).
+// Every fp32 step is a separately rounded intrinsic (no contraction), so the
+// codes are a deterministic function of the fp32 inputs.
+#pragma once
+#include "ptx.cuh"
+
+namespace moe {
+
+__device__ __forceinline__ uint32_t nvfp4_scale(float amax, float q, float& r) {
+  const float t = __fmul_rn(amax, q);
+  const float t6 = __fdiv_rn(t, 6.0f);
+  const uint32_t sf = cvt_e4m3(t6);
+  const float S = e4m3_to_f32(sf);
+  r = (S == 0.0f) ? 0.0f : __fdiv_rn(q, S);
+  return sf;
+}
+
+// One thread quantizes 16 values held in registers: 8 packed bytes (element
+// 2i in the low nibble of byte i) and the E4M3 block-scale byte.
+__device__ __forceinline__ uint32_t nvfp4_quant16(const float (&v)[16], float q, uint2& packed) {
+  float amax = 0.0f;
+#pragma unroll
+  for (int j = 0; j < 16; ++j) amax = fmaxf(amax, fabsf(v[j]));
+  float r;
+  const uint32_t sf = nvfp4_scale(amax, q, r);
+  uint32_t w[2] = {0u, 0u};
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const uint32_t b = cvt_e2m1x2(__fmul_rn(v[2 * i + 1], r), __fmul_rn(v[2 * i], r));
+    w[i >> 2] |= b << (8 * (i & 3));
+  }
+  packed = make_uint2(w[0], w[1]);
+  return sf;
+}
+
+// Lane-distributed form: each 16-lane half of the warp holds one group, one
+// value per lane (lane l holds element l % 16).  Returns the block-scale byte
+// (same in all 16 lanes of the group); `word` receives, in lanes with
+// lane % 8 == 0, the 4 packed bytes of elements lane .. lane+7.
+__device__ __forceinline__ uint32_t nvfp4_quant_lanes16(float a, float q, uint32_t& word) {
+  float amax = fabsf(a);
+#pragma unroll
+  for (int off = 8; off >= 1; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+  float r;
+  const uint32_t sf = nvfp4_scale(amax, q, r);
+  uint32_t v = cvt_e2m1x2(0.0f, __fmul_rn(a, r)) & 0xFu;
+  v |= (__shfl_down_sync(0xffffffffu, v, 1) & 0xFu) << 4;
+  v = (v & 0xFFu) | ((__shfl_down_sync(0xffffffffu, v, 2) & 0xFFu) << 8);
+  v = (v & 0xFFFFu) | ((__shfl_down_sync(0xffffffffu, v, 4) & 0xFFFFu) << 16);
+  word = v;
+  return sf;
+}
+
+// SiTU ("Cake SiTU backend": default (4*tanh(g/4)*sigmoid(g))*(25*tanh(u/25)),
+// per-expert gate and linear smoothing parameters beta, lambda).
+__device__ __forceinline__ float situ_f32(float g, float u, float beta, float lam) {
+  const float sig = 1.0f / (1.0f + expf(-g));
+  const float gate = beta * tanhf(g / beta) * sig;
+  const float lin = lam * tanhf(u / lam);
+  return gate * lin;
+}
+
+__device__ __forceinline__ float bf16_bits_to_f32(uint32_t b) { return __uint_as_float(b << 16); }
+
+// Byte offset of the block scale of (row, chunk) in the 128x4 atom layout
+// ("Nvfp4 Tensor", block_scale) for a matrix with `kchunks` 16-element chunks
+// per row (kchunks % 4 == 0).
+__device__ __forceinline__ size_t atom_offset(int64_t row, int chunk, int kchunks) {
+  return ((size_t)(row >> 7) * (size_t)(kchunks >> 2) + (size_t)(chunk >> 2)) * 512u + (size_t)(row & 31) * 16u +
+         (size_t)((row >> 5) & 3) * 4u + (size_t)(chunk & 3);
+}
+
+}  // namespace moe

@@ -1,0 +1,181 @@
+// plan.h -- internal: shape constants, workspace carve-up and the kernel
+// parameter blocks shared by the host launcher and the kernels.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+
+namespace moe {
+
+// Tile geometry (fixed by the kernels).
+constexpr int kTileRows = 128;      // weight rows per MMA (M) and token rows per tile
+constexpr int kFc1KBlock = 256;     // FP4 elements per FC1 k-block (128 B per row, 128B swizzle)
+constexpr int kFc2KBlock = 128;     // FP4 elements per FC2 k-sub-block (64 B per row, 64B swizzle)
+constexpr int kTokChunk = 16;       // rows per activation TMA box (and MMA N granule)
+constexpr int kRouteSmallMax = 4096;  // pairs handled by the one-CTA routing kernel
+constexpr int kRouteChunk = 4096;     // pairs per CTA of the multi-CTA routing kernels
+constexpr int kMaxExperts = 1024;
+constexpr int kMaxTopK = 32;
+
+// Workspace header words (int32).
+enum : int {
+  HDR_STATUS = 0,      // OR of DEVSTAT_* codes
+  HDR_INVALID = 1,     // count of skipped (out-of-range) expert ids
+  HDR_NUM_TT = 2,      // number of token tiles this call
+  HDR_PPAD = 3,        // padded rows this call
+  HDR_DONE = 4,        // last-arriver ticket of the multi-CTA routing
+  HDR_NVALID = 5,      // routed pairs this call
+  HDR_WORDS = 64,
+};
+
+struct Shape {
+  int32_t H, I, E, k;
+};
+
+// Byte offsets of every region of the workspace (all 1024-B aligned).
+struct WsLayout {
+  int64_t max_tokens, Pmax, PpadMax, TTmax, nblkMax;
+  size_t header, count, cumsum, offs, poffs, ttoffs;
+  size_t sorted_row, gather, row_pos, prow_pair, tt_list, blockhist;
+  size_t xq, sfx, aq, sfa, out_f32, beta_def, lam_def;
+  size_t total;
+};
+
+inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+inline int64_t tt_bound(int64_t P, int64_t E) {  // max token tiles for P pairs
+  return P / kTileRows + (P < E ? P : E);
+}
+
+inline WsLayout make_layout(const Shape& s, int64_t max_tokens) {
+  WsLayout L{};
+  L.max_tokens = max_tokens;
+  L.Pmax = max_tokens * s.k;
+  const int64_t padded = L.Pmax + (int64_t)(kTileRows - 1) * (L.Pmax < s.E ? L.Pmax : s.E);
+  L.PpadMax = (int64_t)align_up((size_t)padded, kTileRows);
+  L.TTmax = tt_bound(L.Pmax, s.E);
+  L.nblkMax = (L.Pmax + kRouteChunk - 1) / kRouteChunk;
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    size_t at = o;
+    o = align_up(o + (bytes ? bytes : 1), 1024);
+    return at;
+  };
+  L.header = take(HDR_WORDS * 4);
+  L.count = take((size_t)s.E * 4);
+  L.cumsum = take((size_t)s.E * 4);
+  L.offs = take((size_t)(s.E + 1) * 4);
+  L.poffs = take((size_t)(s.E + 1) * 4);
+  L.ttoffs = take((size_t)(s.E + 1) * 4);
+  L.sorted_row = take((size_t)L.Pmax * 4);
+  L.gather = take((size_t)L.Pmax * 4);
+  L.row_pos = take((size_t)L.Pmax * 4);
+  L.prow_pair = take((size_t)L.PpadMax * 4);
+  L.tt_list = take((size_t)L.TTmax * 16);
+  L.blockhist = take((size_t)L.nblkMax * s.E * 4);
+  L.xq = take((size_t)L.PpadMax * (s.H / 2));
+  L.sfx = take((size_t)(L.PpadMax / kTileRows) * (s.H / 64) * 512);
+  L.aq = take((size_t)L.PpadMax * (s.I / 2));
+  L.sfa = take((size_t)(L.PpadMax / kTileRows) * (s.I / 64) * 512);
+  L.out_f32 = take((size_t)max_tokens * s.H * 4);
+  L.beta_def = take((size_t)s.E * 4);
+  L.lam_def = take((size_t)s.E * 4);
+  L.total = o;
+  return L;
+}
+
+// Routing outputs (device pointers into the workspace).
+struct RouteArgs {
+  const int32_t* ids;
+  int64_t P;
+  int32_t k, E;
+  int32_t* hdr;
+  int32_t* count;
+  int32_t* cumsum;
+  int32_t* offs;
+  int32_t* poffs;
+  int32_t* ttoffs;
+  int32_t* sorted_row;
+  int32_t* gather;
+  int32_t* row_pos;
+  int32_t* prow_pair;
+  int32_t* tt_list;   // int4 {expert, row0, rows, 0}
+  int32_t* blockhist;
+  int32_t nblk;
+};
+
+struct Fc1Args {
+  const uint8_t* sf13p;
+  const uint8_t* sfx;
+  const int32_t* tt_list;
+  const int32_t* hdr;
+  const float* dXdW13;
+  const float* qA;
+  const float* beta;
+  const float* lam;
+  uint8_t* aq;
+  uint8_t* sfa;
+  int32_t* status;
+  int32_t H, I, E;
+  int32_t max_tiles;      // capacity of the tile list
+  int64_t max_rows;       // padded rows of the workspace
+};
+
+struct Fc2Args {
+  const uint8_t* sf2p;
+  const uint8_t* sfa;
+  const int32_t* tt_list;
+  const int32_t* hdr;
+  const int32_t* prow_pair;
+  const uint16_t* route_w;  // bf16 bits [T, k]
+  const float* dAdW2;
+  float* out_f32;
+  int32_t* status;
+  int32_t H, I, E, k;
+  int32_t max_tiles;
+  int64_t max_rows;
+  int64_t num_pairs;      // T * k of this call
+};
+
+struct InitMoveArgs {
+  const uint16_t* x;          // [T, H] bf16
+  const int32_t* ids;         // [T, k]
+  const int32_t* gather;      // dropless sorted position per flat pair (ws)
+  const int32_t* offs;        // [E] (ws)
+  int64_t T;
+  int32_t k, E, H, drop_pad, C, quant_mode, row_idx_type;
+  void* expanded_x;
+  float* expanded_scale;
+  int32_t* expanded_row_idx;
+};
+
+struct InitFinishArgs {
+  const int32_t* count;
+  const int32_t* cumsum;
+  const int32_t* sorted_row;
+  int64_t P;
+  int32_t E, H, C, drop_pad, row_idx_type, tokens_num_type, esize;
+  void* expanded_x;
+  float* expanded_scale;
+  int32_t* expanded_row_idx;
+  int32_t* tokens_out;
+};
+
+struct QuantXArgs {
+  const uint16_t* x;        // [T, H] bf16
+  const int32_t* row_pos;   // [T*k] padded expanded row of each pair, -1 if not routed
+  const float* qX;          // [1]
+  uint8_t* xq;              // [Ppad, H/2]
+  uint8_t* sfx;             // atom layout, H/16 chunks per row
+  float* out_f32;           // [T, H] accumulator, zeroed here for the FC2 combine
+  int64_t T;
+  int32_t H, k;
+  int64_t max_rows;         // padded rows of the workspace
+};
+
+struct PrepArgs {
+  const uint8_t *w13, *sf13, *w2, *sf2;
+  uint8_t *w13o, *sf13o, *w2o, *sf2o;
+  int32_t H, I, E;
+};
+
+}  // namespace moe

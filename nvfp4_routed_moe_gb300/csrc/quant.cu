@@ -1,0 +1,271 @@
+// quant.cu -- activation quantization with token gather, BF16 finalize,
+// weight preparation into the kernel layout, and the test kernels that expose
+// the device quantizer and codecs.
+#include <cuda_bf16.h>
+
+#include "nvfp4.cuh"
+#include "plan.h"
+
+namespace moe {
+
+cudaError_t launch_with_pdl(const void* fn, dim3 grid, dim3 block, size_t smem, cudaStream_t st, void** args);
+
+// ------------------------------------------------------------ X quantization
+// One warp per token: each lane quantizes 16-element groups g = lane + 32*i
+// of the token ("Cake SiTU backend": group-16 NVFP4 input quantization with
+// qX) once, and writes the codes and block scales to the padded expanded row
+// of every pair the token is routed to ("npu_moe_init_routing_v2", formula 5,
+// gather form: expandedX[gatherRowIdx[i]] = quantResult[i // k]).  The warp
+// also zeroes the token's row of the fp32 output accumulator.
+__global__ void __launch_bounds__(256) quant_x_kernel(const QuantXArgs a) {
+  const int lane = threadIdx.x & 31;
+  const int64_t t = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+  pdl_wait();
+  pdl_launch_dependents();
+  if (t >= a.T) return;
+  const int H = a.H, G = H / 16, KC = H / 16;
+  const float q = __ldg(a.qX);
+  const int rp = (lane < a.k) ? a.row_pos[t * a.k + lane] : -1;
+  float4* orow = reinterpret_cast<float4*>(a.out_f32 + t * H);
+  for (int v = lane; v < H / 4; v += 32) orow[v] = make_float4(0.f, 0.f, 0.f, 0.f);
+  const uint4* xr = reinterpret_cast<const uint4*>(a.x + t * H);
+  for (int g0 = 0; g0 < G; g0 += 32) {
+    const int g = g0 + lane;
+    const bool valid = g < G;
+    float v[16];
+    if (valid) {
+      const uint4 u0 = __ldg(xr + 2 * g), u1 = __ldg(xr + 2 * g + 1);
+      const uint32_t w[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        v[2 * i] = bf16_bits_to_f32(w[i] & 0xFFFFu);
+        v[2 * i + 1] = bf16_bits_to_f32(w[i] >> 16);
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) v[i] = 0.f;
+    }
+    uint2 packed;
+    const uint32_t sf = nvfp4_quant16(v, q, packed);
+    // four consecutive groups share one 32-bit word of a scale atom row
+    uint32_t word = sf << (8 * (lane & 3));
+    word |= __shfl_xor_sync(0xffffffffu, word, 1);
+    word |= __shfl_xor_sync(0xffffffffu, word, 2);
+    for (int j = 0; j < a.k; ++j) {
+      const int row = __shfl_sync(0xffffffffu, rp, j);
+      if (row < 0 || row >= a.max_rows || !valid) continue;
+      *reinterpret_cast<uint2*>(a.xq + (size_t)row * (H / 2) + g * 8) = packed;
+      if ((lane & 3) == 0) *reinterpret_cast<uint32_t*>(a.sfx + atom_offset(row, g, KC)) = word;
+    }
+  }
+}
+
+// ------------------------------------------------------------------ finalize
+// out[t, h] = bf16_rn(acc[t, h]) ("Cake SiTU backend": BF16 weighted
+// finalization; the fp32 weighted sum over k was accumulated by FC2).
+__global__ void __launch_bounds__(256) finalize_kernel(const float* __restrict__ acc, uint16_t* __restrict__ out,
+                                                       int64_t n8) {
+  pdl_wait();
+  pdl_launch_dependents();
+  for (int64_t i = (int64_t)blockIdx.x * 256 + threadIdx.x; i < n8; i += (int64_t)gridDim.x * 256) {
+    const float4 a = reinterpret_cast<const float4*>(acc)[2 * i];
+    const float4 b = reinterpret_cast<const float4*>(acc)[2 * i + 1];
+    const float f[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    uint32_t w[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const __nv_bfloat162 h = __floats2bfloat162_rn(f[2 * j], f[2 * j + 1]);
+      w[j] = *reinterpret_cast<const uint32_t*>(&h);
+    }
+    reinterpret_cast<uint4*>(out)[i] = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+
+// --------------------------------------------------------- weight preparation
+// Kernel layout of the prepared weights:
+//   W13 codes  [E][I/128][H/256][256 rows][128 B]: rows 0..127 of a tile are
+//              gate rows it*128.., rows 128..255 the matching up rows;
+//   W13 scales [E][I/128][H/256][2 (gate, up)][4 atoms][512 B];
+//   W2 codes   [E][H/128][I/128][128 rows][64 B];
+//   W2 scales  [E][H/128][I/64 atoms][512 B];
+// atoms in the 128x4 layout of the "Nvfp4 Tensor" page (block_scale).
+__global__ void __launch_bounds__(256) prep_w13_codes_kernel(const PrepArgs a) {
+  const int NIT = a.I / 128, NKB = a.H / 256;
+  const int64_t units = (int64_t)a.E * 2 * a.I * (a.H / 2) / 16;
+  for (int64_t u = (int64_t)blockIdx.x * 256 + threadIdx.x; u < units; u += (int64_t)gridDim.x * 256) {
+    const int64_t o = u * 16;
+    const int64_t tile = o / 32768;
+    const int r = (int)((o / 128) % 256), byte = (int)(o % 128);
+    const int kb = (int)(tile % NKB), it = (int)((tile / NKB) % NIT);
+    const int64_t e = tile / ((int64_t)NKB * NIT);
+    const int64_t src_row = e * 2 * a.I + (r / 128) * a.I + it * 128 + (r % 128);
+    const uint4 v = *reinterpret_cast<const uint4*>(a.w13 + src_row * (a.H / 2) + kb * 128 + byte);
+    *reinterpret_cast<uint4*>(a.w13o + o) = v;
+  }
+}
+
+__global__ void __launch_bounds__(256) prep_w13_sf_kernel(const PrepArgs a) {
+  const int NIT = a.I / 128, NKB = a.H / 256;
+  const int64_t n = (int64_t)a.E * 2 * a.I * (a.H / 16);
+  for (int64_t o = (int64_t)blockIdx.x * 256 + threadIdx.x; o < n; o += (int64_t)gridDim.x * 256) {
+    const int within = (int)(o % 512);
+    const int64_t atom = o / 512;             // (((e*NIT + it)*NKB + kb)*2 + half)*4 + kt
+    const int kt = (int)(atom % 4), half = (int)((atom / 4) % 2);
+    const int64_t tile = atom / 8;
+    const int kb = (int)(tile % NKB), it = (int)((tile / NKB) % NIT);
+    const int64_t e = tile / ((int64_t)NKB * NIT);
+    const int rr = (within & 15) / 4 * 32 + within / 16;   // innerM*32 + outerM
+    const int c = kb * 16 + kt * 4 + (within & 3);
+    const int64_t src_row = e * 2 * a.I + half * a.I + it * 128 + rr;
+    a.sf13o[o] = a.sf13[src_row * (a.H / 16) + c];
+  }
+}
+
+__global__ void __launch_bounds__(256) prep_w2_codes_kernel(const PrepArgs a) {
+  const int NMT = a.H / 128, NKB2 = a.I / 128;
+  const int64_t units = (int64_t)a.E * a.H * (a.I / 2) / 16;
+  for (int64_t u = (int64_t)blockIdx.x * 256 + threadIdx.x; u < units; u += (int64_t)gridDim.x * 256) {
+    const int64_t o = u * 16;
+    const int64_t tile = o / 8192;            // (e*NMT + mt)*NKB2 + kb
+    const int r = (int)((o / 64) % 128), byte = (int)(o % 64);
+    const int kb = (int)(tile % NKB2), mt = (int)((tile / NKB2) % NMT);
+    const int64_t e = tile / ((int64_t)NKB2 * NMT);
+    const int64_t src_row = e * a.H + mt * 128 + r;
+    const uint4 v = *reinterpret_cast<const uint4*>(a.w2 + src_row * (a.I / 2) + kb * 64 + byte);
+    *reinterpret_cast<uint4*>(a.w2o + o) = v;
+  }
+}
+
+__global__ void __launch_bounds__(256) prep_w2_sf_kernel(const PrepArgs a) {
+  const int NMT = a.H / 128, NA = a.I / 64;
+  const int64_t n = (int64_t)a.E * a.H * (a.I / 16);
+  for (int64_t o = (int64_t)blockIdx.x * 256 + threadIdx.x; o < n; o += (int64_t)gridDim.x * 256) {
+    const int within = (int)(o % 512);
+    const int64_t atom = o / 512;             // (e*NMT + mt)*NA + a
+    const int at = (int)(atom % NA);
+    const int64_t tile = atom / NA;
+    const int mt = (int)(tile % NMT);
+    const int64_t e = tile / NMT;
+    const int rr = (within & 15) / 4 * 32 + within / 16;
+    const int c = at * 4 + (within & 3);
+    const int64_t src_row = e * a.H + mt * 128 + rr;
+    a.sf2o[o] = a.sf2[src_row * (a.I / 16) + c];
+  }
+}
+
+// --------------------------------------------------------------- test kernels
+__global__ void __launch_bounds__(256) codec_sweep_kernel(uint32_t start, int64_t n, uint8_t* lo, uint8_t* hi,
+                                                          uint8_t* e4) {
+  for (int64_t i = (int64_t)blockIdx.x * 256 + threadIdx.x; i < n; i += (int64_t)gridDim.x * 256) {
+    const float v = __uint_as_float(start + (uint32_t)i);
+    if (lo) lo[i] = (uint8_t)(cvt_e2m1x2(0.0f, v) & 0xFu);
+    if (hi) hi[i] = (uint8_t)(cvt_e2m1x2(v, 0.0f) >> 4);
+    if (e4) e4[i] = (uint8_t)cvt_e4m3(v);
+  }
+}
+
+__global__ void __launch_bounds__(256) quant_rows_kernel(const float* x, int64_t rows, int cols, const float* qpr,
+                                                         uint8_t* packed, uint8_t* sf) {
+  const int G = cols / 16;
+  const int64_t n = rows * G;
+  for (int64_t i = (int64_t)blockIdx.x * 256 + threadIdx.x; i < n; i += (int64_t)gridDim.x * 256) {
+    const int64_t r = i / G;
+    const int g = (int)(i % G);
+    float v[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) v[j] = x[r * cols + g * 16 + j];
+    uint2 p;
+    sf[i] = (uint8_t)nvfp4_quant16(v, qpr[r], p);
+    *reinterpret_cast<uint2*>(packed + r * (cols / 2) + g * 8) = p;
+  }
+}
+
+// One warp per (row, 32 features): the FC1 epilogue's per-lane SiTU and
+// 16-lane requant, written in the canonical layout.
+__global__ void __launch_bounds__(256) situ_requant_kernel(const float* z, int64_t rows, int I, float qA, float beta,
+                                                           float lam, float* a_out, uint8_t* packed, uint8_t* sf) {
+  const int lane = threadIdx.x & 31;
+  const int64_t w = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int per_row = I / 32;
+  if (w >= rows * per_row) return;
+  const int64_t r = w / per_row;
+  const int f = (int)(w % per_row) * 32 + lane;
+  const float g = z[r * 2 * I + f], u = z[r * 2 * I + I + f];
+  const float act = situ_f32(g, u, beta, lam);
+  a_out[r * I + f] = act;
+  uint32_t word;
+  const uint32_t s = nvfp4_quant_lanes16(act, qA, word);
+  if ((lane & 7) == 0) *reinterpret_cast<uint32_t*>(packed + r * (I / 2) + f / 2) = word;
+  if ((lane & 15) == 0) sf[r * (I / 16) + f / 16] = (uint8_t)s;
+}
+
+// The FC1 epilogue's 16-lane requant alone, on given activations.
+__global__ void __launch_bounds__(256) requant_lanes_kernel(const float* act, int64_t rows, int I, float qA,
+                                                            uint8_t* packed, uint8_t* sf) {
+  const int lane = threadIdx.x & 31;
+  const int64_t w = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int per_row = I / 32;
+  if (w >= rows * per_row) return;
+  const int64_t r = w / per_row;
+  const int f = (int)(w % per_row) * 32 + lane;
+  uint32_t word;
+  const uint32_t s = nvfp4_quant_lanes16(act[r * I + f], qA, word);
+  if ((lane & 7) == 0) *reinterpret_cast<uint32_t*>(packed + r * (I / 2) + f / 2) = word;
+  if ((lane & 15) == 0) sf[r * (I / 16) + f / 16] = (uint8_t)s;
+}
+
+// ------------------------------------------------------------------ launchers
+cudaError_t launch_quant_x(const QuantXArgs& a, cudaStream_t st) {
+  QuantXArgs args = a;
+  void* kargs[] = {&args};
+  const unsigned blocks = (unsigned)((a.T + 7) / 8);
+  return launch_with_pdl((const void*)quant_x_kernel, dim3(blocks), dim3(256), 0, st, kargs);
+}
+
+cudaError_t launch_finalize(const float* acc, uint16_t* out, int64_t n, int num_sms, cudaStream_t st) {
+  int64_t n8 = n / 8;
+  void* kargs[] = {(void*)&acc, (void*)&out, (void*)&n8};
+  int64_t want = (n8 + 255) / 256;
+  const unsigned blocks = (unsigned)(want < (int64_t)num_sms * 8 ? want : (int64_t)num_sms * 8);
+  return launch_with_pdl((const void*)finalize_kernel, dim3(blocks ? blocks : 1), dim3(256), 0, st, kargs);
+}
+
+cudaError_t launch_prep(const PrepArgs& a, cudaStream_t st, int num_sms) {
+  PrepArgs args = a;
+  dim3 grid(num_sms * 8), block(256);
+  prep_w13_codes_kernel<<<grid, block, 0, st>>>(args);
+  prep_w13_sf_kernel<<<grid, block, 0, st>>>(args);
+  prep_w2_codes_kernel<<<grid, block, 0, st>>>(args);
+  prep_w2_sf_kernel<<<grid, block, 0, st>>>(args);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_codec_sweep(uint32_t start, int64_t n, uint8_t* lo, uint8_t* hi, uint8_t* e4, cudaStream_t st,
+                               int num_sms) {
+  codec_sweep_kernel<<<num_sms * 16, 256, 0, st>>>(start, n, lo, hi, e4);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quant_rows(const float* x, int64_t rows, int cols, const float* qpr, uint8_t* packed, uint8_t* sf,
+                              cudaStream_t st, int num_sms) {
+  quant_rows_kernel<<<num_sms * 8, 256, 0, st>>>(x, rows, cols, qpr, packed, sf);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_situ_requant(const float* z, int64_t rows, int I, float qA, float beta, float lam, float* a_out,
+                                uint8_t* packed, uint8_t* sf, cudaStream_t st) {
+  const int64_t warps = rows * (I / 32);
+  const unsigned blocks = (unsigned)((warps + 7) / 8);
+  situ_requant_kernel<<<blocks ? blocks : 1, 256, 0, st>>>(z, rows, I, qA, beta, lam, a_out, packed, sf);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_requant_lanes(const float* act, int64_t rows, int I, float qA, uint8_t* packed, uint8_t* sf,
+                                 cudaStream_t st) {
+  const int64_t warps = rows * (I / 32);
+  const unsigned blocks = (unsigned)((warps + 7) / 8);
+  requant_lanes_kernel<<<blocks ? blocks : 1, 256, 0, st>>>(act, rows, I, qA, packed, sf);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

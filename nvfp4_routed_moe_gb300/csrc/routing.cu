@@ -1,0 +1,462 @@
+// routing.cu -- init-routing kernels: stable counting sort of expert ids,
+// expanded row index in gather and scatter form, per-expert histogram and
+// inclusive cumsum, padded per-expert row offsets and the token-tile list the
+// grouped GEMMs run over; plus the token move of the standalone init-routing
+// (dynamic int8 quant, drop/pad).
+//
+// Definitions ("npu_moe_init_routing_v2", section 计算公式):
+//   formula 1  sortedExpertIdx, sortedRowIdx = keyValueSort(expertIdx, rowIdx)
+//              with rowIdx = t*k + j; the sort is stable (ties by rowIdx).
+//   formula 2  scatter form expandedRowIdx[i] = sortedRowIdx[i];
+//              gather form expandedRowIdx[sortedRowIdx[i]] = i.
+//   formula 3  per-expert histogram of sortedExpertIdx.
+//   formula 4  dynamic quant: scale = row_max(|x|)/127, q = round(x/scale).
+//   formula 5  expandedX[i] = x[sortedRowIdx[i] // k] (drop/pad: pad every
+//              expert to expertCapacity rows, drop the excess, zero-fill).
+//
+// Sorting method: each warp owns a contiguous run of pairs and walks it 32 at
+// a time in order.  Pass 1 counts its pairs per expert in a private shared-
+// memory histogram (warp match groups lanes with equal ids, the group leader
+// adds the group size).  The per-(block, warp, expert) exclusive prefixes plus
+// the per-expert offsets give every warp the first sorted slot of each
+// expert; pass 2 walks the same run again and hands out slots in order
+// (base + number of equal-id lanes below).  Walking runs in order makes the
+// result stable without any comparison sort.
+#include "nvfp4.cuh"
+#include "plan.h"
+
+namespace moe {
+
+cudaError_t launch_with_pdl(const void* fn, dim3 grid, dim3 block, size_t smem, cudaStream_t st, void** args);
+
+__device__ __forceinline__ uint32_t lanemask_lt() {
+  uint32_t m;
+  asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+  return m;
+}
+
+// Pass 1: per-warp histogram of ids[begin, end) into hist_w[E] (shared).
+__device__ __forceinline__ void warp_histogram(const int32_t* __restrict__ ids, int64_t begin, int64_t end, int E,
+                                               int* hist_w) {
+  const int lane = threadIdx.x & 31;
+  for (int64_t base = begin; base < end; base += 32) {
+    const int64_t f = base + lane;
+    const bool in = f < end;
+    const int id = in ? __ldg(ids + f) : -1;
+    const bool ok = in && id >= 0 && id < E;
+    const uint32_t okmask = __ballot_sync(0xffffffffu, ok);
+    if (ok) {
+      const uint32_t peers = __match_any_sync(okmask, id);
+      if (lane == __ffs(peers) - 1) hist_w[id] += __popc(peers);
+    }
+    __syncwarp();
+  }
+}
+
+// Pass 2: hand out sorted slots.  base_w[e] holds the next slot of expert e
+// for this warp; offs/poffs are the expert's first dropless / padded row.
+__device__ __forceinline__ int warp_rank(const RouteArgs& a, int64_t begin, int64_t end, int* base_w,
+                                         const int* s_offs, const int* s_poffs) {
+  const int lane = threadIdx.x & 31;
+  int invalid = 0;
+  for (int64_t base = begin; base < end; base += 32) {
+    const int64_t f = base + lane;
+    const bool in = f < end;
+    const int id = in ? __ldg(a.ids + f) : -1;
+    const bool ok = in && id >= 0 && id < a.E;
+    const uint32_t okmask = __ballot_sync(0xffffffffu, ok);
+    if (ok) {
+      const uint32_t peers = __match_any_sync(okmask, id);
+      const int leader = __ffs(peers) - 1;
+      const int slot = base_w[id] + __popc(peers & lanemask_lt());
+      __syncwarp(okmask);
+      if (lane == leader) base_w[id] += __popc(peers);
+      a.sorted_row[slot] = (int32_t)f;
+      a.gather[f] = slot;
+      const int prow = s_poffs[id] + (slot - s_offs[id]);
+      a.row_pos[f] = prow;
+      a.prow_pair[prow] = (int32_t)f;
+    } else if (in) {
+      a.gather[f] = -1;
+      a.row_pos[f] = -1;
+      ++invalid;
+    }
+    __syncwarp();
+  }
+  return invalid;
+}
+
+// Block-wide exclusive scan of (count, padded count, tile count) over experts
+// and the tile list.  cnt_s[E] holds the counts on entry; on exit s_offs and
+// s_poffs hold the dropless / padded first rows.  NT threads, E <= NT * 4.
+template <int NT>
+__device__ void scan_experts(const RouteArgs& a, const int* cnt_s, int* s_offs, int* s_poffs, int* s_tmp) {
+  constexpr int NWARP = NT / 32;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int E = a.E;
+  const int per = (E + NT - 1) / NT;  // experts per thread (consecutive)
+  const int e0 = tid * per;
+  int c[4] = {0, 0, 0, 0};
+  int v0 = 0, v1 = 0, v2 = 0;
+  for (int i = 0; i < per; ++i) {
+    const int e = e0 + i;
+    const int n = (e < E) ? cnt_s[e] : 0;
+    c[i] = n;
+    v0 += n;
+    v1 += (n + kTileRows - 1) / kTileRows * kTileRows;
+    v2 += (n + kTileRows - 1) / kTileRows;
+  }
+  int i0 = v0, i1 = v1, i2 = v2;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int t0 = __shfl_up_sync(0xffffffffu, i0, off);
+    const int t1 = __shfl_up_sync(0xffffffffu, i1, off);
+    const int t2 = __shfl_up_sync(0xffffffffu, i2, off);
+    if (lane >= off) {
+      i0 += t0;
+      i1 += t1;
+      i2 += t2;
+    }
+  }
+  if (lane == 31) {
+    s_tmp[warp * 3 + 0] = i0;
+    s_tmp[warp * 3 + 1] = i1;
+    s_tmp[warp * 3 + 2] = i2;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    int w0 = lane < NWARP ? s_tmp[lane * 3 + 0] : 0;
+    int w1 = lane < NWARP ? s_tmp[lane * 3 + 1] : 0;
+    int w2 = lane < NWARP ? s_tmp[lane * 3 + 2] : 0;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int t0 = __shfl_up_sync(0xffffffffu, w0, off);
+      const int t1 = __shfl_up_sync(0xffffffffu, w1, off);
+      const int t2 = __shfl_up_sync(0xffffffffu, w2, off);
+      if (lane >= off) {
+        w0 += t0;
+        w1 += t1;
+        w2 += t2;
+      }
+    }
+    if (lane < NWARP) {
+      s_tmp[96 + lane * 3 + 0] = w0;
+      s_tmp[96 + lane * 3 + 1] = w1;
+      s_tmp[96 + lane * 3 + 2] = w2;
+    }
+  }
+  __syncthreads();
+  const int wb0 = warp ? s_tmp[96 + (warp - 1) * 3 + 0] : 0;
+  const int wb1 = warp ? s_tmp[96 + (warp - 1) * 3 + 1] : 0;
+  const int wb2 = warp ? s_tmp[96 + (warp - 1) * 3 + 2] : 0;
+  int o0 = wb0 + i0 - v0, o1 = wb1 + i1 - v1, o2 = wb2 + i2 - v2;  // exclusive
+  for (int i = 0; i < per; ++i) {
+    const int e = e0 + i;
+    if (e < E) {
+      const int n = c[i];
+      const int nt = (n + kTileRows - 1) / kTileRows;
+      s_offs[e] = o0;
+      s_poffs[e] = o1;
+      a.count[e] = n;
+      a.cumsum[e] = o0 + n;
+      a.offs[e] = o0;
+      a.poffs[e] = o1;
+      a.ttoffs[e] = o2;
+      int4* tl = reinterpret_cast<int4*>(a.tt_list);
+      for (int j = 0; j < nt; ++j) {
+        const int rows = min(kTileRows, n - j * kTileRows);
+        tl[o2 + j] = make_int4(e, o1 + j * kTileRows, rows, 0);
+      }
+      o0 += n;
+      o1 += nt * kTileRows;
+      o2 += nt;
+    }
+  }
+  if (tid == NT - 1) {
+    // the last thread's running sums are the grand totals
+    a.offs[E] = o0;
+    a.poffs[E] = o1;
+    a.ttoffs[E] = o2;
+    a.hdr[HDR_NVALID] = o0;
+    a.hdr[HDR_PPAD] = o1;
+    a.hdr[HDR_NUM_TT] = o2;
+    s_tmp[200] = o0;
+  }
+  __syncthreads();
+}
+
+// ---------------------------------------------------------------- small path
+// One CTA of 1024 threads sorts up to kRouteSmallMax pairs in one launch.
+__global__ void __launch_bounds__(1024, 1) route_small_kernel(const RouteArgs a) {
+  extern __shared__ int sm[];
+  const int E = a.E;
+  int* hist = sm;                  // [32][E]
+  int* s_cnt = hist + 32 * E;      // [E]
+  int* s_offs = s_cnt + E;         // [E]
+  int* s_poffs = s_offs + E;       // [E]
+  int* s_tmp = s_poffs + E;        // [256]
+  const int tid = threadIdx.x, warp = tid >> 5;
+  pdl_wait();
+  pdl_launch_dependents();
+  for (int i = tid; i < 32 * E; i += 1024) hist[i] = 0;
+  __syncthreads();
+  const int64_t per = (a.P + 31) / 32;
+  const int64_t b = warp * per, en = min(a.P, b + per);
+  warp_histogram(a.ids, b, en, E, hist + warp * E);
+  __syncthreads();
+  for (int e = tid; e < E; e += 1024) {
+    int run = 0;
+    for (int w = 0; w < 32; ++w) {
+      const int c = hist[w * E + e];
+      hist[w * E + e] = run;
+      run += c;
+    }
+    s_cnt[e] = run;
+  }
+  __syncthreads();
+  scan_experts<1024>(a, s_cnt, s_offs, s_poffs, s_tmp);
+  for (int i = tid; i < 32 * E; i += 1024) hist[i] += s_offs[i % E];
+  __syncthreads();
+  const int invalid = warp_rank(a, b, en, hist + warp * E, s_offs, s_poffs);
+  const int nvalid = s_tmp[200];
+  for (int64_t i = nvalid + tid; i < a.P; i += 1024) a.sorted_row[i] = -1;
+  if (invalid) {
+    atomicAdd(&a.hdr[HDR_INVALID], invalid);
+    atomicOr(&a.hdr[HDR_STATUS], DEVSTAT_INVALID_EXPERT);
+  }
+}
+
+// ---------------------------------------------------------------- large path
+// Kernel 1: per-block histograms; the last block to finish (ticket counter,
+// no waiting) scans them into per-(block, expert) bases and per-expert
+// offsets, and writes the tile list.  256 threads, kRouteChunk pairs per block.
+__global__ void __launch_bounds__(256) route_hist_kernel(const RouteArgs a) {
+  extern __shared__ int sm[];
+  const int E = a.E;
+  int* hist = sm;                 // [8][E]
+  int* s_cnt = hist + 8 * E;      // [E]
+  int* s_offs = s_cnt + E;        // [E]
+  int* s_poffs = s_offs + E;      // [E]
+  int* s_tmp = s_poffs + E;       // [256]
+  __shared__ int s_last;
+  const int tid = threadIdx.x, warp = tid >> 5;
+  pdl_wait();
+  pdl_launch_dependents();
+  for (int i = tid; i < 8 * E; i += 256) hist[i] = 0;
+  __syncthreads();
+  const int64_t cb = (int64_t)blockIdx.x * kRouteChunk;
+  const int64_t wb = cb + (int64_t)warp * (kRouteChunk / 8);
+  warp_histogram(a.ids, min(wb, a.P), min(wb + kRouteChunk / 8, a.P), E, hist + warp * E);
+  __syncthreads();
+  for (int e = tid; e < E; e += 256) {
+    int s = 0;
+    for (int w = 0; w < 8; ++w) s += hist[w * E + e];
+    a.blockhist[(size_t)blockIdx.x * E + e] = s;
+  }
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) s_last = (atomicAdd(&a.hdr[HDR_DONE], 1) == a.nblk - 1);
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  for (int e = tid; e < E; e += 256) {
+    int run = 0;
+    for (int blk = 0; blk < a.nblk; ++blk) {
+      int* p = &a.blockhist[(size_t)blk * E + e];
+      const int c = __ldcg(p);
+      *p = run;
+      run += c;
+    }
+    s_cnt[e] = run;
+  }
+  __syncthreads();
+  scan_experts<256>(a, s_cnt, s_offs, s_poffs, s_tmp);
+}
+
+// Kernel 2: every block recounts its pairs per warp and hands out slots.
+__global__ void __launch_bounds__(256) route_rank_kernel(const RouteArgs a) {
+  extern __shared__ int sm[];
+  const int E = a.E;
+  int* hist = sm;                 // [8][E]
+  int* s_offs = hist + 8 * E;     // [E]
+  int* s_poffs = s_offs + E;      // [E]
+  const int tid = threadIdx.x, warp = tid >> 5;
+  pdl_wait();
+  pdl_launch_dependents();
+  if (blockIdx.x == 0 && tid == 0) a.hdr[HDR_DONE] = 0;  // re-arm the ticket for the next call
+  for (int i = tid; i < 8 * E; i += 256) hist[i] = 0;
+  for (int e = tid; e < E; e += 256) {
+    s_offs[e] = a.offs[e];
+    s_poffs[e] = a.poffs[e];
+  }
+  __syncthreads();
+  const int64_t cb = (int64_t)blockIdx.x * kRouteChunk;
+  const int64_t wb = cb + (int64_t)warp * (kRouteChunk / 8);
+  const int64_t b = min(wb, a.P), en = min(wb + kRouteChunk / 8, a.P);
+  warp_histogram(a.ids, b, en, E, hist + warp * E);
+  __syncthreads();
+  for (int e = tid; e < E; e += 256) {
+    int run = s_offs[e] + a.blockhist[(size_t)blockIdx.x * E + e];
+    for (int w = 0; w < 8; ++w) {
+      const int c = hist[w * E + e];
+      hist[w * E + e] = run;
+      run += c;
+    }
+  }
+  __syncthreads();
+  const int invalid = warp_rank(a, b, en, hist + warp * E, s_offs, s_poffs);
+  const int nvalid = a.offs[E];
+  const int64_t t0 = max((int64_t)nvalid, cb), t1 = min(a.P, cb + kRouteChunk);
+  for (int64_t i = t0 + tid; i < t1; i += 256) a.sorted_row[i] = -1;
+  if (invalid) {
+    atomicAdd(&a.hdr[HDR_INVALID], invalid);
+    atomicOr(&a.hdr[HDR_STATUS], DEVSTAT_INVALID_EXPERT);
+  }
+}
+
+// -------------------------------------------------------- init-routing move
+// One warp per token: dynamic int8 quant of the row (formula 4) or a bf16
+// copy, written to each destination row of the token's pairs (formula 5).
+__global__ void __launch_bounds__(256) init_move_kernel(const InitMoveArgs a) {
+  const int lane = threadIdx.x & 31;
+  const int64_t t = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+  pdl_wait();
+  pdl_launch_dependents();
+  if (t >= a.T) return;
+  const uint16_t* xr = a.x + t * a.H;
+  int dest = -1;
+  if (lane < a.k) {
+    const int64_t f = t * a.k + lane;
+    const int i = a.gather[f];
+    if (i >= 0) {
+      if (!a.drop_pad) {
+        dest = i;
+      } else {
+        const int e = a.ids[f];
+        const int r = i - a.offs[e];
+        dest = (r < a.C) ? e * a.C + r : -1;
+      }
+    }
+    if (a.row_idx_type == 0) a.expanded_row_idx[f] = dest;
+  }
+  const int nvec = a.H / 8;  // 8 bf16 per 16-byte vector
+  const uint4* xv = reinterpret_cast<const uint4*>(xr);
+  if (a.quant_mode == 1) {
+    float amax = 0.0f;
+    for (int v = lane; v < nvec; v += 32) {
+      const uint4 u = __ldg(xv + v);
+      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        amax = fmaxf(amax, fabsf(bf16_bits_to_f32(w[i] & 0xFFFFu)));
+        amax = fmaxf(amax, fabsf(bf16_bits_to_f32(w[i] >> 16)));
+      }
+    }
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+    const float s = __fdiv_rn(amax, 127.0f);
+    for (int v = lane; v < nvec; v += 32) {
+      const uint4 u = __ldg(xv + v);
+      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+      uint32_t q[2] = {0u, 0u};
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const uint32_t bits = (i & 1) ? (w[i >> 1] >> 16) : (w[i >> 1] & 0xFFFFu);
+        int qi = 0;
+        if (s != 0.0f) {
+          float y = rintf(__fdiv_rn(bf16_bits_to_f32(bits), s));
+          y = fminf(fmaxf(y, -127.0f), 127.0f);
+          qi = (int)y;
+        }
+        q[i >> 2] |= ((uint32_t)qi & 0xFFu) << (8 * (i & 3));
+      }
+      for (int j = 0; j < a.k; ++j) {
+        const int d = __shfl_sync(0xffffffffu, dest, j);
+        if (d >= 0)
+          *reinterpret_cast<uint2*>(static_cast<int8_t*>(a.expanded_x) + (int64_t)d * a.H + v * 8) =
+              make_uint2(q[0], q[1]);
+      }
+    }
+    for (int j = 0; j < a.k; ++j) {
+      const int d = __shfl_sync(0xffffffffu, dest, j);
+      if (d >= 0 && lane == 0 && a.expanded_scale) a.expanded_scale[d] = s;
+    }
+  } else {
+    for (int v = lane; v < nvec; v += 32) {
+      const uint4 u = __ldg(xv + v);
+      for (int j = 0; j < a.k; ++j) {
+        const int d = __shfl_sync(0xffffffffu, dest, j);
+        if (d >= 0) reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.expanded_x) + (int64_t)d * a.H)[v] = u;
+      }
+    }
+  }
+}
+
+// Histogram output (formula 3, count or inclusive cumsum), the scatter form of
+// expanded_row_idx (formula 2), and the zero fill of unfilled drop/pad slots.
+__global__ void __launch_bounds__(256) init_finish_kernel(const InitFinishArgs a) {
+  pdl_wait();
+  pdl_launch_dependents();
+  const int64_t gtid = (int64_t)blockIdx.x * 256 + threadIdx.x;
+  const int64_t nthr = (int64_t)gridDim.x * 256;
+  for (int64_t e = gtid; e < a.E; e += nthr) a.tokens_out[e] = a.tokens_num_type == 1 ? a.count[e] : a.cumsum[e];
+  if (a.row_idx_type == 1)
+    for (int64_t i = gtid; i < a.P; i += nthr) a.expanded_row_idx[i] = a.sorted_row[i];
+  if (a.drop_pad) {
+    const int lane = threadIdx.x & 31;
+    const int64_t gw = gtid >> 5, nw = nthr >> 5;
+    const int64_t nslot = (int64_t)a.E * a.C;
+    const int64_t row_bytes = (int64_t)a.H * a.esize;
+    for (int64_t s = gw; s < nslot; s += nw) {
+      const int e = (int)(s / a.C), r = (int)(s % a.C);
+      if (r < a.count[e]) continue;
+      uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(a.expanded_x) + s * row_bytes);
+      for (int64_t v = lane; v < row_bytes / 16; v += 32) dst[v] = make_uint4(0, 0, 0, 0);
+      if (lane == 0 && a.expanded_scale) a.expanded_scale[s] = 0.0f;
+    }
+  }
+}
+
+// ------------------------------------------------------------------ launchers
+size_t route_small_smem(int E) { return (size_t)(32 * E + 3 * E + 256) * 4; }
+size_t route_big_smem(int E) { return (size_t)(8 * E + 3 * E + 256) * 4; }
+
+cudaError_t launch_routing(const RouteArgs& a, cudaStream_t st, int* launches) {
+  RouteArgs args = a;
+  void* kargs[] = {&args};
+  if (a.P <= kRouteSmallMax) {
+    *launches = 1;
+    return launch_with_pdl((const void*)route_small_kernel, dim3(1), dim3(1024), route_small_smem(a.E), st, kargs);
+  }
+  *launches = 2;
+  cudaError_t err =
+      launch_with_pdl((const void*)route_hist_kernel, dim3(a.nblk), dim3(256), route_big_smem(a.E), st, kargs);
+  if (err != cudaSuccess) return err;
+  return launch_with_pdl((const void*)route_rank_kernel, dim3(a.nblk), dim3(256), route_big_smem(a.E), st, kargs);
+}
+
+cudaError_t launch_init_move(const InitMoveArgs& a, cudaStream_t st) {
+  InitMoveArgs args = a;
+  void* kargs[] = {&args};
+  const unsigned blocks = (unsigned)((a.T + 7) / 8);
+  return launch_with_pdl((const void*)init_move_kernel, dim3(blocks ? blocks : 1), dim3(256), 0, st, kargs);
+}
+
+cudaError_t launch_init_finish(const InitFinishArgs& a, cudaStream_t st, int num_sms) {
+  InitFinishArgs args = a;
+  void* kargs[] = {&args};
+  return launch_with_pdl((const void*)init_finish_kernel, dim3(num_sms * 4), dim3(256), 0, st, kargs);
+}
+
+cudaError_t routing_set_attributes(int E) {
+  cudaError_t err = cudaFuncSetAttribute((const void*)route_small_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)route_small_smem(E));
+  if (err != cudaSuccess) return err;
+  err = cudaFuncSetAttribute((const void*)route_hist_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)route_big_smem(E));
+  if (err != cudaSuccess) return err;
+  return cudaFuncSetAttribute((const void*)route_rank_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)route_big_smem(E));
+}
+
+}  // namespace moe
