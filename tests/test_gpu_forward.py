@@ -1,0 +1,244 @@
+"""GPU forward through the C ABI against the oracle.
+
+Tiny case: every output, plus the intermediates in the workspace (routing
+arrays and quantized X bit-exact, quantized A codes up to rounding-boundary
+cases).  Full shape (H=3584, I=384, E=896, k=16): every output for decode
+T in {1, 8, 16}; sampled tokens for prefill (T=4096, Zipf routing) and max
+batch (T=16384, 1% of rows x50), with whole-output properties.  Edge cases:
+ragged T, x = 0, exact-arithmetic inputs, invalid ids, per-expert SiTU
+parameters, workspace reuse, CUDA-graph replay."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle import cases
+from nvfp4_routed_moe_gb300 import api
+from nvfp4_routed_moe_gb300 import inputs as gen
+from gpu_util import Model, assert_close, dev, out_bits, ws_i32, ws_u8, ws_view
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def tiny():
+    inp = cases.prepare_tiny(0)
+    return inp, Model(inp)
+
+
+def test_tiny_forward_matches_oracle(tiny):
+    inp, m = tiny
+    out, ws = m.forward_inputs()
+    torch.cuda.synchronize()
+    assert api.moe_read_status(ws) == (0, 0)
+    ref = cases.run_oracle(inp)
+    assert_close(out_bits(out), ref, "tiny")
+
+
+def test_tiny_intermediates(tiny):
+    inp, m = tiny
+    out, ws = m.forward_inputs()
+    torch.cuda.synchronize()
+    lay = ws_view(m, ws)
+    T, k, E, H, I = inp.T, inp.k, inp.E, inp.H, inp.I
+    P = T * k
+    r = oracle.routing(inp.expert_ids, E)
+    np.testing.assert_array_equal(ws_i32(ws, lay.count, E), r["count"])
+    np.testing.assert_array_equal(ws_i32(ws, lay.cumsum, E), r["cumsum"])
+    np.testing.assert_array_equal(ws_i32(ws, lay.sorted_row, P), r["sorted_row"])
+    np.testing.assert_array_equal(ws_i32(ws, lay.gather, P), r["gather"])
+    row_pos = ws_i32(ws, lay.row_pos, P)
+    # padded row of pair f: expert segment start (rounded to 128) + rank within the expert
+    pstart = np.concatenate([[0], np.cumsum((r["count"] + 127) // 128 * 128)])[:-1]
+    rank = r["gather"] - (r["cumsum"] - r["count"])[inp.expert_ids.ravel()]
+    np.testing.assert_array_equal(row_pos, pstart[inp.expert_ids.ravel()] + rank)
+    # quantized X rows, bit-exact (oracle quantizes each token with qX)
+    xq_ref, xsf_ref = oracle.nvfp4_quant_rows(gen.bf16_bits_to_f32(inp.x), q=inp.qX)
+    npad = int(row_pos.max()) + 1
+    xq = ws_u8(ws, lay.xq, npad * (H // 2)).reshape(npad, H // 2)
+    sfx = ws_u8(ws, lay.sfx, ((npad + 127) // 128) * (H // 64) * 512)
+    for f in range(P):
+        t, p = f // k, row_pos[f]
+        np.testing.assert_array_equal(xq[p], xq_ref[t])
+        got_sf = [sfx[oracle.scale_atom_offset(p, c, H // 16)] for c in range(H // 16)]
+        np.testing.assert_array_equal(got_sf, xsf_ref[t])
+    # quantized A codes: equal except where FC1 sums round differently near a boundary
+    _, mid = cases.run_oracle(inp, want_intermediates=True)
+    aq = ws_u8(ws, lay.aq, npad * (I // 2)).reshape(npad, I // 2)
+    table = np.array([oracle.e2m1_value(c) for c in range(16)])
+    total = mism = 0
+    for f in range(P):
+        t, j, p = f // k, f % k, row_pos[f]
+        g = np.stack([aq[p] & 15, aq[p] >> 4], -1).ravel()
+        rr = np.stack([mid["aq"][t, j] & 15, mid["aq"][t, j] >> 4], -1).ravel()
+        total += g.size
+        mism += int((table[g] != table[rr]).sum())
+    assert mism <= 0.01 * total, f"A code mismatch rate {mism}/{total}"
+
+
+@pytest.mark.parametrize("T", [1, 2, 7, 33, 300])
+def test_tiny_shape_ragged_token_counts(T):
+    inp = cases.prepare_tiny(1, T=T)
+    m = Model(inp)
+    out, ws = m.forward_inputs()
+    ref = cases.run_oracle(inp)
+    assert_close(out_bits(out), ref, f"T={T}")
+    assert api.moe_read_status(ws) == (0, 0)
+
+
+def test_zero_input_gives_zero_output(tiny):
+    inp, m = tiny
+    x = torch.zeros((inp.T, inp.H), dtype=torch.bfloat16, device="cuda")
+    out, _ = m.forward(x, dev(inp.expert_ids), dev(inp.route_weights, torch.bfloat16))
+    assert not out.float().abs().sum().item()
+
+
+def test_exact_inputs_match_to_the_last_bit():
+    """Power-of-two block scales, grid-valued x and unit qX: X quantizes
+    exactly and every FC1 sum is exact in fp32, so GPU and oracle see the same
+    SiTU inputs; the outputs then agree bit for bit except where an fp32 sum
+    lands on a bf16 rounding boundary (at most one bf16 ulp)."""
+    H, I, E, k, T = 512, 128, 8, 2, 5
+    rs = np.random.default_rng(11)
+    grid = np.array([0, 0.5, 1, 1.5, 2, 3, 4, 6], np.float32)
+    x = rs.choice(np.concatenate([grid, -grid]), size=(T, H)).astype(np.float32)
+    x[:, ::16] = 6.0
+    ids = np.stack([rs.permutation(E)[:k] for _ in range(T)]).astype(np.int32)
+    rw = gen.f32_to_bf16_bits(np.array([[0.5, 0.25]] * T, np.float32))
+    inp = gen.MoEInputs(H, I, E, k, T, gen.f32_to_bf16_bits(x), ids, rw, np.float32(1.0))
+    inp.w13 = rs.integers(0, 256, size=(E, 2 * I, H // 2), dtype=np.uint8)
+    inp.sf13 = np.full((E, 2 * I, H // 16), 0x38, np.uint8)
+    inp.w2 = rs.integers(0, 256, size=(E, H, I // 2), dtype=np.uint8)
+    inp.sf2 = np.full((E, H, I // 16), 0x30, np.uint8)
+    inp.dXdW13 = np.full(E, 2.0 ** -6, np.float32)
+    inp.qA = np.full(E, 1.0, np.float32)
+    inp.dAdW2 = np.full(E, 2.0 ** -6, np.float32)
+    m = Model(inp)
+    out, _ = m.forward_inputs()
+    ref = cases.run_oracle(inp)
+    got = out_bits(out)
+    same = got == ref
+    assert same.mean() >= 0.99, f"only {same.mean():.4f} of outputs identical"
+    gv, rv = gen.bf16_bits_to_f32(got), gen.bf16_bits_to_f32(ref)
+    assert np.all(np.abs(gv - rv) <= np.abs(rv) * 2.0 ** -7)
+
+
+def test_invalid_ids_skipped_and_flagged(tiny):
+    inp, m = tiny
+    ids = inp.expert_ids.copy()
+    ids[2, 1] = -5
+    ids[9, 3] = inp.E + 3
+    out, ws = m.forward(dev(inp.x, torch.bfloat16), dev(ids), dev(inp.route_weights, torch.bfloat16))
+    st = api.moe_read_status(ws)
+    assert st == (api.DEVSTAT_INVALID_EXPERT, 2)
+    inp2 = cases.prepare_tiny(0)
+    inp2.expert_ids = ids
+    ref = cases.run_oracle(inp2)
+    assert_close(out_bits(out), ref, "invalid ids")
+
+
+def test_situ_parameters_per_expert(tiny):
+    inp, m = tiny
+    rs = np.random.default_rng(3)
+    beta = rs.uniform(1.0, 6.0, inp.E).astype(np.float32)
+    lam = rs.uniform(5.0, 40.0, inp.E).astype(np.float32)
+    out, _ = m.forward_inputs(beta=dev(beta), lam=dev(lam))
+    ref = cases.run_oracle(inp, beta=beta, lam=lam)
+    assert_close(out_bits(out), ref, "situ beta/lambda")
+
+
+def test_workspace_reuse_across_token_counts(tiny):
+    """One maximum-size workspace serves every smaller prepared T."""
+    inp, m = tiny
+    ws = m.workspace(inp.T)
+    for T in (inp.T, 3, 1):
+        api.moe_prepare_workspace(m.shape, ws, T)
+    x, ids, rw = dev(inp.x, torch.bfloat16), dev(inp.expert_ids), dev(inp.route_weights, torch.bfloat16)
+    full = cases.run_oracle(inp)
+    for T in (inp.T, 3, 1):
+        out, _ = m.forward(x[:T], ids[:T], rw[:T], ws=ws, T=T, prepare=False)
+        assert_close(out_bits(out), full[:T], f"reuse T={T}")
+
+
+def test_not_prepared_is_rejected(tiny):
+    inp, m = tiny
+    ws = m.workspace(inp.T)
+    with pytest.raises(api.MoeError) as e:
+        m.forward_inputs(ws=ws, prepare=False)
+    assert e.value.status == 4
+
+
+def test_cuda_graph_replay(tiny):
+    inp, m = tiny
+    x, ids, rw = dev(inp.x, torch.bfloat16), dev(inp.expert_ids), dev(inp.route_weights, torch.bfloat16)
+    ws = m.workspace(inp.T)
+    api.moe_prepare_workspace(m.shape, ws, inp.T)
+    out = torch.empty((inp.T, inp.H), dtype=torch.bfloat16, device="cuda")
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        m.forward(x, ids, rw, ws=ws, out=out, prepare=False)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        m.forward(x, ids, rw, ws=ws, out=out, prepare=False)
+    ref = cases.run_oracle(inp)
+    for _ in range(3):
+        out.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert_close(out_bits(out), ref, "graph replay")
+    # new inputs in the same buffers
+    inp2 = cases.prepare_tiny(0)
+    inp2.x = gen.draw_x(9, inp.T, inp.H)
+    inp2.expert_ids = gen.draw_ids_uniform(9, inp.T, inp.E, inp.k)
+    x.copy_(dev(inp2.x, torch.bfloat16))
+    ids.copy_(dev(inp2.expert_ids))
+    g.replay()
+    torch.cuda.synchronize()
+    assert_close(out_bits(out), cases.run_oracle(inp2), "graph replay new inputs")
+
+
+# ------------------------------------------------------------------ full shape
+@pytest.fixture(scope="module")
+def full_model():
+    inp = gen.full(0, T=16)
+    return inp, Model(inp)
+
+
+def _full_case(model_inp, T, routing, big=0.0, seed=0):
+    inp = gen.full(seed, T=T, routing=routing, big_rows_frac=big, weights=False)
+    inp.w13, inp.sf13, inp.w2, inp.sf2 = model_inp.w13, model_inp.sf13, model_inp.w2, model_inp.sf2
+    inp.dXdW13, inp.qA, inp.dAdW2 = model_inp.dXdW13, model_inp.qA, model_inp.dAdW2
+    return inp
+
+
+@pytest.mark.parametrize("T", [1, 8, 16])
+def test_full_shape_decode_all_tokens(full_model, T):
+    minp, m = full_model
+    inp = _full_case(minp, T, "uniform", seed=T)
+    out, ws = m.forward_inputs(inp)
+    torch.cuda.synchronize()
+    assert api.moe_read_status(ws) == (0, 0)
+    ref = cases.run_oracle(inp)
+    assert_close(out_bits(out), ref, f"decode T={T}")
+
+
+@pytest.mark.parametrize("T,routing,big", [(512, "uniform", 0.0), (4096, "zipf", 0.0), (16384, "uniform", 0.01)])
+def test_full_shape_sampled_tokens(full_model, T, routing, big):
+    minp, m = full_model
+    inp = _full_case(minp, T, routing, big)
+    out, ws = m.forward_inputs(inp)
+    torch.cuda.synchronize()
+    assert api.moe_read_status(ws) == (0, 0)
+    rs = np.random.default_rng(T)
+    sample = np.unique(np.concatenate([[0, T - 1], rs.choice(T, 14, replace=False)]))
+    if big:
+        xf = np.abs(gen.bf16_bits_to_f32(inp.x)).max(axis=1)
+        sample = np.unique(np.concatenate([sample, np.argsort(-xf)[:2]]))
+    ref = cases.run_oracle(inp, tokens=sample)
+    assert_close(out_bits(out)[sample], ref, f"T={T} {routing}")
+    assert torch.isfinite(out.float()).all()
+    counts = np.bincount(inp.expert_ids.ravel(), minlength=inp.E)
+    lay = ws_view(m, ws)
+    np.testing.assert_array_equal(ws_i32(ws, lay.count, inp.E), counts)
