@@ -1,0 +1,423 @@
+#!/usr/bin/env python
+"""Benchmark of the routed NVFP4 SiTU MoE forward on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload maxbatch] [--impl ours|reference]
+
+One step is one moe_forward (routing, X quantization, FC1 + SiTU + requant,
+FC2 + weighted combine, BF16 finalize) over one batch of seeded synthetic
+input already resident in HBM.  Default workload: T=16384 tokens at
+H=3584, I=384, E=896, k=16, uniform distinct expert ids, 1% of rows x50
+(the max-batch case); its 2.08 GB of weights are larger than L2, so no flush
+is needed between steps.  Under torchrun each rank runs its own batch on its
+own GPU with replicated weights (weak scaling, no collective on the data
+path); rank 0 prints one JSON line.
+
+Also measured: per-stage times from timing events recorded between the
+stages inside the timed steps (the dominant kernel's roofline uses them),
+an end-to-end pass with pinned host buffers (copies inside the timed
+region), SM clocks during the timed region, a decode/prefill sweep (L2
+flushed between steps), and the CPU oracle on a bounded sample of the same
+workload (rank 0, one GPU only).
+
+--impl reference times the CPU oracle alone (there is no other implementation
+to run): each step evaluates a bounded sample of the same workload on the
+host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from nvfp4_routed_moe_gb300 import inputs as gen  # noqa: E402
+
+METRIC = "MoE tokens/s at H3584/I384/E896/k16 (T=1..16384); % HBM or FP4 roofline"
+H, I, E, K = gen.FULL["H"], gen.FULL["I"], gen.FULL["E"], gen.FULL["k"]
+FC1_BYTES_PER_EXPERT = 2 * I * H // 2 + 2 * I * H // 16          # 1,548,288
+FC2_BYTES_PER_EXPERT = H * I // 2 + H * I // 16                  # 774,144
+WORKLOADS = {
+    "maxbatch": dict(T=16384, routing="uniform", big_rows_frac=0.01,
+                     text="T=16384, H=3584, I=384, E=896, top-k=16, uniform distinct ids, 1% of rows x50"),
+    "prefill": dict(T=4096, routing="zipf", big_rows_frac=0.0,
+                    text="T=4096, H=3584, I=384, E=896, top-k=16, Zipf(1.1) ids without replacement"),
+    "decode16": dict(T=16, routing="uniform", big_rows_frac=0.0,
+                     text="T=16, H=3584, I=384, E=896, top-k=16, uniform distinct ids"),
+    # a small case of the same kernels for counter captures (weights 0.3 GB, still larger than L2)
+    "small_e128": dict(T=1024, routing="uniform", big_rows_frac=0.0, E=128,
+                       text="T=1024, H=3584, I=384, E=128, top-k=16, uniform distinct ids (profiling case)"),
+}
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def step_bytes(T, n_active):
+    """Algorithmic bytes of one forward: weights and block scales of the
+    active experts, x read and out written (bf16), ids and route weights."""
+    return n_active * (FC1_BYTES_PER_EXPERT + FC2_BYTES_PER_EXPERT) + 2 * T * H * 2 + T * K * 6
+
+
+def fc1_bytes(T, n_active):
+    """Algorithmic bytes of one FC1 launch: W13 codes + scales of the active
+    experts, each token's quantized row once, the quantized intermediate of
+    every routed pair written once."""
+    return n_active * FC1_BYTES_PER_EXPERT + T * (H // 2 + H // 16) + T * K * (I // 2 + I // 16)
+
+
+def fc1_traffic_from_profile():
+    """DRAM bytes per FC1 launch from the committed ncu summary, used only
+    while the kernel source is unchanged since the capture."""
+    path = os.path.join(ROOT, "profiles", "fc1_kernel_maxbatch.md")
+    try:
+        lines = open(path).read().splitlines()
+        want = {l.split("=", 1)[0].strip(): l.split("=", 1)[1].strip() for l in lines if "=" in l and
+                l.startswith(("gemm_cu_sha1", "fc1_dram_bytes_per_launch_full"))}
+        sha = hashlib.sha1(open(os.path.join(ROOT, "nvfp4_routed_moe_gb300", "csrc", "gemm.cu"), "rb").read())
+        if want.get("gemm_cu_sha1") == sha.hexdigest():
+            return float(want["fc1_dram_bytes_per_launch_full"])
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clock samples every 200 ms in a background process."""
+
+    def __init__(self, gpu_id: str):
+        self.rows = []
+        self.marks = {}
+        q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", f"--query-gpu={q}", "--format=csv,noheader,nounits",
+                                       "-lms", "200", "-i", gpu_id], stdout=subprocess.PIPE,
+                                      stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.p = None
+
+    def _read(self):
+        for line in self.p.stdout:
+            self.rows.append((time.time(), [c.strip() for c in line.split(",")]))
+
+    def mark(self, name):
+        self.marks[name] = time.time()
+
+    def stop(self):
+        if self.p is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.3)
+        self.p.terminate()
+        try:
+            self.p.wait(timeout=5)
+        except Exception:
+            self.p.kill()
+        t0, t1 = self.marks.get("start", 0), self.marks.get("end", 1e30)
+        inside = [r for t, r in self.rows if t0 <= t <= t1 + 0.2]
+        window = "timed region"
+        if not inside:
+            inside = [r for _, r in self.rows]
+            window = "whole run (timed region shorter than one sample)"
+        sm = [float(r[1]) for r in inside if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in inside if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in inside for i in range(4) if len(r) > 5 + i and r[5 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(inside), "window": window}
+
+
+def cpu_baseline(inp, target_s=12.0, max_tokens=512):
+    """The oracle as it stands on a bounded sample (the first n tokens)."""
+    import oracle
+    from oracle import cases
+    oracle.build()
+    n, spent, done = 4, 0.0, 0
+    t_start = time.time()
+    while spent < target_s and done < max_tokens:
+        toks = np.arange(done, min(done + n, inp.T))
+        t0 = time.time()
+        cases.run_oracle(inp, tokens=toks)
+        spent += time.time() - t0
+        done += len(toks)
+        n = min(2 * n, max_tokens - done) if done < max_tokens else 0
+        if n <= 0 or done >= inp.T:
+            break
+    wall = time.time() - t_start
+    return {"value": done / spent, "unit": "tokens/s", "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"first {done} tokens of the timed workload (same weights and routing), {spent:.1f} s"}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+    from oracle import cases
+    oracle.build()
+    wl = WORKLOADS[args.workload]
+    inp = gen.full(0, T=wl["T"], routing=wl["routing"], big_rows_frac=wl["big_rows_frac"], E=wl.get("E"))
+    per_step = oracle.num_threads()       # one token per host thread: a step costs about one token's time
+    for s in range(args.warmup):
+        cases.run_oracle(inp, tokens=np.arange(s * per_step, (s + 1) * per_step) % inp.T)
+    t0 = time.time()
+    done = 0
+    for s in range(args.steps):
+        toks = (np.arange(per_step) + (args.warmup + s) * per_step) % inp.T
+        cases.run_oracle(inp, tokens=toks)
+        done += per_step
+    dt = time.time() - t0
+    value = done / dt
+    sample = f"{per_step} tokens of the {args.workload} workload per step, one per host thread"
+    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+            "config": {"workload": f"{args.workload}: {wl['text']}", "T": wl["T"]},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": oracle.num_threads(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default="maxbatch", choices=sorted(WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-stage-events", action="store_true", help="time the steps without stage events")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    if args.impl == "reference":
+        run_reference(args)
+        return
+
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    from nvfp4_routed_moe_gb300 import api
+    from nvfp4_routed_moe_gb300 import build as nvbuild
+    if rank == 0 or world == 1:
+        nvbuild.build()
+    if world > 1:
+        dist.barrier()
+    api.lib()
+
+    def dev(a, dtype=None):
+        a = np.ascontiguousarray(a)
+        if a.dtype == np.uint16:
+            a = a.view(np.int16)
+        t = torch.from_numpy(a)
+        return (t.view(dtype) if dtype is not None else t).cuda()
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    wl = WORKLOADS[args.workload]
+    E = wl.get("E", gen.FULL["E"])
+    inp = gen.full(rank, T=wl["T"], routing=wl["routing"], big_rows_frac=wl["big_rows_frac"], weights=False, E=E)
+    winp = gen.full(0, T=1, weights=True, E=E)     # same weights on every rank
+    shp = api.shape(H, I, E, K)
+    sizes = api.moe_prepared_weight_bytes(shp)
+    w = [torch.empty(n, dtype=torch.uint8, device="cuda") for n in sizes]
+    canon = [dev(winp.w13), dev(winp.sf13), dev(winp.w2), dev(winp.sf2)]
+    api.moe_prepare_weights(shp, *canon, *w)
+    torch.cuda.synchronize()
+    del canon
+    torch.cuda.empty_cache()
+    scales = [dev(winp.dXdW13), dev(winp.qA), dev(winp.dAdW2)]
+
+    def make_batch(b):
+        return dict(x=dev(b.x, torch.bfloat16), ids=dev(b.expert_ids), rw=dev(b.route_weights, torch.bfloat16),
+                    qX=dev(np.array([b.qX], np.float32)), T=b.T,
+                    n_active=int((np.bincount(b.expert_ids.ravel(), minlength=E) > 0).sum()))
+
+    def forward(bt, ws, out, stream=None):
+        api.moe_forward(shp, bt["T"], bt["x"], bt["ids"], bt["rw"], *w, bt["qX"], *scales, None, None, ws, out,
+                        stream)
+
+    batch = make_batch(inp)
+    T = batch["T"]
+    ws = torch.empty(api.moe_workspace_size(shp, T), dtype=torch.uint8, device="cuda")
+    api.moe_prepare_workspace(shp, ws, T)
+    out = torch.empty((T, H), dtype=torch.bfloat16, device="cuda")
+    for _ in range(args.warmup):
+        forward(batch, ws, out)
+    torch.cuda.synchronize()
+    status = api.moe_read_status(ws)
+    if status != (0, 0):
+        raise SystemExit(f"device status {status}")
+
+    # ------------------------------------------------------------ timed region
+    props = torch.cuda.get_device_properties(local)
+    gpu_id = str(getattr(props, "uuid", "")) or str(local)
+    if gpu_id and not gpu_id.startswith("GPU-") and len(gpu_id) > 8:
+        gpu_id = "GPU-" + gpu_id
+    clocks = ClockSampler(gpu_id)
+    time.sleep(0.5)
+    stage = None
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if not args.no_stage_events:
+        api.moe_profile_start(args.steps)
+    barrier()
+    torch.cuda.synchronize()
+    clocks.mark("start")
+    ev0.record()
+    for _ in range(args.steps):
+        forward(batch, ws, out)
+    ev1.record()
+    torch.cuda.synchronize()
+    clocks.mark("end")
+    barrier()
+    ms = ev0.elapsed_time(ev1)
+    if not args.no_stage_events:
+        stage_ms, ncalls = api.moe_profile_stop()
+        stage = {k: v / max(ncalls, 1) for k, v in stage_ms.items()}
+    clk = clocks.stop()
+    ms_t = torch.tensor([ms], dtype=torch.float64, device="cuda")
+    if world > 1:
+        dist.all_reduce(ms_t, op=dist.ReduceOp.MAX)
+    ms = float(ms_t.item())
+    ms_per_step = ms / args.steps
+    value = world * T * args.steps / (ms / 1e3)
+    launches = api.moe_forward_launch_count(shp, T) * args.steps
+
+    # ------------------------------------------------------------ end to end
+    x_h = batch["x"].cpu().pin_memory()
+    ids_h = batch["ids"].cpu().pin_memory()
+    rw_h = batch["rw"].cpu().pin_memory()
+    out_h = torch.empty((T, H), dtype=torch.bfloat16).pin_memory()
+    xb, idb, rwb = torch.empty_like(batch["x"]), torch.empty_like(batch["ids"]), torch.empty_like(batch["rw"])
+    ebatch = dict(batch, x=xb, ids=idb, rw=rwb)
+    e2e_steps = min(args.steps, 200)
+    for _ in range(2):
+        xb.copy_(x_h, non_blocking=True)
+        idb.copy_(ids_h, non_blocking=True)
+        rwb.copy_(rw_h, non_blocking=True)
+        forward(ebatch, ws, out)
+        out_h.copy_(out, non_blocking=True)
+    barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(e2e_steps):
+        xb.copy_(x_h, non_blocking=True)
+        idb.copy_(ids_h, non_blocking=True)
+        rwb.copy_(rw_h, non_blocking=True)
+        forward(ebatch, ws, out)
+        out_h.copy_(out, non_blocking=True)
+    e1.record()
+    torch.cuda.synchronize()
+    e2e_ms = torch.tensor([e0.elapsed_time(e1)], dtype=torch.float64, device="cuda")
+    if world > 1:
+        dist.all_reduce(e2e_ms, op=dist.ReduceOp.MAX)
+    e2e_val = world * T * e2e_steps / (float(e2e_ms.item()) / 1e3)
+    h2d = x_h.numel() * 2 + ids_h.numel() * 4 + rw_h.numel() * 2
+    d2h = out_h.numel() * 2
+    assert torch.equal(out_h.view(torch.int16), out.cpu().view(torch.int16))
+
+    # ------------------------------------------------------------ roofline
+    peak, peak_src = peaks()
+    n_active = batch["n_active"]
+    fc1_b = fc1_bytes(T, n_active)
+    roof = {"kernel": "fc1_kernel", "bound": "hbm", "achieved": None, "peak": peak, "unit": "GB/s", "frac": None,
+            "traffic": None, "peak_source": peak_src,
+            "bytes_per_launch": fc1_b, "bytes_formula": "n_active*1548288 + T*2016 + T*k*216"}
+    if stage:
+        ach = fc1_b / (stage["fc1"] * 1e-3) / 1e9
+        roof.update(achieved=ach, frac=ach / peak)
+        tr = fc1_traffic_from_profile()
+        if tr is not None:
+            roof["traffic"] = tr * (T / 16384)
+    step_b = step_bytes(T, n_active)
+    fwd_roof = {"bytes_per_step": step_b, "achieved": step_b / (ms_per_step * 1e-3) / 1e9}
+    fwd_roof["frac"] = fwd_roof["achieved"] / peak
+
+    # ------------------------------------------------------------ sweep
+    sweep = None
+    if not args.no_sweep and world == 1:
+        sweep = {}
+        flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
+        for name, T_s, routing in (("decode1", 1, "uniform"), ("decode8", 8, "uniform"), ("decode16", 16, "uniform"),
+                                   ("T128", 128, "uniform"), ("T1024", 1024, "uniform"),
+                                   ("prefill", 4096, "zipf")):
+            b = make_batch(gen.full(100 + T_s, T=T_s, routing=routing, weights=False, E=E))
+            ws_s = torch.empty(api.moe_workspace_size(shp, T_s), dtype=torch.uint8, device="cuda")
+            api.moe_prepare_workspace(shp, ws_s, T_s)
+            out_s = torch.empty((T_s, H), dtype=torch.bfloat16, device="cuda")
+            for _ in range(3):
+                forward(b, ws_s, out_s)
+            n_s = 20
+            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_s)]
+            api.moe_profile_start(n_s)
+            for a, c in evs:
+                flush.fill_(1)
+                a.record()
+                forward(b, ws_s, out_s)
+                c.record()
+            torch.cuda.synchronize()
+            st_ms, nc = api.moe_profile_stop()
+            t_ms = statistics.median([a.elapsed_time(c) for a, c in evs])
+            byt = step_bytes(T_s, b["n_active"])
+            sweep[name] = {"T": T_s, "ms": round(t_ms, 4), "tokens_per_s": T_s / (t_ms * 1e-3),
+                           "hbm_frac": byt / (t_ms * 1e-3) / 1e9 / peak, "n_active": b["n_active"],
+                           "fc1_ms": round(st_ms["fc1"] / nc, 4), "fc2_ms": round(st_ms["fc2"] / nc, 4),
+                           "fc1_hbm_frac": fc1_bytes(T_s, b["n_active"]) / (st_ms["fc1"] / nc * 1e-3) / 1e9 / peak}
+        del flush
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        inp_w = gen.full(rank, T=wl["T"], routing=wl["routing"], big_rows_frac=wl["big_rows_frac"], weights=False,
+                         E=E)
+        inp_w.w13, inp_w.sf13, inp_w.w2, inp_w.sf2 = winp.w13, winp.sf13, winp.w2, winp.sf2
+        inp_w.dXdW13, inp_w.qA, inp_w.dAdW2 = winp.dXdW13, winp.qA, winp.dAdW2
+        cpu = cpu_baseline(inp_w)
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "nvfp4 (e2m1 x e4m3-scaled, fp32 accumulate, bf16 out)",
+                "data": "synthetic",
+                "config": {"workload": f"{args.workload}: {wl['text']}", "T": T, "n_active_experts": n_active,
+                           "l2": "inputs larger than L2 (2.08 GB of weights read per step)",
+                           "parallelism": f"replicas x{world} (data parallel, weak scaling)"},
+                "roofline": roof, "forward_roofline": fwd_roof, "stages_ms": stage, "cpu_baseline": cpu,
+                "e2e": {"value": e2e_val, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                        "steps": e2e_steps},
+                "gpu_launches": launches, "clocks": clk, "sweep": sweep}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -75,6 +75,18 @@ moe_status_t moe_workspace_layout(const moe_shape_t* shape, size_t ws_bytes, moe
  * (host out). */
 moe_status_t moe_forward_launch_count(const moe_shape_t* shape, int64_t num_tokens, int32_t* launches);
 
+/* Stage timing (tracing): after moe_profile_start(max_calls), each of the
+ * next max_calls moe_forward calls records a CUDA timing event before each of
+ * its five stages (routing, X quantization, FC1, FC2, finalize) and one after
+ * the last, on the call's stream.  moe_profile_stop synchronizes on those
+ * events, writes the summed milliseconds per stage to stage_ms[0..4] and the
+ * number of recorded calls to *calls (HOST pointers), and frees the events.
+ * Events recorded between stages make the stages run back to back (no launch
+ * overlap across stage boundaries).  Not thread-safe against concurrent
+ * moe_forward calls; not for use inside stream capture. */
+moe_status_t moe_profile_start(int32_t max_calls);
+moe_status_t moe_profile_stop(float* stage_ms, int32_t* calls);
+
 #ifdef __cplusplus
 }
 #endif

@@ -26,7 +26,7 @@ DEVSTAT_INVALID_EXPERT, DEVSTAT_TIMEOUT, DEVSTAT_BAD_TILE = 1, 2, 4
 EXPORTED = ["moe_workspace_size", "moe_prepared_weight_bytes", "moe_prepare_weights", "moe_prepare_workspace",
             "moe_forward", "moe_init_routing", "moe_read_status", "moe_status_string", "moe_test_codec_sweep",
             "moe_test_quantize_rows", "moe_test_situ_requant", "moe_test_requant_lanes", "moe_test_mma_fp4",
-            "moe_workspace_layout", "moe_forward_launch_count"]
+            "moe_workspace_layout", "moe_forward_launch_count", "moe_profile_start", "moe_profile_stop"]
 
 
 class MoeError(RuntimeError):
@@ -82,6 +82,8 @@ def lib():
         "moe_test_mma_fp4": [P, P, P, P, i32, i32, P, P, P],
         "moe_workspace_layout": [S, sz, ctypes.POINTER(moe_ws_layout_t)],
         "moe_forward_launch_count": [S, i64, ctypes.POINTER(i32)],
+        "moe_profile_start": [i32],
+        "moe_profile_stop": [ctypes.POINTER(ctypes.c_float), ctypes.POINTER(i32)],
     }
     for name, args in sig.items():
         fn = getattr(L, name)
@@ -204,3 +206,18 @@ def moe_forward_launch_count(shp, num_tokens: int) -> int:
     _check(lib().moe_forward_launch_count(ctypes.byref(shp), num_tokens, ctypes.byref(out)),
            "moe_forward_launch_count")
     return out.value
+
+
+STAGES = ("routing", "quant_x", "fc1", "fc2", "finalize")
+
+
+def moe_profile_start(max_calls: int):
+    _check(lib().moe_profile_start(max_calls), "moe_profile_start")
+
+
+def moe_profile_stop():
+    """Returns ({stage: summed ms}, calls)."""
+    ms = (ctypes.c_float * 5)()
+    calls = ctypes.c_int32()
+    _check(lib().moe_profile_stop(ms, ctypes.byref(calls)), "moe_profile_stop")
+    return dict(zip(STAGES, [float(v) for v in ms])), calls.value

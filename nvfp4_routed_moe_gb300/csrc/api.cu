@@ -206,6 +206,27 @@ static RouteArgs route_args(const Shape& s, const WsLayout& L, uint8_t* ws, cons
 
 static int forward_launches(int64_t P) { return (P <= kRouteSmallMax ? 1 : 2) + 4; }
 
+// ------------------------------------------------------------ stage timing
+// While a profile is open, every moe_forward records a timing event before
+// each stage and one after the last, from a pool created by moe_profile_start.
+constexpr int kStages = 5;  // routing, quant X, FC1, FC2, finalize
+struct Profile {
+  bool on = false;
+  int max_calls = 0, calls = 0;
+  std::vector<cudaEvent_t> ev;  // (kStages + 1) per call
+};
+static Profile g_prof;
+
+static void prof_mark(int stage, cudaStream_t st) {
+  if (!g_prof.on || g_prof.calls >= g_prof.max_calls) return;
+  cudaEventRecord(g_prof.ev[(size_t)g_prof.calls * (kStages + 1) + stage], st);
+}
+static void prof_end_call(cudaStream_t st) {
+  if (!g_prof.on || g_prof.calls >= g_prof.max_calls) return;
+  prof_mark(kStages, st);
+  ++g_prof.calls;
+}
+
 }  // namespace moe
 
 using namespace moe;
@@ -339,6 +360,7 @@ moe_status_t moe_forward(const moe_shape_t* shape, int64_t num_tokens, const voi
   }
 
   // 1. routing
+  prof_mark(0, stream);
   RouteArgs ra = route_args(s, L, w, expert_ids, T);
   int nl = 0;
   MOE_CUDA(launch_routing(ra, stream, &nl));
@@ -355,6 +377,7 @@ moe_status_t moe_forward(const moe_shape_t* shape, int64_t num_tokens, const voi
   qa.H = s.H;
   qa.k = s.k;
   qa.max_rows = L.PpadMax;
+  prof_mark(1, stream);
   MOE_CUDA(launch_quant_x(qa, stream));
 
   // 3. FC1 + SiTU + requant
@@ -377,6 +400,7 @@ moe_status_t moe_forward(const moe_shape_t* shape, int64_t num_tokens, const voi
   f1.max_tiles = (int32_t)L.TTmax;
   f1.max_rows = L.PpadMax;
   const int grid1 = (int)std::min<int64_t>(sms, tt * NIT);
+  prof_mark(2, stream);
   MOE_CUDA(launch_fc1(tm_w13, tm_xq, f1, grid1, stream));
 
   // 4. FC2 + weighted combine into the fp32 accumulator
@@ -398,11 +422,14 @@ moe_status_t moe_forward(const moe_shape_t* shape, int64_t num_tokens, const voi
   f2.max_rows = L.PpadMax;
   f2.num_pairs = P;
   const int grid2 = (int)std::min<int64_t>(sms, tt * NMT);
+  prof_mark(3, stream);
   MOE_CUDA(launch_fc2(tm_w2, tm_aq, f2, grid2, stream));
 
   // 5. BF16 finalize
+  prof_mark(4, stream);
   MOE_CUDA(launch_finalize(reinterpret_cast<const float*>(w + L.out_f32), static_cast<uint16_t*>(out), T * s.H, sms,
                            stream));
+  prof_end_call(stream);
   return MOE_OK;
 }
 
@@ -572,6 +599,43 @@ moe_status_t moe_workspace_layout(const moe_shape_t* shape, size_t ws_bytes, moe
   out->out_f32 = (int64_t)L.out_f32;
   out->total = (int64_t)L.total;
   return MOE_OK;
+}
+
+moe_status_t moe_profile_start(int32_t max_calls) {
+  if (max_calls < 1 || max_calls > 100000) return MOE_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (g_prof.on) return MOE_ERR_INVALID_ARG;
+  g_prof.ev.assign((size_t)max_calls * (kStages + 1), nullptr);
+  for (auto& e : g_prof.ev)
+    if (cudaEventCreate(&e) != cudaSuccess) return MOE_ERR_CUDA;
+  g_prof.max_calls = max_calls;
+  g_prof.calls = 0;
+  g_prof.on = true;
+  return MOE_OK;
+}
+
+moe_status_t moe_profile_stop(float* stage_ms, int32_t* calls) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (!g_prof.on) return MOE_ERR_INVALID_ARG;
+  moe_status_t st = MOE_OK;
+  float acc[kStages] = {0, 0, 0, 0, 0};
+  for (int c = 0; c < g_prof.calls && st == MOE_OK; ++c) {
+    cudaEvent_t* e = &g_prof.ev[(size_t)c * (kStages + 1)];
+    if (cudaEventSynchronize(e[kStages]) != cudaSuccess) st = MOE_ERR_CUDA;
+    for (int i = 0; i < kStages && st == MOE_OK; ++i) {
+      float ms = 0.f;
+      if (cudaEventElapsedTime(&ms, e[i], e[i + 1]) != cudaSuccess) st = MOE_ERR_CUDA;
+      acc[i] += ms;
+    }
+  }
+  if (stage_ms)
+    for (int i = 0; i < kStages; ++i) stage_ms[i] = acc[i];
+  if (calls) *calls = g_prof.calls;
+  for (auto& e : g_prof.ev) cudaEventDestroy(e);
+  g_prof.ev.clear();
+  g_prof.on = false;
+  g_prof.calls = g_prof.max_calls = 0;
+  return st;
 }
 
 moe_status_t moe_forward_launch_count(const moe_shape_t* shape, int64_t num_tokens, int32_t* launches) {

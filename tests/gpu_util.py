@@ -48,23 +48,27 @@ class Model:
         n = api.moe_workspace_size(self.shape, max_tokens)
         return torch.empty(n, dtype=torch.uint8, device="cuda")
 
-    def forward(self, x, ids, rw, ws=None, T=None, beta=None, lam=None, out=None, prepare=True):
+    def forward(self, x, ids, rw, ws=None, T=None, beta=None, lam=None, out=None, prepare=True, qX=None):
         T = T if T is not None else x.shape[0]
+        qX = self.qX if qX is None else qX
         if ws is None:
             ws = self.workspace(T)
         if prepare:
             api.moe_prepare_workspace(self.shape, ws, T)
         if out is None:
             out = torch.empty((T, self.inp.H), dtype=torch.bfloat16, device="cuda")
-        api.moe_forward(self.shape, T, x, ids, rw, self.w13, self.sf13, self.w2, self.sf2, self.qX, self.dXdW13,
+        api.moe_forward(self.shape, T, x, ids, rw, self.w13, self.sf13, self.w2, self.sf2, qX, self.dXdW13,
                         self.qA, self.dAdW2, beta, lam, ws, out)
         return out, ws
 
     def forward_inputs(self, inp: gen.MoEInputs | None = None, **kw):
+        """Forward of `inp`'s activations, routing and qX (weights and
+        per-expert scales are the model's)."""
         inp = inp or self.inp
         x = dev(inp.x, torch.bfloat16)
         ids = dev(inp.expert_ids)
         rw = dev(inp.route_weights, torch.bfloat16)
+        kw.setdefault("qX", dev(np.array([inp.qX], np.float32)))
         return self.forward(x, ids, rw, **kw)
 
 

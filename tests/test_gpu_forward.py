@@ -161,8 +161,11 @@ def test_workspace_reuse_across_token_counts(tiny):
 
 
 def test_not_prepared_is_rejected(tiny):
+    """A workspace never passed to moe_prepare_workspace for this T is
+    refused (its byte size is unique in this module, so no earlier prepared
+    entry with a recycled address can match)."""
     inp, m = tiny
-    ws = m.workspace(inp.T)
+    ws = m.workspace(inp.T + 61)
     with pytest.raises(api.MoeError) as e:
         m.forward_inputs(ws=ws, prepare=False)
     assert e.value.status == 4
@@ -192,6 +195,7 @@ def test_cuda_graph_replay(tiny):
     inp2 = cases.prepare_tiny(0)
     inp2.x = gen.draw_x(9, inp.T, inp.H)
     inp2.expert_ids = gen.draw_ids_uniform(9, inp.T, inp.E, inp.k)
+    inp2.qX = inp.qX          # the captured graph keeps reading the same qX buffer
     x.copy_(dev(inp2.x, torch.bfloat16))
     ids.copy_(dev(inp2.expert_ids))
     g.replay()
