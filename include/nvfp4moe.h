@@ -137,6 +137,29 @@ moe_status_t moe_init_routing(const moe_shape_t* shape, int64_t num_rows, const 
                               int32_t* tokens_cumsum_or_count, float* expanded_scale, void* ws, size_t ws_bytes,
                               cudaStream_t stream);
 
+/* Init-routing without a workspace, for callers that cannot allocate device
+ * memory (code running inside an allocator or memory-pool callback, plug-ins
+ * under a framework that owns every device allocation, processes that must
+ * not grow their device footprint after start-up).  The pages have no
+ * counterpart of this entry point.  Same arguments, outputs and kernels as
+ * moe_init_routing, minus ws/ws_bytes: the routing scratch lives in one
+ * 2 MiB static device array of the library, held by every GPU that loads it
+ * until the process exits.
+ *  - Limits: num_rows * top_k <= 65536 routed pairs and num_experts <= 1024;
+ *    larger calls return MOE_ERR_WORKSPACE_TOO_SMALL and launch nothing.
+ *  - The first call on each device looks up the array's device address and
+ *    sets kernel attributes (no allocation); make that first call before any
+ *    stream capture.
+ *  - Every call on a device shares the one array and clears its header on
+ *    entry; calls whose work overlaps on the GPU (different streams, other
+ *    threads) race on it.  Serialize them.
+ *  - The device status word (skipped ids) is kept in the shared array and is
+ *    not reported by this entry point. */
+moe_status_t moe_init_routing_static(const moe_shape_t* shape, int64_t num_rows, const void* x,
+                                     const int32_t* expert_ids, const moe_routing_opts_t* opts, void* expanded_x,
+                                     int32_t* expanded_row_idx, int32_t* tokens_cumsum_or_count,
+                                     float* expanded_scale, cudaStream_t stream);
+
 /* Test helper: synchronizes `stream`, copies the device status word and the
  * count of skipped expert ids to host_status[0..1] (HOST pointer) and clears
  * them.  Returns MOE_ERR_DEVICE_STATUS if the status word was non-zero. */

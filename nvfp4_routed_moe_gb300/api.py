@@ -24,7 +24,7 @@ STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
 DEVSTAT_INVALID_EXPERT, DEVSTAT_TIMEOUT, DEVSTAT_BAD_TILE = 1, 2, 4
 
 EXPORTED = ["moe_workspace_size", "moe_prepared_weight_bytes", "moe_prepare_weights", "moe_prepare_workspace",
-            "moe_forward", "moe_init_routing", "moe_read_status", "moe_status_string", "moe_test_codec_sweep",
+            "moe_forward", "moe_init_routing", "moe_init_routing_static", "moe_read_status", "moe_status_string", "moe_test_codec_sweep",
             "moe_test_quantize_rows", "moe_test_situ_requant", "moe_test_requant_lanes", "moe_test_mma_fp4",
             "moe_workspace_layout", "moe_forward_launch_count", "moe_profile_start", "moe_profile_stop"]
 
@@ -74,6 +74,7 @@ def lib():
         "moe_prepare_workspace": [S, P, sz, i64, P],
         "moe_forward": [S, i64] + [P] * 13 + [P, sz, P, P],
         "moe_init_routing": [S, i64, P, P, ctypes.POINTER(moe_routing_opts_t), P, P, P, P, P, sz, P],
+        "moe_init_routing_static": [S, i64, P, P, ctypes.POINTER(moe_routing_opts_t), P, P, P, P, P],
         "moe_read_status": [P, P, P],
         "moe_test_codec_sweep": [u32, i64, P, P, P, P],
         "moe_test_quantize_rows": [P, i64, i32, P, P, P, P],
@@ -157,6 +158,13 @@ def moe_init_routing(shp, num_rows, x, expert_ids, opts: moe_routing_opts_t, exp
     _check(lib().moe_init_routing(ctypes.byref(shp), num_rows, _p(x), _p(expert_ids), ctypes.byref(opts),
                                   _p(expanded_x), _p(expanded_row_idx), _p(tokens_cumsum_or_count),
                                   _p(expanded_scale), _p(ws), _nbytes(ws), _stream(stream)), "moe_init_routing")
+
+
+def moe_init_routing_static(shp, num_rows, x, expert_ids, opts: moe_routing_opts_t, expanded_x, expanded_row_idx,
+                            tokens_cumsum_or_count, expanded_scale, stream=None):
+    _check(lib().moe_init_routing_static(ctypes.byref(shp), num_rows, _p(x), _p(expert_ids), ctypes.byref(opts),
+                                         _p(expanded_x), _p(expanded_row_idx), _p(tokens_cumsum_or_count),
+                                         _p(expanded_scale), _stream(stream)), "moe_init_routing_static")
 
 
 def moe_read_status(ws, stream=None):
