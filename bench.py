@@ -378,15 +378,19 @@ def main():
                 forward(b, ws_s, out_s)
             n_s = 20
             evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_s)]
-            api.moe_profile_start(n_s)
             for a, c in evs:
                 flush.fill_(1)
                 a.record()
                 forward(b, ws_s, out_s)
                 c.record()
             torch.cuda.synchronize()
-            st_ms, nc = api.moe_profile_stop()
             t_ms = statistics.median([a.elapsed_time(c) for a, c in evs])
+            api.moe_profile_start(n_s)           # stage breakdown in a separate pass
+            for _ in range(n_s):
+                flush.fill_(1)
+                forward(b, ws_s, out_s)
+            torch.cuda.synchronize()
+            st_ms, nc = api.moe_profile_stop()
             byt = step_bytes(T_s, b["n_active"])
             sweep[name] = {"T": T_s, "ms": round(t_ms, 4), "tokens_per_s": T_s / (t_ms * 1e-3),
                            "hbm_frac": byt / (t_ms * 1e-3) / 1e9 / peak, "n_active": b["n_active"],

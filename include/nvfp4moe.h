@@ -58,8 +58,8 @@ typedef struct {
 /* Workspace bytes for any token count 1..max_tokens ("Cake SiTU backend",
  * "The size query uses host metadata only").  *bytes is a HOST pointer.
  * The workspace holds the routing arrays, the quantized activations, the
- * quantized intermediate, an fp32 output accumulator and the default SiTU
- * constants.  Its carve-up depends only on the shape and its byte size, so
+ * quantized intermediate, the fp32 FC2 output of every routed pair and the
+ * default SiTU constants.  Its carve-up depends only on the shape and its byte size, so
  * a maximum-size workspace serves every smaller token count. */
 moe_status_t moe_workspace_size(const moe_shape_t* shape, int64_t max_tokens, size_t* bytes);
 

@@ -62,11 +62,12 @@ moe_status_t moe_test_mma_fp4(const uint8_t* a, const uint8_t* sfa_atoms, const 
  * intermediates in tests (host out struct).  Routing arrays are int32;
  * xq/aq are packed codes of padded expanded rows ([rows, H/2] / [rows, I/2]);
  * sfx/sfa are their block scales in the 128x4 atom layout; row_pos maps a
- * flat pair t*k+j to its padded row. */
+ * flat pair t*k+j to its padded row; y [rows, H] fp32 holds each routed
+ * pair's route-weighted FC2 output. */
 typedef struct {
   int64_t max_tokens, pairs_max, padded_rows_max, tiles_max;
   int64_t header, count, cumsum, offs, poffs, sorted_row, gather, row_pos, prow_pair, tt_list;
-  int64_t xq, sfx, aq, sfa, out_f32, total;
+  int64_t xq, sfx, aq, sfa, y, total;
 } moe_ws_layout_t;
 
 moe_status_t moe_workspace_layout(const moe_shape_t* shape, size_t ws_bytes, moe_ws_layout_t* layout);

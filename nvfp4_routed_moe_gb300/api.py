@@ -49,7 +49,7 @@ class moe_ws_layout_t(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int64) for n in
                 ("max_tokens", "pairs_max", "padded_rows_max", "tiles_max", "header", "count", "cumsum", "offs",
                  "poffs", "sorted_row", "gather", "row_pos", "prow_pair", "tt_list", "xq", "sfx", "aq", "sfa",
-                 "out_f32", "total")]
+                 "y", "total")]
 
 
 def shape(hidden: int, inter: int, num_experts: int, top_k: int) -> moe_shape_t:

@@ -19,7 +19,8 @@ cudaError_t routing_set_attributes(int E);
 cudaError_t launch_init_move(const InitMoveArgs& a, cudaStream_t st);
 cudaError_t launch_init_finish(const InitFinishArgs& a, cudaStream_t st, int num_sms);
 cudaError_t launch_quant_x(const QuantXArgs& a, cudaStream_t st);
-cudaError_t launch_finalize(const float* acc, uint16_t* out, int64_t n, int num_sms, cudaStream_t st);
+cudaError_t launch_finalize(const float* y, const int32_t* row_pos, uint16_t* out, int64_t T, int H, int k,
+                            int64_t max_rows, int num_sms, cudaStream_t st);
 cudaError_t launch_prep(const PrepArgs& a, cudaStream_t st, int num_sms);
 cudaError_t launch_codec_sweep(uint32_t start, int64_t n, uint8_t* lo, uint8_t* hi, uint8_t* e4, cudaStream_t st,
                                int num_sms);
@@ -30,8 +31,8 @@ cudaError_t launch_situ_requant(const float* z, int64_t rows, int I, float qA, f
 cudaError_t launch_requant_lanes(const float* act, int64_t rows, int I, float qA, uint8_t* packed, uint8_t* sf,
                                  cudaStream_t st);
 cudaError_t gemm_set_attributes();
-cudaError_t launch_fc1(const CUtensorMap& w13, const CUtensorMap& xq, const Fc1Args& a, int grid, cudaStream_t st);
-cudaError_t launch_fc2(const CUtensorMap& w2, const CUtensorMap& aq, const Fc2Args& a, int grid, cudaStream_t st);
+cudaError_t launch_fc1(const CUtensorMap& w13, const RowMaps& xq, const Fc1Args& a, int grid, cudaStream_t st);
+cudaError_t launch_fc2(const CUtensorMap& w2, const RowMaps& aq, const Fc2Args& a, int grid, cudaStream_t st);
 cudaError_t launch_mma_check(const CUtensorMap& a, const CUtensorMap& b, const uint8_t* sfa, const uint8_t* sfb,
                              int N, int K, float* d, int32_t* status, cudaStream_t st);
 
@@ -127,6 +128,20 @@ static bool make_map(CUtensorMap* m, const void* base, int rank, const uint64_t*
                   CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
+}
+
+// Row-major [rows, row_bytes] byte matrix seen through boxes of inner_bytes x
+// {16, 32, 64, 128} rows.
+static bool make_row_maps(RowMaps* m, const void* base, uint64_t row_bytes, uint64_t rows, uint32_t inner_bytes,
+                          CUtensorMapSwizzle sw) {
+  const uint64_t d[2] = {row_bytes, rows};
+  const uint64_t str[1] = {row_bytes};
+  CUtensorMap* out[4] = {&m->m16, &m->m32, &m->m64, &m->m128};
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t box[2] = {inner_bytes, (uint32_t)(kTokChunk << i)};
+    if (!make_map(out[i], base, 2, d, str, box, sw)) return false;
+  }
+  return true;
 }
 
 // ------------------------------------------------------------ validation
@@ -331,33 +346,26 @@ moe_status_t moe_forward(const moe_shape_t* shape, int64_t num_tokens, const voi
   MOE_CUDA(device_ready(&sms));
   uint8_t* w = static_cast<uint8_t*>(ws);
   const int64_t T = num_tokens, P = T * s.k;
-  const int NIT = s.I / 128, NKB = s.H / kFc1KBlock, NMT = s.H / 128, NKB2 = s.I / kFc2KBlock;
+  const int NIT = s.I / 64, NKB = s.H / kFc1KBlock, NMT = s.H / 128, NKB2 = s.I / kFc2KBlock;
 
-  CUtensorMap tm_w13, tm_xq, tm_w2, tm_aq;
+  CUtensorMap tm_w13, tm_w2;
+  RowMaps tm_xq, tm_aq;
   {
-    const uint64_t d[3] = {128, 256, (uint64_t)s.E * NIT * NKB};
-    const uint64_t str[2] = {128, 32768};
-    const uint32_t box[3] = {128, 256, 1};
+    const uint64_t d[3] = {128, 128, (uint64_t)s.E * NIT * NKB};
+    const uint64_t str[2] = {128, 16384};
+    const uint32_t box[3] = {128, 128, 1};
     if (!make_map(&tm_w13, w13, 3, d, str, box, CU_TENSOR_MAP_SWIZZLE_128B)) return MOE_ERR_CUDA;
   }
-  {
-    const uint64_t d[2] = {(uint64_t)s.H / 2, (uint64_t)L.PpadMax};
-    const uint64_t str[1] = {(uint64_t)s.H / 2};
-    const uint32_t box[2] = {128, (uint32_t)kTokChunk};
-    if (!make_map(&tm_xq, w + L.xq, 2, d, str, box, CU_TENSOR_MAP_SWIZZLE_128B)) return MOE_ERR_CUDA;
-  }
+  if (!make_row_maps(&tm_xq, w + L.xq, (uint64_t)s.H / 2, (uint64_t)L.PpadMax, 128, CU_TENSOR_MAP_SWIZZLE_128B))
+    return MOE_ERR_CUDA;
   {
     const uint64_t d[3] = {64, 128, (uint64_t)s.E * NMT * NKB2};
     const uint64_t str[2] = {64, 8192};
     const uint32_t box[3] = {64, 128, 1};
     if (!make_map(&tm_w2, w2, 3, d, str, box, CU_TENSOR_MAP_SWIZZLE_64B)) return MOE_ERR_CUDA;
   }
-  {
-    const uint64_t d[2] = {(uint64_t)s.I / 2, (uint64_t)L.PpadMax};
-    const uint64_t str[1] = {(uint64_t)s.I / 2};
-    const uint32_t box[2] = {64, (uint32_t)kTokChunk};
-    if (!make_map(&tm_aq, w + L.aq, 2, d, str, box, CU_TENSOR_MAP_SWIZZLE_64B)) return MOE_ERR_CUDA;
-  }
+  if (!make_row_maps(&tm_aq, w + L.aq, (uint64_t)s.I / 2, (uint64_t)L.PpadMax, 64, CU_TENSOR_MAP_SWIZZLE_64B))
+    return MOE_ERR_CUDA;
 
   // 1. routing
   prof_mark(0, stream);
@@ -365,14 +373,15 @@ moe_status_t moe_forward(const moe_shape_t* shape, int64_t num_tokens, const voi
   int nl = 0;
   MOE_CUDA(launch_routing(ra, stream, &nl));
 
-  // 2. quantize X into the padded expanded rows, zero the fp32 accumulator
+  // 2. quantize X into the padded expanded rows
   QuantXArgs qa{};
   qa.x = static_cast<const uint16_t*>(x);
   qa.row_pos = ra.row_pos;
+  qa.route_w = static_cast<const uint16_t*>(route_weights);
+  qa.wrow = reinterpret_cast<float*>(w + L.wrow);
   qa.qX = qX;
   qa.xq = w + L.xq;
   qa.sfx = w + L.sfx;
-  qa.out_f32 = reinterpret_cast<float*>(w + L.out_f32);
   qa.T = T;
   qa.H = s.H;
   qa.k = s.k;
@@ -403,16 +412,16 @@ moe_status_t moe_forward(const moe_shape_t* shape, int64_t num_tokens, const voi
   prof_mark(2, stream);
   MOE_CUDA(launch_fc1(tm_w13, tm_xq, f1, grid1, stream));
 
-  // 4. FC2 + weighted combine into the fp32 accumulator
+  // 4. FC2: route-weighted fp32 rows of every routed pair
   Fc2Args f2{};
   f2.sf2p = sf2;
   f2.sfa = w + L.sfa;
   f2.tt_list = ra.tt_list;
   f2.hdr = ra.hdr;
   f2.prow_pair = ra.prow_pair;
-  f2.route_w = static_cast<const uint16_t*>(route_weights);
+  f2.wrow = reinterpret_cast<const float*>(w + L.wrow);
   f2.dAdW2 = dA_dW2;
-  f2.out_f32 = reinterpret_cast<float*>(w + L.out_f32);
+  f2.y = reinterpret_cast<float*>(w + L.y);
   f2.status = ra.hdr + HDR_STATUS;
   f2.H = s.H;
   f2.I = s.I;
@@ -425,10 +434,10 @@ moe_status_t moe_forward(const moe_shape_t* shape, int64_t num_tokens, const voi
   prof_mark(3, stream);
   MOE_CUDA(launch_fc2(tm_w2, tm_aq, f2, grid2, stream));
 
-  // 5. BF16 finalize
+  // 5. BF16 finalize: sum of each token's k rows
   prof_mark(4, stream);
-  MOE_CUDA(launch_finalize(reinterpret_cast<const float*>(w + L.out_f32), static_cast<uint16_t*>(out), T * s.H, sms,
-                           stream));
+  MOE_CUDA(launch_finalize(reinterpret_cast<const float*>(w + L.y), ra.row_pos, static_cast<uint16_t*>(out), T, s.H,
+                           s.k, L.PpadMax, sms, stream));
   prof_end_call(stream);
   return MOE_OK;
 }
@@ -596,7 +605,7 @@ moe_status_t moe_workspace_layout(const moe_shape_t* shape, size_t ws_bytes, moe
   out->sfx = (int64_t)L.sfx;
   out->aq = (int64_t)L.aq;
   out->sfa = (int64_t)L.sfa;
-  out->out_f32 = (int64_t)L.out_f32;
+  out->y = (int64_t)L.y;
   out->total = (int64_t)L.total;
   return MOE_OK;
 }

@@ -6,21 +6,29 @@
 // and decode-sized groups still fill the 128-row MMA.
 //
 // FC1 ("Cake SiTU backend": FC1 over gate and up, SiTU, intermediate NVFP4
-// requantization): per work unit (token tile, intermediate tile of 128
-// features) two accumulators D_g, D_u [128 features x N tokens] in TMEM
-// collect K = H over k-blocks of 256 FP4 elements; the epilogue computes
-// z = acc * dX*dW13[e], a = SiTU(z_g, z_u), and quantizes a per 16 features
-// with qA[e] into the padded expanded rows of A (codes + atom-layout scales).
+// requantization): a prepared W13 tile holds 64 intermediate features with
+// gate and up rows interleaved (row 2i = gate of feature i, row 2i+1 = up),
+// so the two halves of one feature land in neighbouring TMEM lanes of the
+// same warp.  Per work unit (token tile, 64 features) one accumulator
+// [128 rows x N tokens] collects K = H over k-blocks of 256 FP4 elements;
+// accumulators are double-buffered in TMEM so the epilogue of one unit runs
+// under the MMAs of the next.  The epilogue forms z = acc * dX*dW13[e],
+// a = SiTU(z_g, z_u) (one shuffle pairs g and u; even lanes take one token
+// column, odd lanes the next), and quantizes a per 16 features with qA[e]
+// into the padded expanded rows of A (codes + atom-layout scales).
 //
 // FC2 ("Cake SiTU backend": FC2, BF16 weighted finalization): per work unit
 // (token tile, 128 output features) one accumulator [128 x N] over K = I in
 // k-blocks of 128; the epilogue scales by dA*dW2[e] and the route weight and
-// adds the result into the fp32 [T, H] accumulator (one red per element).
+// stores each routed pair's 128 outputs into its padded row of the fp32 y
+// buffer (one coalesced 128-byte store per warp and token).  The finalize
+// kernel adds a token's k rows.
 //
-// Warp roles (320 threads): warp 0 issues TMA, warp 1 owns TMEM and issues
-// MMAs, warps 2..9 drain TMEM (two warps per 32-lane quarter, alternating
-// 16-column chunks).  Persistent CTAs stride over the work units; the stage
-// ring and the barrier phases carry across units.  Every wait is bounded.
+// Warp roles: warp 0 issues TMA, warp 1 owns TMEM and issues MMAs, the
+// remaining warps drain TMEM (each 32-lane quarter by several warps taking
+// alternate 16-column chunks).  Persistent CTAs stride over the work units;
+// the stage ring and the barrier phases carry across units.  Every wait is
+// bounded.
 #include "nvfp4.cuh"
 #include "plan.h"
 
@@ -28,19 +36,21 @@ namespace moe {
 
 cudaError_t launch_with_pdl(const void* fn, dim3 grid, dim3 block, size_t smem, cudaStream_t st, void** args);
 
-constexpr int kThreads = 320;
-constexpr int kEpiWarps = 8;
 constexpr uint32_t kTmemCols = 512;
 
-// FC1 stage: A gate [128 x 128 B] | A up [128 x 128 B] | B [128 x 128 B] |
-// SF gate 4 atoms | SF up 4 atoms | SF tokens 4 atoms.
-constexpr int kFc1Stages = 4;
-constexpr int F1_AG = 0, F1_AU = 16384, F1_B = 32768, F1_SG = 49152, F1_SU = 51200, F1_SB = 53248;
-constexpr int kFc1StageBytes = 55296;
+// FC1 stage: A [128 interleaved gate/up rows x 128 B] | B [128 tokens x 128 B] |
+// SF A 4 atoms | SF B 4 atoms.
+constexpr int kFc1Stages = 6;
+constexpr int F1_A = 0, F1_B = 16384, F1_SA = 32768, F1_SB = 34816;
+constexpr int kFc1StageBytes = 36864;
+constexpr int kFc1EpiWarps = 16;
+constexpr int kFc1Threads = 64 + 32 * kFc1EpiWarps;
 // FC2 stage: A [128 x 64 B] | B [128 x 64 B] | SF A 2 atoms | SF B 2 atoms.
 constexpr int kFc2Stages = 12;
 constexpr int F2_A = 0, F2_B = 8192, F2_SA = 16384, F2_SB = 17408;
 constexpr int kFc2StageBytes = 18432;
+constexpr int kFc2EpiWarps = 8;
+constexpr int kFc2Threads = 64 + 32 * kFc2EpiWarps;
 
 struct Barriers {
   uint64_t full[16];
@@ -55,13 +65,32 @@ struct Barriers {
 constexpr size_t kFc1Smem = (size_t)kFc1Stages * kFc1StageBytes + sizeof(Barriers) + 1024;
 constexpr size_t kFc2Smem = (size_t)kFc2Stages * kFc2StageBytes + sizeof(Barriers) + 1024;
 
+// Activation rows of a tile arrive in boxes of 128, 64, 32 or 16 rows,
+// largest first: at most four copies per k-block.
+
+__device__ __forceinline__ void load_rows(uint8_t* dst, const RowMaps& maps, int32_t x, int32_t row0, int nch,
+                                          uint32_t chunk_bytes, uint64_t* bar) {
+  int r = 0;
+  while (r < nch) {
+    const int left = nch - r;
+    const CUtensorMap* m;
+    int n;
+    if (left >= 8) { m = &maps.m128; n = 8; }
+    else if (left >= 4) { m = &maps.m64; n = 4; }
+    else if (left >= 2) { m = &maps.m32; n = 2; }
+    else { m = &maps.m16; n = 1; }
+    tma_load_2d(dst + r * chunk_bytes, m, x, row0 + r * kTokChunk, bar);
+    r += n;
+  }
+}
+
 __device__ __forceinline__ uint8_t* aligned_smem(uint8_t* raw) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~static_cast<uintptr_t>(1023));
 }
 
 __device__ __forceinline__ uint64_t sf_desc(const uint8_t* p) { return smem_desc(smem_u32(p), 0, 128, kLayoutNone); }
 
-template <int STAGES>
+template <int STAGES, int EPI_WARPS>
 __device__ void gemm_setup(Barriers* bars, int warp) {
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -70,7 +99,7 @@ __device__ void gemm_setup(Barriers* bars, int warp) {
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&bars->tmem_full[b], 1);
-      mbar_init(&bars->tmem_empty[b], kEpiWarps);
+      mbar_init(&bars->tmem_empty[b], EPI_WARPS);
     }
     mbar_init(&bars->drain, 1);
     bars->abort_flag = 0;
@@ -103,20 +132,34 @@ __device__ __forceinline__ bool tile_ok(const int4& t, int E, int64_t max_rows) 
 
 __device__ __forceinline__ int clamp_tiles(int n, int max_tiles) { return n < 0 ? 0 : (n > max_tiles ? max_tiles : n); }
 
+// Tile descriptor of work unit `unit` (units_per_tile units share a token
+// tile), or an invalid descriptor past the end.  Issued one or two units
+// ahead so the load latency hides under the current unit.
+__device__ __forceinline__ int4 next_tile(const int4* tiles, int unit, int num_units, int units_per_tile) {
+  return unit < num_units ? tiles[unit / units_per_tile] : make_int4(-1, 0, 0, 0);
+}
+
+// dX*dW13, qA, beta, lambda of the expert of a tile (zeros for an invalid tile).
+__device__ __forceinline__ float4 unit_scalars(const Fc1Args& p, const int4& t) {
+  if (t.x < 0 || t.x >= p.E) return make_float4(0.f, 0.f, 0.f, 0.f);
+  return make_float4(__ldg(p.dXdW13 + t.x), __ldg(p.qA + t.x), __ldg(p.beta + t.x), __ldg(p.lam + t.x));
+}
+
 // ================================================================== FC1
-__global__ void __launch_bounds__(kThreads, 1)
-    fc1_kernel(const __grid_constant__ CUtensorMap tm_w13, const __grid_constant__ CUtensorMap tm_xq,
+__global__ void __launch_bounds__(kFc1Threads, 1)
+    fc1_kernel(const __grid_constant__ CUtensorMap tm_w13, const __grid_constant__ RowMaps tm_xq,
                const Fc1Args p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = aligned_smem(smem_raw);
   Barriers* bars = reinterpret_cast<Barriers*>(smem + kFc1Stages * kFc1StageBytes);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int NIT = p.I / 128, NKB = p.H / kFc1KBlock;
+  const int NIT = p.I / 64, NKB = p.H / kFc1KBlock;
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tm_w13);
-    tma_prefetch_desc(&tm_xq);
+    tma_prefetch_desc(&tm_xq.m16);
+    tma_prefetch_desc(&tm_xq.m128);
   }
-  gemm_setup<kFc1Stages>(bars, warp);
+  gemm_setup<kFc1Stages, kFc1EpiWarps>(bars, warp);
   const uint32_t tmem = bars->tmem_base;
   pdl_wait();
   pdl_launch_dependents();
@@ -129,8 +172,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t stage = 0, phase = 0;
       uint32_t armed = 0, last_phase = 0;  // bit s: stage s armed; its last armed phase
       bool ok = true;
+      int4 nxt = next_tile(tiles, blockIdx.x, num_units, NIT);
       for (int unit = blockIdx.x; unit < num_units && ok; unit += gridDim.x) {
-        const int4 tl = tiles[unit / NIT];
+        const int4 tl = nxt;
+        nxt = next_tile(tiles, unit + gridDim.x, num_units, NIT);   // in flight while this unit streams
         const int it = unit % NIT;
         if (!tile_ok(tl, p.E, p.max_rows)) {
           set_status(p.status, DEVSTAT_BAD_TILE);
@@ -138,7 +183,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const int e = tl.x, row0 = tl.y, rows = tl.z;
         const int nch = (rows + kTokChunk - 1) / kTokChunk;
-        const uint32_t tx = 32768u + (uint32_t)nch * 2048u + 4096u + 2048u;
+        const uint32_t tx = 16384u + (uint32_t)nch * 2048u + 2048u + 2048u;
         for (int kb = 0; kb < NKB; ++kb) {
           if (!wait_or_abort(&bars->empty[stage], phase ^ 1u, bars, p.status)) {
             ok = false;
@@ -148,10 +193,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive_expect_tx(&bars->full[stage], tx);
           armed |= 1u << stage;
           last_phase = (last_phase & ~(1u << stage)) | (phase << stage);
-          tma_load_3d(st + F1_AG, &tm_w13, 0, 0, (e * NIT + it) * NKB + kb, &bars->full[stage]);
-          for (int c = 0; c < nch; ++c)
-            tma_load_2d(st + F1_B + c * 2048, &tm_xq, kb * 128, row0 + c * kTokChunk, &bars->full[stage]);
-          bulk_g2s(st + F1_SG, p.sf13p + (size_t)((e * NIT + it) * NKB + kb) * 4096u, 4096u, &bars->full[stage]);
+          tma_load_3d(st + F1_A, &tm_w13, 0, 0, (e * NIT + it) * NKB + kb, &bars->full[stage]);
+          load_rows(st + F1_B, tm_xq, kb * 128, row0, nch, 2048u, &bars->full[stage]);
+          bulk_g2s(st + F1_SA, p.sf13p + (size_t)((e * NIT + it) * NKB + kb) * 2048u, 2048u, &bars->full[stage]);
           bulk_g2s(st + F1_SB, p.sfx + ((size_t)(row0 >> 7) * (p.H / 64) + (size_t)kb * 4) * 512u, 2048u,
                    &bars->full[stage]);
           if (++stage == kFc1Stages) {
@@ -170,13 +214,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t stage = 0, phase = 0;
       int local = 0;
       bool ok = true;
+      int4 nxt = next_tile(tiles, blockIdx.x, num_units, NIT);
       for (int unit = blockIdx.x; unit < num_units && ok; unit += gridDim.x) {
-        const int4 tl = tiles[unit / NIT];
+        const int4 tl = nxt;
+        nxt = next_tile(tiles, unit + gridDim.x, num_units, NIT);
         if (!tile_ok(tl, p.E, p.max_rows)) continue;
         const uint32_t ncols = (uint32_t)((tl.z + kTokChunk - 1) / kTokChunk * kTokChunk);
         const uint32_t idesc = idesc_mxf4nvf4(128, ncols);
-        if (!wait_or_abort(&bars->tmem_empty[0], ((uint32_t)local & 1u) ^ 1u, bars, p.status)) break;
+        const uint32_t buf = (uint32_t)local & 1u;
+        if (!wait_or_abort(&bars->tmem_empty[buf], (((uint32_t)local >> 1) & 1u) ^ 1u, bars, p.status)) break;
         tc_fence_after();
+        const uint32_t dcol = tmem + buf * 128;
         for (int kb = 0; kb < NKB; ++kb) {
           if (!wait_or_abort(&bars->full[stage], phase, bars, p.status)) {
             ok = false;
@@ -184,21 +232,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc_fence_after();
           const uint8_t* st = smem + stage * kFc1StageBytes;
-          const uint32_t sfc = tmem + 256 + stage * 48;
+          const uint32_t sfc = tmem + 256 + stage * 32;
 #pragma unroll
           for (int a = 0; a < 4; ++a) {
-            tmem_cp_32x128b_x4(sfc + a * 4, sf_desc(st + F1_SG + a * 512));
-            tmem_cp_32x128b_x4(sfc + 16 + a * 4, sf_desc(st + F1_SU + a * 512));
-            tmem_cp_32x128b_x4(sfc + 32 + a * 4, sf_desc(st + F1_SB + a * 512));
+            tmem_cp_32x128b_x4(sfc + a * 4, sf_desc(st + F1_SA + a * 512));
+            tmem_cp_32x128b_x4(sfc + 16 + a * 4, sf_desc(st + F1_SB + a * 512));
           }
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks) {
-            const uint64_t ag = smem_desc(smem_u32(st + F1_AG) + ks * 32, 16, 1024, kLayoutSW128);
-            const uint64_t au = smem_desc(smem_u32(st + F1_AU) + ks * 32, 16, 1024, kLayoutSW128);
+            const uint64_t ad = smem_desc(smem_u32(st + F1_A) + ks * 32, 16, 1024, kLayoutSW128);
             const uint64_t bd = smem_desc(smem_u32(st + F1_B) + ks * 32, 16, 1024, kLayoutSW128);
-            const uint32_t acc = (kb | ks) ? 1u : 0u;
-            mma_mxf4nvf4(tmem + 0, ag, bd, idesc, sfc + ks * 4, sfc + 32 + ks * 4, acc);
-            mma_mxf4nvf4(tmem + 128, au, bd, idesc, sfc + 16 + ks * 4, sfc + 32 + ks * 4, acc);
+            mma_mxf4nvf4(dcol, ad, bd, idesc, sfc + ks * 4, sfc + 16 + ks * 4, (kb | ks) ? 1u : 0u);
           }
           tc_commit(&bars->empty[stage]);
           if (++stage == kFc1Stages) {
@@ -206,7 +250,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             phase ^= 1u;
           }
         }
-        if (ok) tc_commit(&bars->tmem_full[0]);
+        if (ok) tc_commit(&bars->tmem_full[buf]);
         ++local;
       }
       tc_commit(&bars->drain);
@@ -214,44 +258,82 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    const int q = warp & 3, half = (warp - 2) >> 2;
+    constexpr int NGRP = kFc1EpiWarps / 4;     // warps per 32-lane quarter
+    const int q = warp & 3, grp = (warp - 2) >> 2;
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
     const int I2 = p.I / 2, KC = p.I / 16;
+    const bool odd = (lane & 1) != 0;
     int local = 0;
+    int4 nxt = next_tile(tiles, blockIdx.x, num_units, NIT);
+    float4 sc_nxt = unit_scalars(p, nxt);
+    int4 nxt2 = next_tile(tiles, blockIdx.x + gridDim.x, num_units, NIT);
     for (int unit = blockIdx.x; unit < num_units; unit += gridDim.x) {
-      const int4 tl = tiles[unit / NIT];
+      const int4 tl = nxt;
+      const float4 sc = sc_nxt;
+      nxt = nxt2;
+      sc_nxt = unit_scalars(p, nxt);                                   // one unit ahead
+      nxt2 = next_tile(tiles, unit + 2 * gridDim.x, num_units, NIT);  // two units ahead
       if (!tile_ok(tl, p.E, p.max_rows)) continue;
       const int it = unit % NIT;
-      const int e = tl.x, row0 = tl.y, rows = tl.z;
-      if (!wait_or_abort(&bars->tmem_full[0], (uint32_t)local & 1u, bars, p.status)) break;
+      const int row0 = tl.y, rows = tl.z;
+      const uint32_t buf = (uint32_t)local & 1u;
+      if (!wait_or_abort(&bars->tmem_full[buf], ((uint32_t)local >> 1) & 1u, bars, p.status)) break;
       tc_fence_after();
-      const float s13 = __ldg(p.dXdW13 + e), qa = __ldg(p.qA + e);
-      const float be = __ldg(p.beta + e), la = __ldg(p.lam + e);
+      const float s13 = sc.x, qa = sc.y, be = sc.z, la = sc.w;
       const int nch = (rows + kTokChunk - 1) / kTokChunk;
-      const int feat = it * 128 + q * 32 + lane;  // intermediate feature of this lane
-      for (int c = half; c < nch; c += 2) {
-        uint32_t rg[16], ru[16];
-        tmem_ld16(tmem + lane_base + c * 16, rg);
-        tmem_ld16(tmem + lane_base + 128 + c * 16, ru);
+      const int chunk16 = it * 4 + q;                        // 16-feature group of this quarter
+      const size_t aq_off = (size_t)it * 32 + (size_t)q * 8 + (size_t)(lane >> 4) * 4;
+      const float inv_be = 1.0f / be, inv_la = 1.0f / la;
+      for (int c = grp; c < nch; c += NGRP) {
+        uint32_t r[16];
+        tmem_ld16(tmem + lane_base + buf * 128 + c * 16, r);
         tmem_ld_wait();
+        // Pass 1: SiTU and the per-group amax of 8 column pairs.  Even lane l
+        // holds the gate of feature l/2, odd lane the up; even lanes evaluate
+        // column 2pp, odd lanes column 2pp+1.
+        float act[8], amx[8];
 #pragma unroll
-        for (int cc = 0; cc < 16; ++cc) {
-          const int n = c * 16 + cc;
-          if (n < rows) {
-            const float g = __fmul_rn(__uint_as_float(rg[cc]), s13);
-            const float u = __fmul_rn(__uint_as_float(ru[cc]), s13);
-            const float act = situ_f32(g, u, be, la);
-            uint32_t word;
-            const uint32_t sf = nvfp4_quant_lanes16(act, qa, word);
-            const int64_t prow = row0 + n;
-            if ((lane & 7) == 0) *reinterpret_cast<uint32_t*>(p.aq + (size_t)prow * I2 + feat / 2) = word;
-            if ((lane & 15) == 0) p.sfa[atom_offset(prow, feat / 16, KC)] = (uint8_t)sf;
+        for (int pp = 0; pp < 8; ++pp) {
+          const float m0 = __uint_as_float(r[2 * pp]), m1 = __uint_as_float(r[2 * pp + 1]);
+          const float recv = __shfl_xor_sync(0xffffffffu, odd ? m0 : m1, 1);
+          const float g = __fmul_rn(odd ? recv : m0, s13);
+          const float u = __fmul_rn(odd ? m1 : recv, s13);
+          act[pp] = situ_f32(g, u, be, inv_be, la, inv_la);
+          float m = fabsf(act[pp]);
+#pragma unroll
+          for (int off = 2; off <= 16; off <<= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+          amx[pp] = m;
+        }
+        // Pass 2: lane 2pp+p computes the block scale of (column pair pp, parity p) once.
+        const int sel = (lane >> 1) & 7;  // a select tree keeps amx[] in registers
+        const float a01 = (sel & 1) ? amx[1] : amx[0], a23 = (sel & 1) ? amx[3] : amx[2];
+        const float a45 = (sel & 1) ? amx[5] : amx[4], a67 = (sel & 1) ? amx[7] : amx[6];
+        const float a03 = (sel & 2) ? a23 : a01, a47 = (sel & 2) ? a67 : a45;
+        const float am = (sel & 4) ? a47 : a03;
+        float rr;
+        const uint32_t sfv = nvfp4_scale(am, qa, rr);
+        // Pass 3: codes with the broadcast scale, packed and stored.
+#pragma unroll
+        for (int pp = 0; pp < 8; ++pp) {
+          const int src = 2 * pp + (lane & 1);
+          const float rp = __shfl_sync(0xffffffffu, rr, src);
+          const uint32_t sf = __shfl_sync(0xffffffffu, sfv, src);
+          uint32_t v = cvt_e2m1x2(0.0f, __fmul_rn(act[pp], rp)) & 0xFu;
+          v = (v | (__shfl_down_sync(0xffffffffu, v, 2) << 4)) & 0xFFu;
+          const uint32_t word = v | (__shfl_down_sync(0xffffffffu, v, 4) << 8) |
+                                (__shfl_down_sync(0xffffffffu, v, 8) << 16) |
+                                (__shfl_down_sync(0xffffffffu, v, 12) << 24);
+          const int col = c * 16 + 2 * pp + (lane & 1);
+          if (col < rows) {
+            const int64_t prow = row0 + col;
+            if ((lane & ~17) == 0) *reinterpret_cast<uint32_t*>(p.aq + (size_t)prow * I2 + aq_off) = word;
+            if (lane < 2) p.sfa[atom_offset(prow, chunk16, KC)] = (uint8_t)sf;
           }
         }
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->tmem_empty[0]);
+      if (lane == 0) mbar_arrive(&bars->tmem_empty[buf]);
       ++local;
     }
   }
@@ -262,8 +344,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ================================================================== FC2
-__global__ void __launch_bounds__(kThreads, 1)
-    fc2_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_constant__ CUtensorMap tm_aq,
+__global__ void __launch_bounds__(kFc2Threads, 1)
+    fc2_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_constant__ RowMaps tm_aq,
                const Fc2Args p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = aligned_smem(smem_raw);
@@ -272,9 +354,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int NMT = p.H / 128, NKB = p.I / kFc2KBlock, NA = p.I / 64;
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tm_w2);
-    tma_prefetch_desc(&tm_aq);
+    tma_prefetch_desc(&tm_aq.m16);
+    tma_prefetch_desc(&tm_aq.m128);
   }
-  gemm_setup<kFc2Stages>(bars, warp);
+  gemm_setup<kFc2Stages, kFc2EpiWarps>(bars, warp);
   const uint32_t tmem = bars->tmem_base;
   pdl_wait();
   pdl_launch_dependents();
@@ -286,8 +369,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t stage = 0, phase = 0;
       uint32_t armed = 0, last_phase = 0;
       bool ok = true;
+      int4 nxt = next_tile(tiles, blockIdx.x, num_units, NMT);
       for (int unit = blockIdx.x; unit < num_units && ok; unit += gridDim.x) {
-        const int4 tl = tiles[unit / NMT];
+        const int4 tl = nxt;
+        nxt = next_tile(tiles, unit + gridDim.x, num_units, NMT);
         if (!tile_ok(tl, p.E, p.max_rows)) {
           set_status(p.status, DEVSTAT_BAD_TILE);
           continue;
@@ -306,8 +391,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           armed |= 1u << stage;
           last_phase = (last_phase & ~(1u << stage)) | (phase << stage);
           tma_load_3d(st + F2_A, &tm_w2, 0, 0, (e * NMT + mt) * NKB + kb, &bars->full[stage]);
-          for (int c = 0; c < nch; ++c)
-            tma_load_2d(st + F2_B + c * 1024, &tm_aq, kb * 64, row0 + c * kTokChunk, &bars->full[stage]);
+          load_rows(st + F2_B, tm_aq, kb * 64, row0, nch, 1024u, &bars->full[stage]);
           bulk_g2s(st + F2_SA, p.sf2p + ((size_t)(e * NMT + mt) * NA + (size_t)kb * 2) * 512u, 1024u,
                    &bars->full[stage]);
           bulk_g2s(st + F2_SB, p.sfa + ((size_t)(row0 >> 7) * NA + (size_t)kb * 2) * 512u, 1024u,
@@ -326,8 +410,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t stage = 0, phase = 0;
       int local = 0;
       bool ok = true;
+      int4 nxt = next_tile(tiles, blockIdx.x, num_units, NMT);
       for (int unit = blockIdx.x; unit < num_units && ok; unit += gridDim.x) {
-        const int4 tl = tiles[unit / NMT];
+        const int4 tl = nxt;
+        nxt = next_tile(tiles, unit + gridDim.x, num_units, NMT);
         if (!tile_ok(tl, p.E, p.max_rows)) continue;
         const uint32_t ncols = (uint32_t)((tl.z + kTokChunk - 1) / kTokChunk * kTokChunk);
         const uint32_t idesc = idesc_mxf4nvf4(128, ncols);
@@ -367,38 +453,47 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait(&bars->drain, 0, p.status);
     }
   } else {
-    const int q = warp & 3, half = (warp - 2) >> 2;
+    // ------------------------------------------------------------ epilogue
+    constexpr int NGRP = kFc2EpiWarps / 4;
+    const int q = warp & 3, grp = (warp - 2) >> 2;
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
     int local = 0;
+    int4 nxt = next_tile(tiles, blockIdx.x, num_units, NMT);
+    float s2_nxt = (nxt.x >= 0 && nxt.x < p.E) ? __ldg(p.dAdW2 + nxt.x) : 0.0f;
+    int4 nxt2 = next_tile(tiles, blockIdx.x + gridDim.x, num_units, NMT);
     for (int unit = blockIdx.x; unit < num_units; unit += gridDim.x) {
-      const int4 tl = tiles[unit / NMT];
+      const int4 tl = nxt;
+      const float s2 = s2_nxt;
+      nxt = nxt2;
+      s2_nxt = (nxt.x >= 0 && nxt.x < p.E) ? __ldg(p.dAdW2 + nxt.x) : 0.0f;
+      nxt2 = next_tile(tiles, unit + 2 * gridDim.x, num_units, NMT);
       if (!tile_ok(tl, p.E, p.max_rows)) continue;
       const int mt = unit % NMT;
-      const int e = tl.x, row0 = tl.y, rows = tl.z;
+      const int row0 = tl.y, rows = tl.z;
+      // route weights of this warp's columns, loaded before waiting on the accumulator
+      float wgt[(kTileRows / kTokChunk + NGRP - 1) / NGRP];
+#pragma unroll
+      for (int i = 0; i < (kTileRows / kTokChunk + NGRP - 1) / NGRP; ++i) {
+        const int col = (grp + i * NGRP) * 16 + (lane & 15);
+        wgt[i] = (col < rows) ? __ldg(p.wrow + row0 + col) : 0.0f;
+      }
       const uint32_t buf = (uint32_t)local & 1u;
       if (!wait_or_abort(&bars->tmem_full[buf], ((uint32_t)local >> 1) & 1u, bars, p.status)) break;
       tc_fence_after();
-      const float s2 = __ldg(p.dAdW2 + e);
       const int nch = (rows + kTokChunk - 1) / kTokChunk;
-      const int h = mt * 128 + q * 32 + lane;
-      for (int c = half; c < nch; c += 2) {
+      float* ybase = p.y + (size_t)row0 * p.H + (size_t)mt * 128 + q * 32 + lane;
+#pragma unroll
+      for (int i = 0; i < (kTileRows / kTokChunk + NGRP - 1) / NGRP; ++i) {
+        const int c = grp + i * NGRP;
+        if (c >= nch) break;
         uint32_t r[16];
         tmem_ld16(tmem + lane_base + buf * 128 + c * 16, r);
-        int pair = -1;
-        float wgt = 0.0f;
-        if (lane < 16 && c * 16 + lane < rows) {
-          pair = p.prow_pair[row0 + c * 16 + lane];
-          if (pair >= 0 && pair < p.num_pairs) wgt = bf16_bits_to_f32(p.route_w[pair]);
-        }
         tmem_ld_wait();
 #pragma unroll
         for (int cc = 0; cc < 16; ++cc) {
-          const int pr = __shfl_sync(0xffffffffu, pair, cc);
-          const float wv = __shfl_sync(0xffffffffu, wgt, cc);
-          if (c * 16 + cc < rows && pr >= 0 && pr < p.num_pairs) {
-            const float y = __fmul_rn(__uint_as_float(r[cc]), s2);
-            atomicAdd(p.out_f32 + (size_t)(pr / p.k) * p.H + h, __fmul_rn(y, wv));
-          }
+          const float wv = __shfl_sync(0xffffffffu, wgt[i], cc);
+          const int col = c * 16 + cc;
+          if (col < rows) ybase[(size_t)col * p.H] = __fmul_rn(__fmul_rn(__uint_as_float(r[cc]), s2), wv);
         }
       }
       tc_fence_before();
@@ -501,18 +596,20 @@ cudaError_t gemm_set_attributes() {
                               (int)kMmaCheckSmem);
 }
 
-cudaError_t launch_fc1(const CUtensorMap& w13, const CUtensorMap& xq, const Fc1Args& a, int grid, cudaStream_t st) {
-  CUtensorMap m0 = w13, m1 = xq;
+cudaError_t launch_fc1(const CUtensorMap& w13, const RowMaps& xq, const Fc1Args& a, int grid, cudaStream_t st) {
+  CUtensorMap m0 = w13;
+  RowMaps m1 = xq;
   Fc1Args args = a;
   void* kargs[] = {&m0, &m1, &args};
-  return launch_with_pdl((const void*)fc1_kernel, dim3(grid), dim3(kThreads), kFc1Smem, st, kargs);
+  return launch_with_pdl((const void*)fc1_kernel, dim3(grid), dim3(kFc1Threads), kFc1Smem, st, kargs);
 }
 
-cudaError_t launch_fc2(const CUtensorMap& w2, const CUtensorMap& aq, const Fc2Args& a, int grid, cudaStream_t st) {
-  CUtensorMap m0 = w2, m1 = aq;
+cudaError_t launch_fc2(const CUtensorMap& w2, const RowMaps& aq, const Fc2Args& a, int grid, cudaStream_t st) {
+  CUtensorMap m0 = w2;
+  RowMaps m1 = aq;
   Fc2Args args = a;
   void* kargs[] = {&m0, &m1, &args};
-  return launch_with_pdl((const void*)fc2_kernel, dim3(grid), dim3(kThreads), kFc2Smem, st, kargs);
+  return launch_with_pdl((const void*)fc2_kernel, dim3(grid), dim3(kFc2Threads), kFc2Smem, st, kargs);
 }
 
 cudaError_t launch_mma_check(const CUtensorMap& a, const CUtensorMap& b, const uint8_t* sfa, const uint8_t* sfb,

@@ -58,12 +58,29 @@ __device__ __forceinline__ uint32_t nvfp4_quant_lanes16(float a, float q, uint32
   return sf;
 }
 
+// tanh from its definition: the odd Taylor series to y^9 for |y| < 1/4
+// (truncation below 1e-8 relative there), else (1 - e^{-2|y|}) / (1 + e^{-2|y|})
+// with the hardware exponential (relative error below 1e-6 for the result).
+__device__ __forceinline__ float tanh_dev(float y) {
+  const float a = fabsf(y);
+  float t;
+  if (a < 0.25f) {
+    const float a2 = a * a;
+    t = a * (1.0f + a2 * (-1.0f / 3.0f + a2 * (2.0f / 15.0f + a2 * (-17.0f / 315.0f + a2 * (62.0f / 2835.0f)))));
+  } else {
+    const float e = __expf(-2.0f * a);
+    t = __fdividef(1.0f - e, 1.0f + e);
+  }
+  return copysignf(t, y);
+}
+
 // SiTU ("Cake SiTU backend": default (4*tanh(g/4)*sigmoid(g))*(25*tanh(u/25)),
-// per-expert gate and linear smoothing parameters beta, lambda).
-__device__ __forceinline__ float situ_f32(float g, float u, float beta, float lam) {
-  const float sig = 1.0f / (1.0f + expf(-g));
-  const float gate = beta * tanhf(g / beta) * sig;
-  const float lin = lam * tanhf(u / lam);
+// per-expert gate and linear smoothing parameters beta, lambda), with the
+// reciprocals 1/beta and 1/lambda supplied by the caller.
+__device__ __forceinline__ float situ_f32(float g, float u, float beta, float inv_beta, float lam, float inv_lam) {
+  const float sig = __frcp_rn(1.0f + expf(-g));
+  const float gate = beta * tanh_dev(g * inv_beta) * sig;
+  const float lin = lam * tanh_dev(u * inv_lam);
   return gate * lin;
 }
 

@@ -3,6 +3,7 @@
 #pragma once
 #include <cstddef>
 #include <cstdint>
+#include <cuda.h>
 
 namespace moe {
 
@@ -27,6 +28,11 @@ enum : int {
   HDR_WORDS = 64,
 };
 
+// One tensor map per activation-row box height (16, 32, 64, 128 rows).
+struct RowMaps {
+  CUtensorMap m16, m32, m64, m128;
+};
+
 struct Shape {
   int32_t H, I, E, k;
 };
@@ -36,7 +42,7 @@ struct WsLayout {
   int64_t max_tokens, Pmax, PpadMax, TTmax, nblkMax;
   size_t header, count, cumsum, offs, poffs, ttoffs;
   size_t sorted_row, gather, row_pos, prow_pair, tt_list, blockhist;
-  size_t xq, sfx, aq, sfa, out_f32, beta_def, lam_def;
+  size_t xq, sfx, aq, sfa, y, wrow, beta_def, lam_def;
   size_t total;
 };
 
@@ -76,7 +82,8 @@ inline WsLayout make_layout(const Shape& s, int64_t max_tokens) {
   L.sfx = take((size_t)(L.PpadMax / kTileRows) * (s.H / 64) * 512);
   L.aq = take((size_t)L.PpadMax * (s.I / 2));
   L.sfa = take((size_t)(L.PpadMax / kTileRows) * (s.I / 64) * 512);
-  L.out_f32 = take((size_t)max_tokens * s.H * 4);
+  L.y = take((size_t)L.PpadMax * s.H * 4);
+  L.wrow = take((size_t)L.PpadMax * 4);
   L.beta_def = take((size_t)s.E * 4);
   L.lam_def = take((size_t)s.E * 4);
   L.total = o;
@@ -126,9 +133,9 @@ struct Fc2Args {
   const int32_t* tt_list;
   const int32_t* hdr;
   const int32_t* prow_pair;
-  const uint16_t* route_w;  // bf16 bits [T, k]
+  const float* wrow;        // [Ppad] route weight of the pair in each padded row
   const float* dAdW2;
-  float* out_f32;
+  float* y;                 // [Ppad, H] fp32: route-weighted FC2 output of every routed pair
   int32_t* status;
   int32_t H, I, E, k;
   int32_t max_tiles;
@@ -163,10 +170,11 @@ struct InitFinishArgs {
 struct QuantXArgs {
   const uint16_t* x;        // [T, H] bf16
   const int32_t* row_pos;   // [T*k] padded expanded row of each pair, -1 if not routed
+  const uint16_t* route_w;  // [T*k] bf16 route weights
+  float* wrow;              // [Ppad] out: route weight of each padded row (fp32)
   const float* qX;          // [1]
   uint8_t* xq;              // [Ppad, H/2]
   uint8_t* sfx;             // atom layout, H/16 chunks per row
-  float* out_f32;           // [T, H] accumulator, zeroed here for the FC2 combine
   int64_t T;
   int32_t H, k;
   int64_t max_rows;         // padded rows of the workspace

@@ -15,8 +15,8 @@ cudaError_t launch_with_pdl(const void* fn, dim3 grid, dim3 block, size_t smem, 
 // of the token ("Cake SiTU backend": group-16 NVFP4 input quantization with
 // qX) once, and writes the codes and block scales to the padded expanded row
 // of every pair the token is routed to ("npu_moe_init_routing_v2", formula 5,
-// gather form: expandedX[gatherRowIdx[i]] = quantResult[i // k]).  The warp
-// also zeroes the token's row of the fp32 output accumulator.
+// gather form: expandedX[gatherRowIdx[i]] = quantResult[i // k]).  It also
+// stores each pair's route weight (fp32) at the pair's padded row for FC2.
 __global__ void __launch_bounds__(256) quant_x_kernel(const QuantXArgs a) {
   const int lane = threadIdx.x & 31;
   const int64_t t = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
@@ -26,8 +26,7 @@ __global__ void __launch_bounds__(256) quant_x_kernel(const QuantXArgs a) {
   const int H = a.H, G = H / 16, KC = H / 16;
   const float q = __ldg(a.qX);
   const int rp = (lane < a.k) ? a.row_pos[t * a.k + lane] : -1;
-  float4* orow = reinterpret_cast<float4*>(a.out_f32 + t * H);
-  for (int v = lane; v < H / 4; v += 32) orow[v] = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (rp >= 0 && rp < a.max_rows) a.wrow[rp] = bf16_bits_to_f32(a.route_w[t * a.k + lane]);
   const uint4* xr = reinterpret_cast<const uint4*>(a.x + t * H);
   for (int g0 = 0; g0 < G; g0 += 32) {
     const int g = g0 + lane;
@@ -61,20 +60,33 @@ __global__ void __launch_bounds__(256) quant_x_kernel(const QuantXArgs a) {
 }
 
 // ------------------------------------------------------------------ finalize
-// out[t, h] = bf16_rn(acc[t, h]) ("Cake SiTU backend": BF16 weighted
-// finalization; the fp32 weighted sum over k was accumulated by FC2).
-__global__ void __launch_bounds__(256) finalize_kernel(const float* __restrict__ acc, uint16_t* __restrict__ out,
-                                                       int64_t n8) {
+// out[t, h] = bf16_rn( sum_j y[row_pos[t*k + j], h] ) ("Cake SiTU backend":
+// BF16 weighted finalization).  y already carries the route weight; the k
+// rows of a token are added in j order in fp32 and rounded once.  One thread
+// per 8 consecutive outputs of a token; pairs that were not routed are skipped.
+__global__ void __launch_bounds__(256) finalize_kernel(const float* __restrict__ y, const int32_t* __restrict__ row_pos,
+                                                       uint16_t* __restrict__ out, int64_t T, int H, int k,
+                                                       int64_t max_rows) {
   pdl_wait();
   pdl_launch_dependents();
-  for (int64_t i = (int64_t)blockIdx.x * 256 + threadIdx.x; i < n8; i += (int64_t)gridDim.x * 256) {
-    const float4 a = reinterpret_cast<const float4*>(acc)[2 * i];
-    const float4 b = reinterpret_cast<const float4*>(acc)[2 * i + 1];
-    const float f[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+  const int per_tok = H / 8;
+  const int64_t n = T * per_tok;
+  for (int64_t i = (int64_t)blockIdx.x * 256 + threadIdx.x; i < n; i += (int64_t)gridDim.x * 256) {
+    const int64_t t = i / per_tok;
+    const int h8 = (int)(i % per_tok);
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int j = 0; j < k; ++j) {
+      const int rp = __ldg(row_pos + t * k + j);
+      if (rp < 0 || rp >= max_rows) continue;
+      const float4* src = reinterpret_cast<const float4*>(y + (size_t)rp * H) + 2 * h8;
+      const float4 a = __ldcs(src), b = __ldcs(src + 1);
+      acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
+      acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
+    }
     uint32_t w[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      const __nv_bfloat162 h = __floats2bfloat162_rn(f[2 * j], f[2 * j + 1]);
+      const __nv_bfloat162 h = __floats2bfloat162_rn(acc[2 * j], acc[2 * j + 1]);
       w[j] = *reinterpret_cast<const uint32_t*>(&h);
     }
     reinterpret_cast<uint4*>(out)[i] = make_uint4(w[0], w[1], w[2], w[3]);
@@ -83,40 +95,40 @@ __global__ void __launch_bounds__(256) finalize_kernel(const float* __restrict__
 
 // --------------------------------------------------------- weight preparation
 // Kernel layout of the prepared weights:
-//   W13 codes  [E][I/128][H/256][256 rows][128 B]: rows 0..127 of a tile are
-//              gate rows it*128.., rows 128..255 the matching up rows;
-//   W13 scales [E][I/128][H/256][2 (gate, up)][4 atoms][512 B];
+//   W13 codes  [E][I/64][H/256][128 rows][128 B]: tile row 2i is the gate row
+//              of feature it*64 + i, row 2i+1 the matching up row;
+//   W13 scales [E][I/64][H/256][4 atoms][512 B] over the same tile rows;
 //   W2 codes   [E][H/128][I/128][128 rows][64 B];
 //   W2 scales  [E][H/128][I/64 atoms][512 B];
 // atoms in the 128x4 layout of the "Nvfp4 Tensor" page (block_scale).
 __global__ void __launch_bounds__(256) prep_w13_codes_kernel(const PrepArgs a) {
-  const int NIT = a.I / 128, NKB = a.H / 256;
+  const int NIT = a.I / 64, NKB = a.H / 256;
   const int64_t units = (int64_t)a.E * 2 * a.I * (a.H / 2) / 16;
   for (int64_t u = (int64_t)blockIdx.x * 256 + threadIdx.x; u < units; u += (int64_t)gridDim.x * 256) {
     const int64_t o = u * 16;
-    const int64_t tile = o / 32768;
-    const int r = (int)((o / 128) % 256), byte = (int)(o % 128);
+    const int64_t tile = o / 16384;            // (e*NIT + it)*NKB + kb
+    const int r = (int)((o / 128) % 128), byte = (int)(o % 128);
     const int kb = (int)(tile % NKB), it = (int)((tile / NKB) % NIT);
     const int64_t e = tile / ((int64_t)NKB * NIT);
-    const int64_t src_row = e * 2 * a.I + (r / 128) * a.I + it * 128 + (r % 128);
+    const int64_t src_row = e * 2 * a.I + (r & 1) * a.I + it * 64 + (r >> 1);
     const uint4 v = *reinterpret_cast<const uint4*>(a.w13 + src_row * (a.H / 2) + kb * 128 + byte);
     *reinterpret_cast<uint4*>(a.w13o + o) = v;
   }
 }
 
 __global__ void __launch_bounds__(256) prep_w13_sf_kernel(const PrepArgs a) {
-  const int NIT = a.I / 128, NKB = a.H / 256;
+  const int NIT = a.I / 64, NKB = a.H / 256;
   const int64_t n = (int64_t)a.E * 2 * a.I * (a.H / 16);
   for (int64_t o = (int64_t)blockIdx.x * 256 + threadIdx.x; o < n; o += (int64_t)gridDim.x * 256) {
     const int within = (int)(o % 512);
-    const int64_t atom = o / 512;             // (((e*NIT + it)*NKB + kb)*2 + half)*4 + kt
-    const int kt = (int)(atom % 4), half = (int)((atom / 4) % 2);
-    const int64_t tile = atom / 8;
+    const int64_t atom = o / 512;             // ((e*NIT + it)*NKB + kb)*4 + kt
+    const int kt = (int)(atom % 4);
+    const int64_t tile = atom / 4;
     const int kb = (int)(tile % NKB), it = (int)((tile / NKB) % NIT);
     const int64_t e = tile / ((int64_t)NKB * NIT);
-    const int rr = (within & 15) / 4 * 32 + within / 16;   // innerM*32 + outerM
+    const int r = (within & 15) / 4 * 32 + within / 16;   // tile row: innerM*32 + outerM
     const int c = kb * 16 + kt * 4 + (within & 3);
-    const int64_t src_row = e * 2 * a.I + half * a.I + it * 128 + rr;
+    const int64_t src_row = e * 2 * a.I + (r & 1) * a.I + it * 64 + (r >> 1);
     a.sf13o[o] = a.sf13[src_row * (a.H / 16) + c];
   }
 }
@@ -191,7 +203,7 @@ __global__ void __launch_bounds__(256) situ_requant_kernel(const float* z, int64
   const int64_t r = w / per_row;
   const int f = (int)(w % per_row) * 32 + lane;
   const float g = z[r * 2 * I + f], u = z[r * 2 * I + I + f];
-  const float act = situ_f32(g, u, beta, lam);
+  const float act = situ_f32(g, u, beta, 1.0f / beta, lam, 1.0f / lam);
   a_out[r * I + f] = act;
   uint32_t word;
   const uint32_t s = nvfp4_quant_lanes16(act, qA, word);
@@ -222,11 +234,11 @@ cudaError_t launch_quant_x(const QuantXArgs& a, cudaStream_t st) {
   return launch_with_pdl((const void*)quant_x_kernel, dim3(blocks), dim3(256), 0, st, kargs);
 }
 
-cudaError_t launch_finalize(const float* acc, uint16_t* out, int64_t n, int num_sms, cudaStream_t st) {
-  int64_t n8 = n / 8;
-  void* kargs[] = {(void*)&acc, (void*)&out, (void*)&n8};
-  int64_t want = (n8 + 255) / 256;
-  const unsigned blocks = (unsigned)(want < (int64_t)num_sms * 8 ? want : (int64_t)num_sms * 8);
+cudaError_t launch_finalize(const float* y, const int32_t* row_pos, uint16_t* out, int64_t T, int H, int k,
+                            int64_t max_rows, int num_sms, cudaStream_t st) {
+  void* kargs[] = {(void*)&y, (void*)&row_pos, (void*)&out, (void*)&T, (void*)&H, (void*)&k, (void*)&max_rows};
+  const int64_t want = (T * (H / 8) + 255) / 256;
+  const unsigned blocks = (unsigned)(want < (int64_t)num_sms * 16 ? want : (int64_t)num_sms * 16);
   return launch_with_pdl((const void*)finalize_kernel, dim3(blocks ? blocks : 1), dim3(256), 0, st, kargs);
 }
 
