@@ -4,7 +4,7 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload maxbatch] [--impl ours|reference]
 
 One step is one moe_forward (routing, X quantization, FC1 + SiTU + requant,
-FC2 + weighted combine, BF16 finalize) over one batch of seeded synthetic
+FC2 + route-weighted combine, BF16 finalize) over one batch of seeded synthetic
 input already resident in HBM.  Default workload: T=16384 tokens at
 H=3584, I=384, E=896, k=16, uniform distinct expert ids, 1% of rows x50
 (the max-batch case); its 2.08 GB of weights are larger than L2, so no flush

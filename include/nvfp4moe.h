@@ -44,7 +44,7 @@ typedef enum {
 } moe_status_t;
 
 /* H (hidden), I (intermediate), E (local experts), k (top-k).
- * Supported: H % 256 == 0, I % 128 == 0, 1 <= E <= 1024, 1 <= k <= min(32, E).
+ * Supported: H % 256 == 0, I % 128 == 0, I <= 512, 1 <= E <= 1024, 1 <= k <= min(32, E).
  * The pages' shape is H=3584, I=384, E=896, k=16 ("Cake SiTU backend", intro). */
 typedef struct {
   int32_t hidden, inter, num_experts, top_k;

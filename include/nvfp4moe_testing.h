@@ -62,12 +62,12 @@ moe_status_t moe_test_mma_fp4(const uint8_t* a, const uint8_t* sfa_atoms, const 
  * intermediates in tests (host out struct).  Routing arrays are int32;
  * xq/aq are packed codes of padded expanded rows ([rows, H/2] / [rows, I/2]);
  * sfx/sfa are their block scales in the 128x4 atom layout; row_pos maps a
- * flat pair t*k+j to its padded row; y [rows, H] fp32 holds each routed
- * pair's route-weighted FC2 output. */
+ * flat pair t*k+j to its padded row; acc [tokens, H] fp32 is the FC2
+ * combine accumulator (route-weighted sums before the BF16 rounding). */
 typedef struct {
   int64_t max_tokens, pairs_max, padded_rows_max, tiles_max;
   int64_t header, count, cumsum, offs, poffs, sorted_row, gather, row_pos, prow_pair, tt_list;
-  int64_t xq, sfx, aq, sfa, y, total;
+  int64_t xq, sfx, aq, sfa, acc, total;
 } moe_ws_layout_t;
 
 moe_status_t moe_workspace_layout(const moe_shape_t* shape, size_t ws_bytes, moe_ws_layout_t* layout);
@@ -78,9 +78,10 @@ moe_status_t moe_forward_launch_count(const moe_shape_t* shape, int64_t num_toke
 
 /* Stage timing (tracing): after moe_profile_start(max_calls), each of the
  * next max_calls moe_forward calls records a CUDA timing event before each of
- * its five stages (routing, X quantization, FC1, FC2, finalize) and one after
- * the last, on the call's stream.  moe_profile_stop synchronizes on those
- * events, writes the summed milliseconds per stage to stage_ms[0..4] and the
+ * its five stages (routing, X quantization, FC1, FC2 with the combine, BF16
+ * finalize) and one after the last, on the call's stream.  moe_profile_stop
+ * synchronizes on those events, writes the summed milliseconds per stage to
+ * stage_ms[0..4] and the
  * number of recorded calls to *calls (HOST pointers), and frees the events.
  * Events recorded between stages make the stages run back to back (no launch
  * overlap across stage boundaries).  Not thread-safe against concurrent

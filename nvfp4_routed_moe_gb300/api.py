@@ -49,7 +49,7 @@ class moe_ws_layout_t(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int64) for n in
                 ("max_tokens", "pairs_max", "padded_rows_max", "tiles_max", "header", "count", "cumsum", "offs",
                  "poffs", "sorted_row", "gather", "row_pos", "prow_pair", "tt_list", "xq", "sfx", "aq", "sfa",
-                 "y", "total")]
+                 "acc", "total")]
 
 
 def shape(hidden: int, inter: int, num_experts: int, top_k: int) -> moe_shape_t:
@@ -225,7 +225,7 @@ def moe_profile_start(max_calls: int):
 
 def moe_profile_stop():
     """Returns ({stage: summed ms}, calls)."""
-    ms = (ctypes.c_float * 5)()
+    ms = (ctypes.c_float * len(STAGES))()
     calls = ctypes.c_int32()
     _check(lib().moe_profile_stop(ms, ctypes.byref(calls)), "moe_profile_stop")
     return dict(zip(STAGES, [float(v) for v in ms])), calls.value

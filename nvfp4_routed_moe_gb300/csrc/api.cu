@@ -19,8 +19,7 @@ cudaError_t routing_set_attributes(int E);
 cudaError_t launch_init_move(const InitMoveArgs& a, cudaStream_t st);
 cudaError_t launch_init_finish(const InitFinishArgs& a, cudaStream_t st, int num_sms);
 cudaError_t launch_quant_x(const QuantXArgs& a, cudaStream_t st);
-cudaError_t launch_finalize(const float* y, const int32_t* row_pos, uint16_t* out, int64_t T, int H, int k,
-                            int64_t max_rows, int num_sms, cudaStream_t st);
+cudaError_t launch_finalize(const float* acc, uint16_t* out, int64_t T, int H, int num_sms, cudaStream_t st);
 cudaError_t launch_prep(const PrepArgs& a, cudaStream_t st, int num_sms);
 cudaError_t launch_codec_sweep(uint32_t start, int64_t n, uint8_t* lo, uint8_t* hi, uint8_t* e4, cudaStream_t st,
                                int num_sms);
@@ -150,7 +149,7 @@ static bool shape_ok(const moe_shape_t* s) {
 }
 static moe_status_t shape_supported(const moe_shape_t* s) {
   if (!shape_ok(s)) return MOE_ERR_INVALID_ARG;
-  if (s->hidden % 256 != 0 || s->inter % 128 != 0) return MOE_ERR_UNSUPPORTED;
+  if (s->hidden % 256 != 0 || s->inter % 128 != 0 || s->inter > 512) return MOE_ERR_UNSUPPORTED;
   if (s->num_experts > kMaxExperts || s->top_k > kMaxTopK || s->top_k > s->num_experts) return MOE_ERR_UNSUPPORTED;
   if ((int64_t)s->hidden * s->top_k > (int64_t)1 << 30) return MOE_ERR_UNSUPPORTED;
   return MOE_OK;
@@ -221,10 +220,25 @@ static RouteArgs route_args(const Shape& s, const WsLayout& L, uint8_t* ws, cons
 
 static int forward_launches(int64_t P) { return (P <= kRouteSmallMax ? 1 : 2) + 4; }
 
+// Passes of the FC2 combine over H: the fewest (a divisor of H/128) whose
+// accumulator slice, T x H/nq fp32, fits the L2 budget (NVFP4MOE_ACC_PASS_MB
+// overrides the default budget).
+static int combine_passes(const Shape& s, int64_t T) {
+  size_t budget = kAccPassBytes;
+  if (const char* v = std::getenv("NVFP4MOE_ACC_PASS_MB")) {
+    const long mb = std::strtol(v, nullptr, 10);
+    if (mb > 0) budget = (size_t)mb << 20;
+  }
+  const int NMT = s.H / 128;
+  for (int d = 1; d < NMT; ++d)
+    if (NMT % d == 0 && (size_t)T * (size_t)s.H * 4u / (size_t)d <= budget) return d;
+  return NMT;
+}
+
 // ------------------------------------------------------------ stage timing
 // While a profile is open, every moe_forward records a timing event before
 // each stage and one after the last, from a pool created by moe_profile_start.
-constexpr int kStages = 5;  // routing, quant X, FC1, FC2, finalize
+constexpr int kStages = 5;  // routing, quant X, FC1, FC2 with the combine, BF16 finalize
 struct Profile {
   bool on = false;
   int max_calls = 0, calls = 0;
@@ -379,6 +393,8 @@ moe_status_t moe_forward(const moe_shape_t* shape, int64_t num_tokens, const voi
   qa.row_pos = ra.row_pos;
   qa.route_w = static_cast<const uint16_t*>(route_weights);
   qa.wrow = reinterpret_cast<float*>(w + L.wrow);
+  const int nq = combine_passes(s, T);
+  qa.acc = reinterpret_cast<float*>(w + L.acc);
   qa.qX = qX;
   qa.xq = w + L.xq;
   qa.sfx = w + L.sfx;
@@ -412,7 +428,7 @@ moe_status_t moe_forward(const moe_shape_t* shape, int64_t num_tokens, const voi
   prof_mark(2, stream);
   MOE_CUDA(launch_fc1(tm_w13, tm_xq, f1, grid1, stream));
 
-  // 4. FC2: route-weighted fp32 rows of every routed pair
+  // 4. FC2 with the route-weighted combine into the fp32 accumulator
   Fc2Args f2{};
   f2.sf2p = sf2;
   f2.sfa = w + L.sfa;
@@ -421,7 +437,8 @@ moe_status_t moe_forward(const moe_shape_t* shape, int64_t num_tokens, const voi
   f2.prow_pair = ra.prow_pair;
   f2.wrow = reinterpret_cast<const float*>(w + L.wrow);
   f2.dAdW2 = dA_dW2;
-  f2.y = reinterpret_cast<float*>(w + L.y);
+  f2.acc = reinterpret_cast<float*>(w + L.acc);
+  f2.nq = nq;
   f2.status = ra.hdr + HDR_STATUS;
   f2.H = s.H;
   f2.I = s.I;
@@ -434,10 +451,10 @@ moe_status_t moe_forward(const moe_shape_t* shape, int64_t num_tokens, const voi
   prof_mark(3, stream);
   MOE_CUDA(launch_fc2(tm_w2, tm_aq, f2, grid2, stream));
 
-  // 5. BF16 finalize: sum of each token's k rows
+  // 5. BF16 finalize
   prof_mark(4, stream);
-  MOE_CUDA(launch_finalize(reinterpret_cast<const float*>(w + L.y), ra.row_pos, static_cast<uint16_t*>(out), T, s.H,
-                           s.k, L.PpadMax, sms, stream));
+  MOE_CUDA(launch_finalize(reinterpret_cast<const float*>(w + L.acc), static_cast<uint16_t*>(out), T, s.H, sms, stream));
+
   prof_end_call(stream);
   return MOE_OK;
 }
@@ -605,7 +622,7 @@ moe_status_t moe_workspace_layout(const moe_shape_t* shape, size_t ws_bytes, moe
   out->sfx = (int64_t)L.sfx;
   out->aq = (int64_t)L.aq;
   out->sfa = (int64_t)L.sfa;
-  out->y = (int64_t)L.y;
+  out->acc = (int64_t)L.acc;
   out->total = (int64_t)L.total;
   return MOE_OK;
 }

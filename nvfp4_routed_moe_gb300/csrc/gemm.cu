@@ -17,12 +17,17 @@
 // column, odd lanes the next), and quantizes a per 16 features with qA[e]
 // into the padded expanded rows of A (codes + atom-layout scales).
 //
-// FC2 ("Cake SiTU backend": FC2, BF16 weighted finalization): per work unit
-// (token tile, 128 output features) one accumulator [128 x N] over K = I in
-// k-blocks of 128; the epilogue scales by dA*dW2[e] and the route weight and
-// stores each routed pair's 128 outputs into its padded row of the fp32 y
-// buffer (one coalesced 128-byte store per warp and token).  The finalize
-// kernel adds a token's k rows.
+// FC2 ("Cake SiTU backend": FC2, BF16 weighted finalization): a work unit is
+// one token tile and a group of G consecutive 128-feature output tiles.  The
+// tile's quantized activations (K = I, all k-blocks) are loaded into a shared
+// memory slot once and stay there while the group's W2 tiles stream through
+// the ring; each output tile accumulates [128 x N] over K = I in k-blocks of
+// 128.  The epilogue scales by dA*dW2[e] and the route weight and adds each
+// routed pair's 128 outputs into its token's fp32 accumulator row with L2
+// reductions (one coalesced 128-byte reduction per warp and token).  Groups
+// run outermost in nq passes over H, so the accumulator rows of one pass,
+// T x H/nq fp32, stay resident in L2 while they are summed; the per-pair FC2
+// rows never reach memory.  The finalize kernel rounds the sums to BF16.
 //
 // Warp roles: warp 0 issues TMA, warp 1 owns TMEM and issues MMAs, the
 // remaining warps drain TMEM (each 32-lane quarter by several warps taking
@@ -45,25 +50,42 @@ constexpr int F1_A = 0, F1_B = 16384, F1_SA = 32768, F1_SB = 34816;
 constexpr int kFc1StageBytes = 36864;
 constexpr int kFc1EpiWarps = 16;
 constexpr int kFc1Threads = 64 + 32 * kFc1EpiWarps;
-// FC2 stage: A [128 x 64 B] | B [128 x 64 B] | SF A 2 atoms | SF B 2 atoms.
-constexpr int kFc2Stages = 12;
-constexpr int F2_A = 0, F2_B = 8192, F2_SA = 16384, F2_SB = 17408;
-constexpr int kFc2StageBytes = 18432;
-constexpr int kFc2EpiWarps = 8;
+// FC2 shared memory: barriers (1 KB) | two activation slots (a token tile's
+// A codes [I/128 k-blocks][128 rows x 64 B] + its I/64 scale atoms) | ring of
+// W2 stages (A [128 x 64 B] | SF 2 atoms); the stage count follows from I.
+constexpr int kMaxStages = 24;
+constexpr int kFc2StageBytes = 9216;
+constexpr int F2_SA = 8192;
+constexpr int kFc2EpiWarps = 16;
 constexpr int kFc2Threads = 64 + 32 * kFc2EpiWarps;
+constexpr int kFc2MaxI = 512;
+constexpr uint32_t kFc2SfbCol = 448;   // TMEM column of the activation slots' scale factors
 
 struct Barriers {
-  uint64_t full[16];
-  uint64_t empty[16];
+  uint64_t full[kMaxStages];
+  uint64_t empty[kMaxStages];
   uint64_t tmem_full[2];
   uint64_t tmem_empty[2];
+  uint64_t act_full[2];
+  uint64_t act_empty[2];
   uint64_t drain;
   uint32_t tmem_base;
   volatile int32_t abort_flag;
 };
+static_assert(sizeof(Barriers) <= 1024, "barrier block");
 
 constexpr size_t kFc1Smem = (size_t)kFc1Stages * kFc1StageBytes + sizeof(Barriers) + 1024;
-constexpr size_t kFc2Smem = (size_t)kFc2Stages * kFc2StageBytes + sizeof(Barriers) + 1024;
+constexpr size_t kFc2Smem = 232448;    // the opt-in maximum; carved up at run time
+
+__host__ __device__ constexpr int fc2_act_bytes(int I) { return (128 * (I / 2) + (I / 64) * 512 + 1023) / 1024 * 1024; }
+__host__ __device__ constexpr int fc2_stages(int I) {
+  return ((int)kFc2Smem - 1024 - 1024 - 2 * fc2_act_bytes(I)) / kFc2StageBytes < kMaxStages
+             ? ((int)kFc2Smem - 1024 - 1024 - 2 * fc2_act_bytes(I)) / kFc2StageBytes
+             : kMaxStages;
+}
+static_assert(fc2_stages(kFc2MaxI) >= 8 && 256 + 8 * kMaxStages <= (int)kFc2SfbCol &&
+                  kFc2SfbCol + 2 * (kFc2MaxI / 64) * 4 <= kTmemCols,
+              "FC2 shared memory / TMEM plan");
 
 // Activation rows of a tile arrive in boxes of 128, 64, 32 or 16 rows,
 // largest first: at most four copies per k-block.
@@ -100,6 +122,8 @@ __device__ void gemm_setup(Barriers* bars, int warp) {
     for (int b = 0; b < 2; ++b) {
       mbar_init(&bars->tmem_full[b], 1);
       mbar_init(&bars->tmem_empty[b], EPI_WARPS);
+      mbar_init(&bars->act_full[b], 1);
+      mbar_init(&bars->act_empty[b], 1);
     }
     mbar_init(&bars->drain, 1);
     bars->abort_flag = 0;
@@ -143,6 +167,25 @@ __device__ __forceinline__ int4 next_tile(const int4* tiles, int unit, int num_u
 __device__ __forceinline__ float4 unit_scalars(const Fc1Args& p, const int4& t) {
   if (t.x < 0 || t.x >= p.E) return make_float4(0.f, 0.f, 0.f, 0.f);
   return make_float4(__ldg(p.dXdW13 + t.x), __ldg(p.qA + t.x), __ldg(p.beta + t.x), __ldg(p.lam + t.x));
+}
+
+// FC2 work unit -> (token tile, group of G consecutive 128-feature tiles);
+// groups outermost, so the groups of one pass over H run together.
+__device__ __forceinline__ int4 fc2_next_tile(const int4* tiles, int unit, int num_units, int ntiles) {
+  return unit < num_units ? tiles[unit % ntiles] : make_int4(-1, 0, 0, 0);
+}
+
+// Feature tiles per FC2 unit: the largest divisor of the pass width npu that
+// still leaves 8 units per CTA, so that an activation tile is loaded once per
+// group while every SM stays busy.
+__device__ __forceinline__ int fc2_group(int ntiles, int NMT, int npu, int grid) {
+  int G = npu;
+  while (G > 1 && (int64_t)ntiles * (NMT / G) < 8LL * grid) {
+    do {
+      --G;
+    } while (npu % G);
+  }
+  return G;
 }
 
 // ================================================================== FC1
@@ -349,105 +392,137 @@ __global__ void __launch_bounds__(kFc2Threads, 1)
                const Fc2Args p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = aligned_smem(smem_raw);
-  Barriers* bars = reinterpret_cast<Barriers*>(smem + kFc2Stages * kFc2StageBytes);
+  Barriers* bars = reinterpret_cast<Barriers*>(smem);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int NMT = p.H / 128, NKB = p.I / kFc2KBlock, NA = p.I / 64;
+  const int NMT = p.H / 128, NKB = p.I / kFc2KBlock, NA = p.I / 64, npu = NMT / p.nq;
+  const int act_bytes = fc2_act_bytes(p.I), nstages = fc2_stages(p.I);
+  uint8_t* act = smem + 1024;                       // slot s at act + s * act_bytes
+  uint8_t* ring = act + 2 * act_bytes;              // stage s at ring + s * kFc2StageBytes
+  const uint32_t act_sf = (uint32_t)(NKB * 8192);   // scale atoms after the codes of a slot
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tm_w2);
     tma_prefetch_desc(&tm_aq.m16);
     tma_prefetch_desc(&tm_aq.m128);
   }
-  gemm_setup<kFc2Stages, kFc2EpiWarps>(bars, warp);
+  gemm_setup<kMaxStages, kFc2EpiWarps>(bars, warp);
   const uint32_t tmem = bars->tmem_base;
   pdl_wait();
   pdl_launch_dependents();
-  const int num_units = clamp_tiles(p.hdr[HDR_NUM_TT], p.max_tiles) * NMT;
+  const int ntiles = clamp_tiles(p.hdr[HDR_NUM_TT], p.max_tiles);
+  const int G = fc2_group(ntiles, NMT, npu, gridDim.x);
+  const int num_units = ntiles * (NMT / G);
   const int4* tiles = reinterpret_cast<const int4*>(p.tt_list);
 
   if (warp == 0) {
     if (lane == 0) {
+      // ---------------------------------------------------------- producer
       uint32_t stage = 0, phase = 0;
-      uint32_t armed = 0, last_phase = 0;
+      uint32_t armed = 0, last_phase = 0;   // ring stages
+      uint32_t act_armed = 0, act_last = 0;  // activation slots
+      int local = 0;
       bool ok = true;
-      int4 nxt = next_tile(tiles, blockIdx.x, num_units, NMT);
+      int4 nxt = fc2_next_tile(tiles, blockIdx.x, num_units, ntiles);
       for (int unit = blockIdx.x; unit < num_units && ok; unit += gridDim.x) {
         const int4 tl = nxt;
-        nxt = next_tile(tiles, unit + gridDim.x, num_units, NMT);
+        nxt = fc2_next_tile(tiles, unit + gridDim.x, num_units, ntiles);
         if (!tile_ok(tl, p.E, p.max_rows)) {
           set_status(p.status, DEVSTAT_BAD_TILE);
           continue;
         }
-        const int mt = unit % NMT;
+        const int mt0 = (unit / ntiles) * G;
         const int e = tl.x, row0 = tl.y, rows = tl.z;
         const int nch = (rows + kTokChunk - 1) / kTokChunk;
-        const uint32_t tx = 8192u + (uint32_t)nch * 1024u + 1024u + 1024u;
-        for (int kb = 0; kb < NKB; ++kb) {
-          if (!wait_or_abort(&bars->empty[stage], phase ^ 1u, bars, p.status)) {
-            ok = false;
-            break;
-          }
-          uint8_t* st = smem + stage * kFc2StageBytes;
-          mbar_arrive_expect_tx(&bars->full[stage], tx);
-          armed |= 1u << stage;
-          last_phase = (last_phase & ~(1u << stage)) | (phase << stage);
-          tma_load_3d(st + F2_A, &tm_w2, 0, 0, (e * NMT + mt) * NKB + kb, &bars->full[stage]);
-          load_rows(st + F2_B, tm_aq, kb * 64, row0, nch, 1024u, &bars->full[stage]);
-          bulk_g2s(st + F2_SA, p.sf2p + ((size_t)(e * NMT + mt) * NA + (size_t)kb * 2) * 512u, 1024u,
-                   &bars->full[stage]);
-          bulk_g2s(st + F2_SB, p.sfa + ((size_t)(row0 >> 7) * NA + (size_t)kb * 2) * 512u, 1024u,
-                   &bars->full[stage]);
-          if (++stage == kFc2Stages) {
-            stage = 0;
-            phase ^= 1u;
+        // the token tile's activations, once per unit
+        const uint32_t slot = (uint32_t)local & 1u, sph = ((uint32_t)local >> 1) & 1u;
+        if (!wait_or_abort(&bars->act_empty[slot], sph ^ 1u, bars, p.status)) break;
+        uint8_t* as = act + slot * act_bytes;
+        mbar_arrive_expect_tx(&bars->act_full[slot], (uint32_t)(NKB * nch * 1024 + NA * 512));
+        act_armed |= 1u << slot;
+        act_last = (act_last & ~(1u << slot)) | (sph << slot);
+        for (int kb = 0; kb < NKB; ++kb) load_rows(as + kb * 8192, tm_aq, kb * 64, row0, nch, 1024u, &bars->act_full[slot]);
+        bulk_g2s(as + act_sf, p.sfa + (size_t)(row0 >> 7) * NA * 512u, (uint32_t)(NA * 512), &bars->act_full[slot]);
+        ++local;
+        // the group's W2 tiles through the ring
+        for (int g = 0; g < G && ok; ++g) {
+          const int mt = mt0 + g;
+          for (int kb = 0; kb < NKB; ++kb) {
+            if (!wait_or_abort(&bars->empty[stage], phase ^ 1u, bars, p.status)) {
+              ok = false;
+              break;
+            }
+            uint8_t* st = ring + stage * kFc2StageBytes;
+            mbar_arrive_expect_tx(&bars->full[stage], 8192u + 1024u);
+            armed |= 1u << stage;
+            last_phase = (last_phase & ~(1u << stage)) | (phase << stage);
+            tma_load_3d(st, &tm_w2, 0, 0, (e * NMT + mt) * NKB + kb, &bars->full[stage]);
+            bulk_g2s(st + F2_SA, p.sf2p + ((size_t)(e * NMT + mt) * NA + (size_t)kb * 2) * 512u, 1024u,
+                     &bars->full[stage]);
+            if (++stage == (uint32_t)nstages) {
+              stage = 0;
+              phase ^= 1u;
+            }
           }
         }
       }
-      for (int s = 0; s < kFc2Stages; ++s)
+      // every issued copy has landed before the CTA may exit
+      for (int s = 0; s < nstages; ++s)
         if (armed & (1u << s)) mbar_wait(&bars->full[s], (last_phase >> s) & 1u, p.status);
+      for (int s = 0; s < 2; ++s)
+        if (act_armed & (1u << s)) mbar_wait(&bars->act_full[s], (act_last >> s) & 1u, p.status);
     }
   } else if (warp == 1) {
     if (lane == 0) {
+      // --------------------------------------------------------------- MMA
       uint32_t stage = 0, phase = 0;
-      int local = 0;
+      int local = 0, sub = 0;
       bool ok = true;
-      int4 nxt = next_tile(tiles, blockIdx.x, num_units, NMT);
+      int4 nxt = fc2_next_tile(tiles, blockIdx.x, num_units, ntiles);
       for (int unit = blockIdx.x; unit < num_units && ok; unit += gridDim.x) {
         const int4 tl = nxt;
-        nxt = next_tile(tiles, unit + gridDim.x, num_units, NMT);
+        nxt = fc2_next_tile(tiles, unit + gridDim.x, num_units, ntiles);
         if (!tile_ok(tl, p.E, p.max_rows)) continue;
         const uint32_t ncols = (uint32_t)((tl.z + kTokChunk - 1) / kTokChunk * kTokChunk);
         const uint32_t idesc = idesc_mxf4nvf4(128, ncols);
-        const uint32_t buf = (uint32_t)local & 1u;
-        if (!wait_or_abort(&bars->tmem_empty[buf], (((uint32_t)local >> 1) & 1u) ^ 1u, bars, p.status)) break;
+        const uint32_t slot = (uint32_t)local & 1u, sph = ((uint32_t)local >> 1) & 1u;
+        ++local;
+        if (!wait_or_abort(&bars->act_full[slot], sph, bars, p.status)) break;
         tc_fence_after();
-        const uint32_t dcol = tmem + buf * 128;
-        for (int kb = 0; kb < NKB; ++kb) {
-          if (!wait_or_abort(&bars->full[stage], phase, bars, p.status)) {
+        const uint8_t* as = act + slot * act_bytes;
+        const uint32_t sfb = tmem + kFc2SfbCol + slot * (uint32_t)(NA * 4);
+        for (int a = 0; a < NA; ++a) tmem_cp_32x128b_x4(sfb + a * 4, sf_desc(as + act_sf + a * 512));
+        for (int g = 0; g < G && ok; ++g, ++sub) {
+          const uint32_t buf = (uint32_t)sub & 1u;
+          if (!wait_or_abort(&bars->tmem_empty[buf], (((uint32_t)sub >> 1) & 1u) ^ 1u, bars, p.status)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint8_t* st = smem + stage * kFc2StageBytes;
-          const uint32_t sfc = tmem + 256 + stage * 16;
+          const uint32_t dcol = tmem + buf * 128;
+          for (int kb = 0; kb < NKB; ++kb) {
+            if (!wait_or_abort(&bars->full[stage], phase, bars, p.status)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint8_t* st = ring + stage * kFc2StageBytes;
+            const uint32_t sfc = tmem + 256 + stage * 8;
 #pragma unroll
-          for (int a = 0; a < 2; ++a) {
-            tmem_cp_32x128b_x4(sfc + a * 4, sf_desc(st + F2_SA + a * 512));
-            tmem_cp_32x128b_x4(sfc + 8 + a * 4, sf_desc(st + F2_SB + a * 512));
-          }
+            for (int a = 0; a < 2; ++a) tmem_cp_32x128b_x4(sfc + a * 4, sf_desc(st + F2_SA + a * 512));
 #pragma unroll
-          for (int ks = 0; ks < 2; ++ks) {
-            const uint64_t ad = smem_desc(smem_u32(st + F2_A) + ks * 32, 16, 512, kLayoutSW64);
-            const uint64_t bd = smem_desc(smem_u32(st + F2_B) + ks * 32, 16, 512, kLayoutSW64);
-            mma_mxf4nvf4(dcol, ad, bd, idesc, sfc + ks * 4, sfc + 8 + ks * 4, (kb | ks) ? 1u : 0u);
+            for (int ks = 0; ks < 2; ++ks) {
+              const uint64_t ad = smem_desc(smem_u32(st) + ks * 32, 16, 512, kLayoutSW64);
+              const uint64_t bd = smem_desc(smem_u32(as + kb * 8192) + ks * 32, 16, 512, kLayoutSW64);
+              mma_mxf4nvf4(dcol, ad, bd, idesc, sfc + ks * 4, sfb + (kb * 2 + ks) * 4, (kb | ks) ? 1u : 0u);
+            }
+            tc_commit(&bars->empty[stage]);
+            if (++stage == (uint32_t)nstages) {
+              stage = 0;
+              phase ^= 1u;
+            }
           }
-          tc_commit(&bars->empty[stage]);
-          if (++stage == kFc2Stages) {
-            stage = 0;
-            phase ^= 1u;
-          }
+          if (ok) tc_commit(&bars->tmem_full[buf]);
         }
-        if (ok) tc_commit(&bars->tmem_full[buf]);
-        ++local;
+        tc_commit(&bars->act_empty[slot]);   // the slot is free once these MMAs are done
       }
       tc_commit(&bars->drain);
       mbar_wait(&bars->drain, 0, p.status);
@@ -455,51 +530,78 @@ __global__ void __launch_bounds__(kFc2Threads, 1)
   } else {
     // ------------------------------------------------------------ epilogue
     constexpr int NGRP = kFc2EpiWarps / 4;
+    constexpr int NI = (kTileRows / kTokChunk + NGRP - 1) / NGRP;   // column chunks per warp
     const int q = warp & 3, grp = (warp - 2) >> 2;
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
-    int local = 0;
-    int4 nxt = next_tile(tiles, blockIdx.x, num_units, NMT);
+    int sub = 0;
+    int4 nxt = fc2_next_tile(tiles, blockIdx.x, num_units, ntiles);
     float s2_nxt = (nxt.x >= 0 && nxt.x < p.E) ? __ldg(p.dAdW2 + nxt.x) : 0.0f;
-    int4 nxt2 = next_tile(tiles, blockIdx.x + gridDim.x, num_units, NMT);
-    for (int unit = blockIdx.x; unit < num_units; unit += gridDim.x) {
+    int4 nxt2 = fc2_next_tile(tiles, blockIdx.x + gridDim.x, num_units, ntiles);
+    bool ok = true;
+    for (int unit = blockIdx.x; unit < num_units && ok; unit += gridDim.x) {
       const int4 tl = nxt;
       const float s2 = s2_nxt;
       nxt = nxt2;
       s2_nxt = (nxt.x >= 0 && nxt.x < p.E) ? __ldg(p.dAdW2 + nxt.x) : 0.0f;
-      nxt2 = next_tile(tiles, unit + 2 * gridDim.x, num_units, NMT);
+      nxt2 = fc2_next_tile(tiles, unit + 2 * gridDim.x, num_units, ntiles);
       if (!tile_ok(tl, p.E, p.max_rows)) continue;
-      const int mt = unit % NMT;
+      const int mt0 = (unit / ntiles) * G;
       const int row0 = tl.y, rows = tl.z;
-      // route weights of this warp's columns, loaded before waiting on the accumulator
-      float wgt[(kTileRows / kTokChunk + NGRP - 1) / NGRP];
-#pragma unroll
-      for (int i = 0; i < (kTileRows / kTokChunk + NGRP - 1) / NGRP; ++i) {
-        const int col = (grp + i * NGRP) * 16 + (lane & 15);
-        wgt[i] = (col < rows) ? __ldg(p.wrow + row0 + col) : 0.0f;
-      }
-      const uint32_t buf = (uint32_t)local & 1u;
-      if (!wait_or_abort(&bars->tmem_full[buf], ((uint32_t)local >> 1) & 1u, bars, p.status)) break;
-      tc_fence_after();
       const int nch = (rows + kTokChunk - 1) / kTokChunk;
-      float* ybase = p.y + (size_t)row0 * p.H + (size_t)mt * 128 + q * 32 + lane;
+      // route weight and token (-1 if none) of this warp's columns, once per unit
+      float wgt[NI];
+      int tok[NI];
 #pragma unroll
-      for (int i = 0; i < (kTileRows / kTokChunk + NGRP - 1) / NGRP; ++i) {
-        const int c = grp + i * NGRP;
-        if (c >= nch) break;
-        uint32_t r[16];
-        tmem_ld16(tmem + lane_base + buf * 128 + c * 16, r);
-        tmem_ld_wait();
-#pragma unroll
-        for (int cc = 0; cc < 16; ++cc) {
-          const float wv = __shfl_sync(0xffffffffu, wgt[i], cc);
-          const int col = c * 16 + cc;
-          if (col < rows) ybase[(size_t)col * p.H] = __fmul_rn(__fmul_rn(__uint_as_float(r[cc]), s2), wv);
+      for (int i = 0; i < NI; ++i) {
+        const int col = (grp + i * NGRP) * 16 + (lane & 15);
+        wgt[i] = 0.0f;
+        tok[i] = -1;
+        if (col < rows) {
+          const int f = __ldg(p.prow_pair + row0 + col);
+          if (f >= 0 && f < p.num_pairs) {
+            wgt[i] = __ldg(p.wrow + row0 + col);
+            tok[i] = f / p.k;
+          }
         }
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->tmem_empty[buf]);
-      ++local;
+      for (int g = 0; g < G; ++g, ++sub) {
+        const uint32_t buf = (uint32_t)sub & 1u;
+        if (!wait_or_abort(&bars->tmem_full[buf], ((uint32_t)sub >> 1) & 1u, bars, p.status)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        // drain this warp's columns from TMEM first, so the MMA can refill the buffer under the reductions
+        uint32_t r[NI][16];
+#pragma unroll
+        for (int i = 0; i < NI; ++i)
+          if (grp + i * NGRP < nch) tmem_ld16(tmem + lane_base + buf * 128 + (grp + i * NGRP) * 16, r[i]);
+        tmem_ld_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->tmem_empty[buf]);
+        float* accf = p.acc + (size_t)(mt0 + g) * 128 + q * 32 + lane;
+#pragma unroll
+        for (int i = 0; i < NI; ++i) {
+          if (grp + i * NGRP >= nch) break;
+          // per 8 columns: broadcast their weights and tokens first, then issue 8 reductions back to back
+#pragma unroll
+          for (int h = 0; h < 16; h += 8) {
+            float wv[8];
+            int tc[8];
+#pragma unroll
+            for (int cc = 0; cc < 8; ++cc) {
+              wv[cc] = __shfl_sync(0xffffffffu, wgt[i], h + cc);
+              tc[cc] = __shfl_sync(0xffffffffu, tok[i], h + cc);
+            }
+#pragma unroll
+            for (int cc = 0; cc < 8; ++cc)
+              if (tc[cc] >= 0)
+                atomicAdd(accf + (size_t)tc[cc] * p.H,
+                          __fmul_rn(__fmul_rn(__uint_as_float(r[i][h + cc]), s2), wv[cc]));
+          }
+        }
+      }
     }
   }
   tc_fence_before();

@@ -16,6 +16,7 @@ constexpr int kRouteSmallMax = 4096;  // pairs handled by the one-CTA routing ke
 constexpr int kRouteChunk = 4096;     // pairs per CTA of the multi-CTA routing kernels
 constexpr int kMaxExperts = 1024;
 constexpr int kMaxTopK = 32;
+constexpr size_t kAccPassBytes = 64u << 20;  // default L2 budget of one combine pass over H
 
 // Workspace header words (int32).
 enum : int {
@@ -42,7 +43,7 @@ struct WsLayout {
   int64_t max_tokens, Pmax, PpadMax, TTmax, nblkMax;
   size_t header, count, cumsum, offs, poffs, ttoffs;
   size_t sorted_row, gather, row_pos, prow_pair, tt_list, blockhist;
-  size_t xq, sfx, aq, sfa, y, wrow, beta_def, lam_def;
+  size_t xq, sfx, aq, sfa, acc, wrow, beta_def, lam_def;
   size_t total;
 };
 
@@ -82,7 +83,7 @@ inline WsLayout make_layout(const Shape& s, int64_t max_tokens) {
   L.sfx = take((size_t)(L.PpadMax / kTileRows) * (s.H / 64) * 512);
   L.aq = take((size_t)L.PpadMax * (s.I / 2));
   L.sfa = take((size_t)(L.PpadMax / kTileRows) * (s.I / 64) * 512);
-  L.y = take((size_t)L.PpadMax * s.H * 4);
+  L.acc = take((size_t)max_tokens * s.H * 4);
   L.wrow = take((size_t)L.PpadMax * 4);
   L.beta_def = take((size_t)s.E * 4);
   L.lam_def = take((size_t)s.E * 4);
@@ -135,9 +136,10 @@ struct Fc2Args {
   const int32_t* prow_pair;
   const float* wrow;        // [Ppad] route weight of the pair in each padded row
   const float* dAdW2;
-  float* y;                 // [Ppad, H] fp32: route-weighted FC2 output of every routed pair
+  float* acc;               // [T, H] fp32: sum over a token's pairs of route weight x FC2 output
   int32_t* status;
   int32_t H, I, E, k;
+  int32_t nq;               // passes over H (H/128 divisible by nq)
   int32_t max_tiles;
   int64_t max_rows;
   int64_t num_pairs;      // T * k of this call
@@ -172,6 +174,7 @@ struct QuantXArgs {
   const int32_t* row_pos;   // [T*k] padded expanded row of each pair, -1 if not routed
   const uint16_t* route_w;  // [T*k] bf16 route weights
   float* wrow;              // [Ppad] out: route weight of each padded row (fp32)
+  float* acc;               // [T, H] out: zeroed
   const float* qX;          // [1]
   uint8_t* xq;              // [Ppad, H/2]
   uint8_t* sfx;             // atom layout, H/16 chunks per row

@@ -1,4 +1,4 @@
-// quant.cu -- activation quantization with token gather, BF16 finalize,
+// quant.cu -- activation quantization with token gather, the BF16 finalize,
 // weight preparation into the kernel layout, and the test kernels that expose
 // the device quantizer and codecs.
 #include <cuda_bf16.h>
@@ -16,7 +16,9 @@ cudaError_t launch_with_pdl(const void* fn, dim3 grid, dim3 block, size_t smem, 
 // qX) once, and writes the codes and block scales to the padded expanded row
 // of every pair the token is routed to ("npu_moe_init_routing_v2", formula 5,
 // gather form: expandedX[gatherRowIdx[i]] = quantResult[i // k]).  It also
-// stores each pair's route weight (fp32) at the pair's padded row for FC2.
+// stores each pair's route weight (fp32) at the pair's padded row for FC2,
+// and zeroes the token's fp32 combine accumulator row, into which FC2 adds
+// the token's route-weighted expert outputs.
 __global__ void __launch_bounds__(256) quant_x_kernel(const QuantXArgs a) {
   const int lane = threadIdx.x & 31;
   const int64_t t = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
@@ -27,6 +29,8 @@ __global__ void __launch_bounds__(256) quant_x_kernel(const QuantXArgs a) {
   const float q = __ldg(a.qX);
   const int rp = (lane < a.k) ? a.row_pos[t * a.k + lane] : -1;
   if (rp >= 0 && rp < a.max_rows) a.wrow[rp] = bf16_bits_to_f32(a.route_w[t * a.k + lane]);
+  float4* accr = reinterpret_cast<float4*>(a.acc + t * H);
+  for (int i = lane; i < H / 4; i += 32) accr[i] = make_float4(0.f, 0.f, 0.f, 0.f);
   const uint4* xr = reinterpret_cast<const uint4*>(a.x + t * H);
   for (int g0 = 0; g0 < G; g0 += 32) {
     const int g = g0 + lane;
@@ -60,36 +64,25 @@ __global__ void __launch_bounds__(256) quant_x_kernel(const QuantXArgs a) {
 }
 
 // ------------------------------------------------------------------ finalize
-// out[t, h] = bf16_rn( sum_j y[row_pos[t*k + j], h] ) ("Cake SiTU backend":
-// BF16 weighted finalization).  y already carries the route weight; the k
-// rows of a token are added in j order in fp32 and rounded once.  One thread
-// per 8 consecutive outputs of a token; pairs that were not routed are skipped.
-__global__ void __launch_bounds__(256) finalize_kernel(const float* __restrict__ y, const int32_t* __restrict__ row_pos,
-                                                       uint16_t* __restrict__ out, int64_t T, int H, int k,
-                                                       int64_t max_rows) {
+// out[t, h] = bf16_rn(acc[t, h]) ("Cake SiTU backend": BF16 weighted
+// finalization).  FC2 has added every routed pair's route-weighted output
+// into acc in fp32; this rounds once.  One thread per 8 consecutive outputs.
+__global__ void __launch_bounds__(256) finalize_kernel(const float* __restrict__ acc, uint16_t* __restrict__ out,
+                                                       int64_t n8) {
   pdl_wait();
   pdl_launch_dependents();
-  const int per_tok = H / 8;
-  const int64_t n = T * per_tok;
-  for (int64_t i = (int64_t)blockIdx.x * 256 + threadIdx.x; i < n; i += (int64_t)gridDim.x * 256) {
-    const int64_t t = i / per_tok;
-    const int h8 = (int)(i % per_tok);
-    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    for (int j = 0; j < k; ++j) {
-      const int rp = __ldg(row_pos + t * k + j);
-      if (rp < 0 || rp >= max_rows) continue;
-      const float4* src = reinterpret_cast<const float4*>(y + (size_t)rp * H) + 2 * h8;
-      const float4 a = __ldcs(src), b = __ldcs(src + 1);
-      acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
-      acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
-    }
+  const float4* src = reinterpret_cast<const float4*>(acc);
+  uint4* dst = reinterpret_cast<uint4*>(out);
+  for (int64_t i = (int64_t)blockIdx.x * 256 + threadIdx.x; i < n8; i += (int64_t)gridDim.x * 256) {
+    const float4 a = __ldcs(src + 2 * i), b = __ldcs(src + 2 * i + 1);
     uint32_t w[4];
+    const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      const __nv_bfloat162 h = __floats2bfloat162_rn(acc[2 * j], acc[2 * j + 1]);
+      const __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * j], v[2 * j + 1]);
       w[j] = *reinterpret_cast<const uint32_t*>(&h);
     }
-    reinterpret_cast<uint4*>(out)[i] = make_uint4(w[0], w[1], w[2], w[3]);
+    dst[i] = make_uint4(w[0], w[1], w[2], w[3]);
   }
 }
 
@@ -234,11 +227,11 @@ cudaError_t launch_quant_x(const QuantXArgs& a, cudaStream_t st) {
   return launch_with_pdl((const void*)quant_x_kernel, dim3(blocks), dim3(256), 0, st, kargs);
 }
 
-cudaError_t launch_finalize(const float* y, const int32_t* row_pos, uint16_t* out, int64_t T, int H, int k,
-                            int64_t max_rows, int num_sms, cudaStream_t st) {
-  void* kargs[] = {(void*)&y, (void*)&row_pos, (void*)&out, (void*)&T, (void*)&H, (void*)&k, (void*)&max_rows};
-  const int64_t want = (T * (H / 8) + 255) / 256;
-  const unsigned blocks = (unsigned)(want < (int64_t)num_sms * 16 ? want : (int64_t)num_sms * 16);
+cudaError_t launch_finalize(const float* acc, uint16_t* out, int64_t T, int H, int num_sms, cudaStream_t st) {
+  int64_t n8 = T * (H / 8);
+  void* kargs[] = {(void*)&acc, (void*)&out, (void*)&n8};
+  const int64_t want = (n8 + 255) / 256;
+  const unsigned blocks = (unsigned)(want < (int64_t)num_sms * 8 ? want : (int64_t)num_sms * 8);
   return launch_with_pdl((const void*)finalize_kernel, dim3(blocks ? blocks : 1), dim3(256), 0, st, kargs);
 }
 
