@@ -19,6 +19,7 @@ cudaError_t routing_set_attributes(int E);
 cudaError_t launch_init_move(const InitMoveArgs& a, cudaStream_t st);
 cudaError_t launch_init_finish(const InitFinishArgs& a, cudaStream_t st, int num_sms);
 cudaError_t launch_quant_x(const QuantXArgs& a, cudaStream_t st);
+cudaError_t launch_sf_atoms(const SfAtomArgs& a, int64_t max_words, int num_sms, cudaStream_t st);
 cudaError_t launch_finalize(const float* acc, uint16_t* out, int64_t T, int H, int num_sms, cudaStream_t st);
 cudaError_t launch_prep(const PrepArgs& a, cudaStream_t st, int num_sms);
 cudaError_t launch_codec_sweep(uint32_t start, int64_t n, uint8_t* lo, uint8_t* hi, uint8_t* e4, cudaStream_t st,
@@ -218,7 +219,11 @@ static RouteArgs route_args(const Shape& s, const WsLayout& L, uint8_t* ws, cons
   return a;
 }
 
-static int forward_launches(int64_t P) { return (P <= kRouteSmallMax ? 1 : 2) + 4; }
+// Above this many routed pairs the X block scales are written token-major
+// and laid out in atoms by a second kernel.
+constexpr int64_t kSfTwoPassMin = 65536;
+
+static int forward_launches(int64_t P) { return (P <= kRouteSmallMax ? 1 : 2) + 4 + (P > kSfTwoPassMin ? 1 : 0); }
 
 // Passes of the FC2 combine over H: the fewest (a divisor of H/128) whose
 // accumulator slice, T x H/nq fp32, fits the L2 budget (NVFP4MOE_ACC_PASS_MB
@@ -398,12 +403,26 @@ moe_status_t moe_forward(const moe_shape_t* shape, int64_t num_tokens, const voi
   qa.qX = qX;
   qa.xq = w + L.xq;
   qa.sfx = w + L.sfx;
+  qa.sft = P > kSfTwoPassMin ? w + L.sft : nullptr;
   qa.T = T;
   qa.H = s.H;
   qa.k = s.k;
   qa.max_rows = L.PpadMax;
   prof_mark(1, stream);
   MOE_CUDA(launch_quant_x(qa, stream));
+  if (qa.sft) {
+    SfAtomArgs sa{};
+    sa.sft = qa.sft;
+    sa.prow_pair = ra.prow_pair;
+    sa.tt_list = ra.tt_list;
+    sa.hdr = ra.hdr;
+    sa.sfx = reinterpret_cast<uint32_t*>(w + L.sfx);
+    sa.num_pairs = P;
+    sa.H = s.H;
+    sa.k = s.k;
+    sa.max_tiles = (int32_t)L.TTmax;
+    MOE_CUDA(launch_sf_atoms(sa, tt_bound(P, s.E) * (s.H / 64) * 128, sms, stream));
+  }
 
   // 3. FC1 + SiTU + requant
   const int64_t tt = tt_bound(P, s.E);

@@ -43,7 +43,7 @@ struct WsLayout {
   int64_t max_tokens, Pmax, PpadMax, TTmax, nblkMax;
   size_t header, count, cumsum, offs, poffs, ttoffs;
   size_t sorted_row, gather, row_pos, prow_pair, tt_list, blockhist;
-  size_t xq, sfx, aq, sfa, acc, wrow, beta_def, lam_def;
+  size_t xq, sfx, sft, aq, sfa, acc, wrow, beta_def, lam_def;
   size_t total;
 };
 
@@ -81,6 +81,7 @@ inline WsLayout make_layout(const Shape& s, int64_t max_tokens) {
   L.blockhist = take((size_t)L.nblkMax * s.E * 4);
   L.xq = take((size_t)L.PpadMax * (s.H / 2));
   L.sfx = take((size_t)(L.PpadMax / kTileRows) * (s.H / 64) * 512);
+  L.sft = take((size_t)max_tokens * (s.H / 16));
   L.aq = take((size_t)L.PpadMax * (s.I / 2));
   L.sfa = take((size_t)(L.PpadMax / kTileRows) * (s.I / 64) * 512);
   L.acc = take((size_t)max_tokens * s.H * 4);
@@ -177,10 +178,22 @@ struct QuantXArgs {
   float* acc;               // [T, H] out: zeroed
   const float* qX;          // [1]
   uint8_t* xq;              // [Ppad, H/2]
-  uint8_t* sfx;             // atom layout, H/16 chunks per row
+  uint8_t* sfx;             // atom layout, H/16 chunks per row (written here when sft is null)
+  uint8_t* sft;             // [T, H/16] token-major block scales, or null
   int64_t T;
   int32_t H, k;
   int64_t max_rows;         // padded rows of the workspace
+};
+
+// Block scales of X from token-major rows into the atom layout of the padded rows.
+struct SfAtomArgs {
+  const uint8_t* sft;       // [T, H/16]
+  const int32_t* prow_pair; // [Ppad] flat pair of each padded row
+  const int32_t* tt_list;   // int4 {expert, row0, rows, 0} per 128-row tile, in row order
+  const int32_t* hdr;
+  uint32_t* sfx;            // atom layout
+  int64_t num_pairs;
+  int32_t H, k, max_tiles;
 };
 
 struct PrepArgs {

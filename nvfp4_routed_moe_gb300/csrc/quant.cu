@@ -18,7 +18,11 @@ cudaError_t launch_with_pdl(const void* fn, dim3 grid, dim3 block, size_t smem, 
 // gather form: expandedX[gatherRowIdx[i]] = quantResult[i // k]).  It also
 // stores each pair's route weight (fp32) at the pair's padded row for FC2,
 // and zeroes the token's fp32 combine accumulator row, into which FC2 adds
-// the token's route-weighted expert outputs.
+// the token's route-weighted expert outputs.  Block scales go straight into
+// the atom layout of every routed row (few tokens), or, for large batches,
+// once per token into token-major rows that sf_atoms_kernel then lays out
+// with whole-atom writes (a token's scales land in 56 different atoms, and
+// scattered 4-byte writes cost more than the extra pass).
 __global__ void __launch_bounds__(256) quant_x_kernel(const QuantXArgs a) {
   const int lane = threadIdx.x & 31;
   const int64_t t = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
@@ -54,12 +58,40 @@ __global__ void __launch_bounds__(256) quant_x_kernel(const QuantXArgs a) {
     uint32_t word = sf << (8 * (lane & 3));
     word |= __shfl_xor_sync(0xffffffffu, word, 1);
     word |= __shfl_xor_sync(0xffffffffu, word, 2);
+    if (a.sft && valid && (lane & 3) == 0) *reinterpret_cast<uint32_t*>(a.sft + t * G + g) = word;
     for (int j = 0; j < a.k; ++j) {
       const int row = __shfl_sync(0xffffffffu, rp, j);
       if (row < 0 || row >= a.max_rows || !valid) continue;
       *reinterpret_cast<uint2*>(a.xq + (size_t)row * (H / 2) + g * 8) = packed;
-      if ((lane & 3) == 0) *reinterpret_cast<uint32_t*>(a.sfx + atom_offset(row, g, KC)) = word;
+      if (!a.sft && (lane & 3) == 0) *reinterpret_cast<uint32_t*>(a.sfx + atom_offset(row, g, KC)) = word;
     }
+  }
+}
+
+// ------------------------------------------------------------ scale atoms
+// One thread per 4-byte word of the atom layout ("Nvfp4 Tensor", block-scale
+// atom: byte (row%32)*16 + ((row%128)/32)*4 + chunk%4 of atom (row/128,
+// chunk/4)): the word holds the scales of chunks 4c..4c+3 of padded row
+// tile*128 + 32j + l, copied from that row's token in the token-major scales;
+// rows past a tile's fill are zero.
+__global__ void __launch_bounds__(256) sf_atoms_kernel(const SfAtomArgs a) {
+  pdl_wait();
+  pdl_launch_dependents();
+  const int ntiles = min(a.hdr[HDR_NUM_TT], a.max_tiles);
+  const int NA4 = a.H / 64, G = a.H / 16;
+  const int64_t words = (int64_t)(ntiles > 0 ? ntiles : 0) * NA4 * 128;
+  const int4* tiles = reinterpret_cast<const int4*>(a.tt_list);
+  for (int64_t w = (int64_t)blockIdx.x * 256 + threadIdx.x; w < words; w += (int64_t)gridDim.x * 256) {
+    const int64_t tile = w / (NA4 * 128);
+    const int rem = (int)(w - tile * NA4 * 128);
+    const int atom = rem >> 7, wi = rem & 127;
+    const int rr = (wi & 3) * 32 + (wi >> 2);    // row within the tile
+    uint32_t v = 0;
+    if (rr < __ldg(&tiles[tile].z)) {
+      const int f = __ldg(a.prow_pair + tile * kTileRows + rr);
+      if (f >= 0 && f < a.num_pairs) v = __ldg(reinterpret_cast<const uint32_t*>(a.sft + (int64_t)(f / a.k) * G) + atom);
+    }
+    a.sfx[w] = v;
   }
 }
 
@@ -225,6 +257,14 @@ cudaError_t launch_quant_x(const QuantXArgs& a, cudaStream_t st) {
   void* kargs[] = {&args};
   const unsigned blocks = (unsigned)((a.T + 7) / 8);
   return launch_with_pdl((const void*)quant_x_kernel, dim3(blocks), dim3(256), 0, st, kargs);
+}
+
+cudaError_t launch_sf_atoms(const SfAtomArgs& a, int64_t max_words, int num_sms, cudaStream_t st) {
+  SfAtomArgs args = a;
+  void* kargs[] = {&args};
+  const int64_t want = (max_words + 255) / 256;
+  const unsigned blocks = (unsigned)(want < (int64_t)num_sms * 8 ? want : (int64_t)num_sms * 8);
+  return launch_with_pdl((const void*)sf_atoms_kernel, dim3(blocks ? blocks : 1), dim3(256), 0, st, kargs);
 }
 
 cudaError_t launch_finalize(const float* acc, uint16_t* out, int64_t T, int H, int num_sms, cudaStream_t st) {

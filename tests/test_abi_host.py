@@ -96,3 +96,4 @@ def test_null_and_bad_args_rejected_without_device(L):
 def test_launch_count(L):
     assert api.moe_forward_launch_count(api.shape(3584, 384, 896, 16), 1) == 5
     assert api.moe_forward_launch_count(api.shape(3584, 384, 896, 16), 4096) == 6
+    assert api.moe_forward_launch_count(api.shape(3584, 384, 896, 16), 16384) == 7

@@ -76,6 +76,41 @@ def test_tiny_intermediates(tiny):
     assert mism <= 0.01 * total, f"A code mismatch rate {mism}/{total}"
 
 
+def test_two_pass_scale_layout_bit_exact():
+    """Above 65536 routed pairs the X block scales are written per token and
+    then laid out in atoms by a second pass.  On sampled tiles (and the last,
+    partly filled one) the atoms equal the oracle's scales of each row's token
+    scattered through the oracle's atom layout, zero on rows past the tile's
+    fill, and the packed codes equal the oracle's."""
+    base = cases.prepare_tiny(3)
+    inp = gen.tiny(3, 16400)          # weights and per-expert scales of the 16-token case
+    for name in ("w13", "sf13", "w2", "sf2", "dXdW13", "qA", "dAdW2"):
+        setattr(inp, name, getattr(base, name))
+    m = Model(inp)
+    out, ws = m.forward_inputs()
+    torch.cuda.synchronize()
+    assert api.moe_read_status(ws) == (0, 0)
+    lay = ws_view(m, ws)
+    T, k, H = inp.T, inp.k, inp.H
+    ntiles = int(ws_i32(ws, lay.header, 8)[2])
+    prow_pair = ws_i32(ws, lay.prow_pair, ntiles * 128)
+    tl = ws_i32(ws, lay.tt_list, 4 * ntiles).reshape(ntiles, 4)
+    xq_ref, xsf_ref = oracle.nvfp4_quant_rows(gen.bf16_bits_to_f32(inp.x), q=inp.qX)
+    atom_bytes = (H // 64) * 512
+    sample = set(np.random.default_rng(0).choice(ntiles, 6, replace=False).tolist()) | {ntiles - 1}
+    for tile in sorted(sample):
+        rows = int(tl[tile, 2])
+        toks = prow_pair[tile * 128:tile * 128 + rows] // k
+        exp_rows = np.zeros((128, H // 16), np.uint8)
+        exp_rows[:rows] = xsf_ref[toks]
+        got = ws_u8(ws, lay.sfx + tile * atom_bytes, atom_bytes)
+        np.testing.assert_array_equal(got, oracle.to_atom_layout(exp_rows))
+        xq = ws_u8(ws, lay.xq + tile * 128 * (H // 2), rows * (H // 2)).reshape(rows, H // 2)
+        np.testing.assert_array_equal(xq, xq_ref[toks])
+    toks = np.arange(0, T, 97)
+    assert_close(out_bits(out)[toks], cases.run_oracle(inp, tokens=toks), "two-pass scales")
+
+
 @pytest.mark.parametrize("T", [1, 2, 7, 33, 300])
 def test_tiny_shape_ragged_token_counts(T):
     inp = cases.prepare_tiny(1, T=T)
