@@ -1,23 +1,21 @@
 // gemm.cu -- the two block-scaled NVFP4 grouped GEMMs on tcgen05.
 //
-// Both kernels put the weights on the MMA's M side (128 weight rows per MMA)
-// and the tokens routed to one expert on the N side (16..128 padded rows of
-// the expert's segment), so one weight tile serves every token of the tile
-// and decode-sized groups still fill the 128-row MMA.
-//
 // FC1 ("Cake SiTU backend": FC1 over gate and up, SiTU, intermediate NVFP4
-// requantization): a prepared W13 tile holds 64 intermediate features with
-// gate and up rows interleaved (row 2i = gate of feature i, row 2i+1 = up),
-// so the two halves of one feature land in neighbouring TMEM lanes of the
-// same warp.  Per work unit (token tile, 64 features) one accumulator
-// [128 rows x N tokens] collects K = H over k-blocks of 256 FP4 elements;
-// accumulators are double-buffered in TMEM so the epilogue of one unit runs
-// under the MMAs of the next.  The epilogue forms z = acc * dX*dW13[e],
-// a = SiTU(z_g, z_u) (one shuffle pairs g and u; even lanes take one token
-// column, odd lanes the next), and quantizes a per 16 features with qA[e]
-// into the padded expanded rows of A (codes + atom-layout scales).
+// requantization): the MMA takes the routed tokens of one expert tile on its
+// M side (128 rows; a decode-sized group fills only the first rows, which
+// costs the tensor pipe no more than a narrow N would) and one prepared W13
+// tile on its N side: 128 rows holding 64 intermediate features with gate and
+// up rows interleaved (row 2i = gate of feature i, row 2i+1 = up).  Per work
+// unit (token tile, 64 features) one accumulator [128 tokens x 128] collects
+// K = H over k-blocks of 256 FP4 elements; accumulators are double-buffered in
+// TMEM so the epilogue of one unit runs under the MMAs of the next.  In the
+// epilogue a thread owns one token row: it reads 16 features' gate/up pairs,
+// forms z = acc * dX*dW13[e] and a = SiTU(z_g, z_u), and quantizes the 16
+// values with qA[e] in registers into the token's padded row of A (codes and
+// atom-layout scale) -- no cross-lane traffic.
 //
-// FC2 ("Cake SiTU backend": FC2, BF16 weighted finalization): a work unit is
+// FC2 ("Cake SiTU backend": FC2, BF16 weighted finalization): weights on the
+// MMA's M side (128 output features), tokens on N (16..128).  A work unit is
 // one token tile and a group of G consecutive 128-feature output tiles.  The
 // tile's quantized activations (K = I, all k-blocks) are loaded into a shared
 // memory slot once and stay there while the group's W2 tiles stream through
@@ -262,8 +260,7 @@ __global__ void __launch_bounds__(kFc1Threads, 1)
         const int4 tl = nxt;
         nxt = next_tile(tiles, unit + gridDim.x, num_units, NIT);
         if (!tile_ok(tl, p.E, p.max_rows)) continue;
-        const uint32_t ncols = (uint32_t)((tl.z + kTokChunk - 1) / kTokChunk * kTokChunk);
-        const uint32_t idesc = idesc_mxf4nvf4(128, ncols);
+        const uint32_t idesc = idesc_mxf4nvf4(128, 128);
         const uint32_t buf = (uint32_t)local & 1u;
         if (!wait_or_abort(&bars->tmem_empty[buf], (((uint32_t)local >> 1) & 1u) ^ 1u, bars, p.status)) break;
         tc_fence_after();
@@ -282,10 +279,10 @@ __global__ void __launch_bounds__(kFc1Threads, 1)
             tmem_cp_32x128b_x4(sfc + 16 + a * 4, sf_desc(st + F1_SB + a * 512));
           }
 #pragma unroll
-          for (int ks = 0; ks < 4; ++ks) {
-            const uint64_t ad = smem_desc(smem_u32(st + F1_A) + ks * 32, 16, 1024, kLayoutSW128);
-            const uint64_t bd = smem_desc(smem_u32(st + F1_B) + ks * 32, 16, 1024, kLayoutSW128);
-            mma_mxf4nvf4(dcol, ad, bd, idesc, sfc + ks * 4, sfc + 16 + ks * 4, (kb | ks) ? 1u : 0u);
+          for (int ks = 0; ks < 4; ++ks) {   // M = tokens (X tile), N = W13 rows
+            const uint64_t xd = smem_desc(smem_u32(st + F1_B) + ks * 32, 16, 1024, kLayoutSW128);
+            const uint64_t wd = smem_desc(smem_u32(st + F1_A) + ks * 32, 16, 1024, kLayoutSW128);
+            mma_mxf4nvf4(dcol, xd, wd, idesc, sfc + 16 + ks * 4, sfc + ks * 4, (kb | ks) ? 1u : 0u);
           }
           tc_commit(&bars->empty[stage]);
           if (++stage == kFc1Stages) {
@@ -301,11 +298,12 @@ __global__ void __launch_bounds__(kFc1Threads, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    constexpr int NGRP = kFc1EpiWarps / 4;     // warps per 32-lane quarter
+    // Warp w drains TMEM lanes 32*(w%4).. (its tokens) and the 32 accumulator
+    // columns of 16 features: group (w-2)/4 of the unit's 64.
     const int q = warp & 3, grp = (warp - 2) >> 2;
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
     const int I2 = p.I / 2, KC = p.I / 16;
-    const bool odd = (lane & 1) != 0;
+    const int r = q * 32 + lane;                      // token row within the tile
     int local = 0;
     int4 nxt = next_tile(tiles, blockIdx.x, num_units, NIT);
     float4 sc_nxt = unit_scalars(p, nxt);
@@ -323,60 +321,32 @@ __global__ void __launch_bounds__(kFc1Threads, 1)
       if (!wait_or_abort(&bars->tmem_full[buf], ((uint32_t)local >> 1) & 1u, bars, p.status)) break;
       tc_fence_after();
       const float s13 = sc.x, qa = sc.y, be = sc.z, la = sc.w;
-      const int nch = (rows + kTokChunk - 1) / kTokChunk;
-      const int chunk16 = it * 4 + q;                        // 16-feature group of this quarter
-      const size_t aq_off = (size_t)it * 32 + (size_t)q * 8 + (size_t)(lane >> 4) * 4;
       const float inv_be = 1.0f / be, inv_la = 1.0f / la;
-      for (int c = grp; c < nch; c += NGRP) {
-        uint32_t r[16];
-        tmem_ld16(tmem + lane_base + buf * 128 + c * 16, r);
+      // columns 2i / 2i+1 = gate / up of feature it*64 + 16*grp + i
+      uint32_t v0[16], v1[16];
+      const bool any = q * 32 < rows;                  // warp-uniform: this quarter holds tokens
+      if (any) {
+        tmem_ld16(tmem + lane_base + buf * 128 + grp * 32, v0);
+        tmem_ld16(tmem + lane_base + buf * 128 + grp * 32 + 16, v1);
         tmem_ld_wait();
-        // Pass 1: SiTU and the per-group amax of 8 column pairs.  Even lane l
-        // holds the gate of feature l/2, odd lane the up; even lanes evaluate
-        // column 2pp, odd lanes column 2pp+1.
-        float act[8], amx[8];
-#pragma unroll
-        for (int pp = 0; pp < 8; ++pp) {
-          const float m0 = __uint_as_float(r[2 * pp]), m1 = __uint_as_float(r[2 * pp + 1]);
-          const float recv = __shfl_xor_sync(0xffffffffu, odd ? m0 : m1, 1);
-          const float g = __fmul_rn(odd ? recv : m0, s13);
-          const float u = __fmul_rn(odd ? m1 : recv, s13);
-          act[pp] = situ_f32(g, u, be, inv_be, la, inv_la);
-          float m = fabsf(act[pp]);
-#pragma unroll
-          for (int off = 2; off <= 16; off <<= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-          amx[pp] = m;
-        }
-        // Pass 2: lane 2pp+p computes the block scale of (column pair pp, parity p) once.
-        const int sel = (lane >> 1) & 7;  // a select tree keeps amx[] in registers
-        const float a01 = (sel & 1) ? amx[1] : amx[0], a23 = (sel & 1) ? amx[3] : amx[2];
-        const float a45 = (sel & 1) ? amx[5] : amx[4], a67 = (sel & 1) ? amx[7] : amx[6];
-        const float a03 = (sel & 2) ? a23 : a01, a47 = (sel & 2) ? a67 : a45;
-        const float am = (sel & 4) ? a47 : a03;
-        float rr;
-        const uint32_t sfv = nvfp4_scale(am, qa, rr);
-        // Pass 3: codes with the broadcast scale, packed and stored.
-#pragma unroll
-        for (int pp = 0; pp < 8; ++pp) {
-          const int src = 2 * pp + (lane & 1);
-          const float rp = __shfl_sync(0xffffffffu, rr, src);
-          const uint32_t sf = __shfl_sync(0xffffffffu, sfv, src);
-          uint32_t v = cvt_e2m1x2(0.0f, __fmul_rn(act[pp], rp)) & 0xFu;
-          v = (v | (__shfl_down_sync(0xffffffffu, v, 2) << 4)) & 0xFFu;
-          const uint32_t word = v | (__shfl_down_sync(0xffffffffu, v, 4) << 8) |
-                                (__shfl_down_sync(0xffffffffu, v, 8) << 16) |
-                                (__shfl_down_sync(0xffffffffu, v, 12) << 24);
-          const int col = c * 16 + 2 * pp + (lane & 1);
-          if (col < rows) {
-            const int64_t prow = row0 + col;
-            if ((lane & ~17) == 0) *reinterpret_cast<uint32_t*>(p.aq + (size_t)prow * I2 + aq_off) = word;
-            if (lane < 2) p.sfa[atom_offset(prow, chunk16, KC)] = (uint8_t)sf;
-          }
-        }
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars->tmem_empty[buf]);
+      if (any && r < rows) {
+        float act[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const uint32_t g = i < 8 ? v0[2 * i] : v1[2 * i - 16], u = i < 8 ? v0[2 * i + 1] : v1[2 * i - 15];
+          act[i] = situ_f32(__fmul_rn(__uint_as_float(g), s13), __fmul_rn(__uint_as_float(u), s13), be, inv_be, la,
+                            inv_la);
+        }
+        uint2 packed;
+        const uint32_t sf = nvfp4_quant16(act, qa, packed);
+        const int64_t prow = row0 + r;
+        *reinterpret_cast<uint2*>(p.aq + (size_t)prow * I2 + it * 32 + grp * 8) = packed;
+        p.sfa[atom_offset(prow, it * 4 + grp, KC)] = (uint8_t)sf;
+      }
       ++local;
     }
   }
