@@ -443,7 +443,7 @@ moe_status_t moe_forward(const moe_shape_t* shape, int64_t num_tokens, const voi
   f1.E = s.E;
   f1.max_tiles = (int32_t)L.TTmax;
   f1.max_rows = L.PpadMax;
-  const int grid1 = (int)std::min<int64_t>(sms, tt * NIT);
+  const int grid1 = (int)std::min<int64_t>(sms, tt * (s.I / 128));
   prof_mark(2, stream);
   MOE_CUDA(launch_fc1(tm_w13, tm_xq, f1, grid1, stream));
 

@@ -3,13 +3,16 @@
 // FC1 ("Cake SiTU backend": FC1 over gate and up, SiTU, intermediate NVFP4
 // requantization): the MMA takes the routed tokens of one expert tile on its
 // M side (128 rows; a decode-sized group fills only the first rows, which
-// costs the tensor pipe no more than a narrow N would) and one prepared W13
+// costs the tensor pipe no more than a narrow N would) and a prepared W13
 // tile on its N side: 128 rows holding 64 intermediate features with gate and
-// up rows interleaved (row 2i = gate of feature i, row 2i+1 = up).  Per work
-// unit (token tile, 64 features) one accumulator [128 tokens x 128] collects
-// K = H over k-blocks of 256 FP4 elements; accumulators are double-buffered in
-// TMEM so the epilogue of one unit runs under the MMAs of the next.  In the
-// epilogue a thread owns one token row: it reads 16 features' gate/up pairs,
+// up rows interleaved (row 2i = gate of feature i, row 2i+1 = up).  A work
+// unit is one token tile and two such W13 tiles (128 features): per k-block of
+// 256 FP4 elements the X tile and its scale atoms serve both, so a k-block
+// costs 12 scale-atom copies to TMEM for 8 MMAs instead of 16, and 54 KB of
+// loads for two [128 x 128] products instead of 72.  The two accumulators
+// (256 TMEM columns) are single-buffered; the epilogue releases each as soon
+// as it has read it.  In the epilogue a thread owns one token row: it reads
+// 16 features' gate/up pairs,
 // forms z = acc * dX*dW13[e] and a = SiTU(z_g, z_u), and quantizes the 16
 // values with qA[e] in registers into the token's padded row of A (codes and
 // atom-layout scale) -- no cross-lane traffic.
@@ -41,13 +44,18 @@ cudaError_t launch_with_pdl(const void* fn, dim3 grid, dim3 block, size_t smem, 
 
 constexpr uint32_t kTmemCols = 512;
 
-// FC1 stage: A [128 interleaved gate/up rows x 128 B] | B [128 tokens x 128 B] |
-// SF A 4 atoms | SF B 4 atoms.
-constexpr int kFc1Stages = 6;
-constexpr int F1_A = 0, F1_B = 16384, F1_SA = 32768, F1_SB = 34816;
-constexpr int kFc1StageBytes = 36864;
+// FC1 stage: X [128 tokens x 128 B] | W0, W1 [128 interleaved gate/up rows x
+// 128 B] | X scale atoms | W0 scale atoms | W1 scale atoms (4 of 512 B each).
+constexpr int kFc1Stages = 4;
+constexpr int F1_X = 0, F1_W0 = 16384, F1_W1 = 32768, F1_SX = 49152, F1_SW0 = 51200, F1_SW1 = 53248;
+constexpr int kFc1StageBytes = 55296;
 constexpr int kFc1EpiWarps = 16;
-constexpr int kFc1Threads = 64 + 32 * kFc1EpiWarps;
+// FC1 warps: 2 TMA producer, 3 MMA issuer and TMEM owner, 4.. epilogue (0 and
+// 1 idle).  TMEM lane quarter q is read by warps w with w % 4 == q, which share
+// a scheduler; tiles fill the low quarters first, so the two issuing warps sit
+// on the schedulers of quarters 2 and 3.
+constexpr int kFc1Producer = 2, kFc1Mma = 3, kFc1Epi0 = 4;
+constexpr int kFc1Threads = 32 * (kFc1Epi0 + kFc1EpiWarps);
 // FC2 shared memory: barriers (1 KB) | two activation slots (a token tile's
 // A codes [I/128 k-blocks][128 rows x 64 B] + its I/64 scale atoms) | ring of
 // W2 stages (A [128 x 64 B] | SF 2 atoms); the stage count follows from I.
@@ -111,7 +119,7 @@ __device__ __forceinline__ uint8_t* aligned_smem(uint8_t* raw) {
 __device__ __forceinline__ uint64_t sf_desc(const uint8_t* p) { return smem_desc(smem_u32(p), 0, 128, kLayoutNone); }
 
 template <int STAGES, int EPI_WARPS>
-__device__ void gemm_setup(Barriers* bars, int warp) {
+__device__ void gemm_setup(Barriers* bars, int warp, int tmem_warp) {
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&bars->full[s], 1);
@@ -127,7 +135,7 @@ __device__ void gemm_setup(Barriers* bars, int warp) {
     bars->abort_flag = 0;
     fence_barrier_init();
   }
-  if (warp == 1) {
+  if (warp == tmem_warp) {
     tmem_alloc(&bars->tmem_base, kTmemCols);
     tmem_relinquish();
   }
@@ -186,6 +194,26 @@ __device__ __forceinline__ int fc2_group(int ntiles, int NMT, int npu, int grid)
   return G;
 }
 
+// nvfp4_quant16 over 16 activations held in the even slots of two
+// 16-register arrays (activation i in lo[2i] for i < 8, hi[2i-16] after).
+__device__ __forceinline__ uint32_t quant16_even(const uint32_t (&lo)[16], const uint32_t (&hi)[16], float q,
+                                                 uint2& packed) {
+  float amax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(lo[2 * i])), fabsf(__uint_as_float(hi[2 * i]))));
+  float r;
+  const uint32_t sf = nvfp4_scale(amax, q, r);
+  uint32_t w[2] = {0u, 0u};
+#pragma unroll
+  for (int m = 0; m < 8; ++m) {
+    const float a0 = __uint_as_float(m < 4 ? lo[4 * m] : hi[4 * m - 16]);
+    const float a1 = __uint_as_float(m < 4 ? lo[4 * m + 2] : hi[4 * m - 14]);
+    w[m >> 2] |= cvt_e2m1x2(__fmul_rn(a1, r), __fmul_rn(a0, r)) << (8 * (m & 3));
+  }
+  packed = make_uint2(w[0], w[1]);
+  return sf;
+}
+
 // ================================================================== FC1
 __global__ void __launch_bounds__(kFc1Threads, 1)
     fc1_kernel(const __grid_constant__ CUtensorMap tm_w13, const __grid_constant__ RowMaps tm_xq,
@@ -194,37 +222,39 @@ __global__ void __launch_bounds__(kFc1Threads, 1)
   uint8_t* smem = aligned_smem(smem_raw);
   Barriers* bars = reinterpret_cast<Barriers*>(smem + kFc1Stages * kFc1StageBytes);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int NIT = p.I / 64, NKB = p.H / kFc1KBlock;
-  if (warp == 0 && lane == 0) {
+  const int NIT = p.I / 64, NP = p.I / 128, NKB = p.H / kFc1KBlock;
+  if (warp == kFc1Producer && lane == 0) {
     tma_prefetch_desc(&tm_w13);
     tma_prefetch_desc(&tm_xq.m16);
     tma_prefetch_desc(&tm_xq.m128);
   }
-  gemm_setup<kFc1Stages, kFc1EpiWarps>(bars, warp);
+  gemm_setup<kFc1Stages, kFc1EpiWarps>(bars, warp, kFc1Mma);
   const uint32_t tmem = bars->tmem_base;
   pdl_wait();
   pdl_launch_dependents();
-  const int num_units = clamp_tiles(p.hdr[HDR_NUM_TT], p.max_tiles) * NIT;
+  const int num_units = clamp_tiles(p.hdr[HDR_NUM_TT], p.max_tiles) * NP;   // (token tile, W13 tile pair)
   const int4* tiles = reinterpret_cast<const int4*>(p.tt_list);
 
-  if (warp == 0) {
+  if (warp < kFc1Producer) {
+    // idle
+  } else if (warp == kFc1Producer) {
     if (lane == 0) {
       // ---------------------------------------------------------- producer
       uint32_t stage = 0, phase = 0;
       uint32_t armed = 0, last_phase = 0;  // bit s: stage s armed; its last armed phase
       bool ok = true;
-      int4 nxt = next_tile(tiles, blockIdx.x, num_units, NIT);
+      int4 nxt = next_tile(tiles, blockIdx.x, num_units, NP);
       for (int unit = blockIdx.x; unit < num_units && ok; unit += gridDim.x) {
         const int4 tl = nxt;
-        nxt = next_tile(tiles, unit + gridDim.x, num_units, NIT);   // in flight while this unit streams
-        const int it = unit % NIT;
+        nxt = next_tile(tiles, unit + gridDim.x, num_units, NP);   // in flight while this unit streams
         if (!tile_ok(tl, p.E, p.max_rows)) {
           set_status(p.status, DEVSTAT_BAD_TILE);
           continue;
         }
         const int e = tl.x, row0 = tl.y, rows = tl.z;
+        const int w0 = (e * NIT + 2 * (unit % NP)) * NKB;   // first W13 tile of the pair; the second is NKB later
         const int nch = (rows + kTokChunk - 1) / kTokChunk;
-        const uint32_t tx = 16384u + (uint32_t)nch * 2048u + 2048u + 2048u;
+        const uint32_t tx = (uint32_t)nch * 2048u + 2u * 16384u + 3u * 2048u;
         for (int kb = 0; kb < NKB; ++kb) {
           if (!wait_or_abort(&bars->empty[stage], phase ^ 1u, bars, p.status)) {
             ok = false;
@@ -234,11 +264,13 @@ __global__ void __launch_bounds__(kFc1Threads, 1)
           mbar_arrive_expect_tx(&bars->full[stage], tx);
           armed |= 1u << stage;
           last_phase = (last_phase & ~(1u << stage)) | (phase << stage);
-          tma_load_3d(st + F1_A, &tm_w13, 0, 0, (e * NIT + it) * NKB + kb, &bars->full[stage]);
-          load_rows(st + F1_B, tm_xq, kb * 128, row0, nch, 2048u, &bars->full[stage]);
-          bulk_g2s(st + F1_SA, p.sf13p + (size_t)((e * NIT + it) * NKB + kb) * 2048u, 2048u, &bars->full[stage]);
-          bulk_g2s(st + F1_SB, p.sfx + ((size_t)(row0 >> 7) * (p.H / 64) + (size_t)kb * 4) * 512u, 2048u,
+          load_rows(st + F1_X, tm_xq, kb * 128, row0, nch, 2048u, &bars->full[stage]);
+          tma_load_3d(st + F1_W0, &tm_w13, 0, 0, w0 + kb, &bars->full[stage]);
+          tma_load_3d(st + F1_W1, &tm_w13, 0, 0, w0 + NKB + kb, &bars->full[stage]);
+          bulk_g2s(st + F1_SX, p.sfx + ((size_t)(row0 >> 7) * (p.H / 64) + (size_t)kb * 4) * 512u, 2048u,
                    &bars->full[stage]);
+          bulk_g2s(st + F1_SW0, p.sf13p + (size_t)(w0 + kb) * 2048u, 2048u, &bars->full[stage]);
+          bulk_g2s(st + F1_SW1, p.sf13p + (size_t)(w0 + NKB + kb) * 2048u, 2048u, &bars->full[stage]);
           if (++stage == kFc1Stages) {
             stage = 0;
             phase ^= 1u;
@@ -249,40 +281,50 @@ __global__ void __launch_bounds__(kFc1Threads, 1)
       for (int s = 0; s < kFc1Stages; ++s)
         if (armed & (1u << s)) mbar_wait(&bars->full[s], (last_phase >> s) & 1u, p.status);
     }
-  } else if (warp == 1) {
+  } else if (warp == kFc1Mma) {
     if (lane == 0) {
       // --------------------------------------------------------------- MMA
+      // TMEM: accumulators of the pair at columns 0 and 128; the scale atoms
+      // of stage s at 256 + 48 s (X, W0, W1: 16 columns each).
       uint32_t stage = 0, phase = 0;
       int local = 0;
       bool ok = true;
-      int4 nxt = next_tile(tiles, blockIdx.x, num_units, NIT);
+      const uint32_t idesc = idesc_mxf4nvf4(128, 128);
+      int4 nxt = next_tile(tiles, blockIdx.x, num_units, NP);
       for (int unit = blockIdx.x; unit < num_units && ok; unit += gridDim.x) {
         const int4 tl = nxt;
-        nxt = next_tile(tiles, unit + gridDim.x, num_units, NIT);
+        nxt = next_tile(tiles, unit + gridDim.x, num_units, NP);
         if (!tile_ok(tl, p.E, p.max_rows)) continue;
-        const uint32_t idesc = idesc_mxf4nvf4(128, 128);
-        const uint32_t buf = (uint32_t)local & 1u;
-        if (!wait_or_abort(&bars->tmem_empty[buf], (((uint32_t)local >> 1) & 1u) ^ 1u, bars, p.status)) break;
-        tc_fence_after();
-        const uint32_t dcol = tmem + buf * 128;
+        const uint32_t par = ((uint32_t)local & 1u) ^ 1u;
         for (int kb = 0; kb < NKB; ++kb) {
           if (!wait_or_abort(&bars->full[stage], phase, bars, p.status)) {
             ok = false;
             break;
           }
+          if (kb == 0) {   // both accumulators drained by the previous unit's epilogue
+            if (!wait_or_abort(&bars->tmem_empty[0], par, bars, p.status) ||
+                !wait_or_abort(&bars->tmem_empty[1], par, bars, p.status)) {
+              ok = false;
+              break;
+            }
+          }
           tc_fence_after();
           const uint8_t* st = smem + stage * kFc1StageBytes;
-          const uint32_t sfc = tmem + 256 + stage * 32;
+          const uint32_t sfc = tmem + 256 + stage * 48;
 #pragma unroll
           for (int a = 0; a < 4; ++a) {
-            tmem_cp_32x128b_x4(sfc + a * 4, sf_desc(st + F1_SA + a * 512));
-            tmem_cp_32x128b_x4(sfc + 16 + a * 4, sf_desc(st + F1_SB + a * 512));
+            tmem_cp_32x128b_x4(sfc + a * 4, sf_desc(st + F1_SX + a * 512));
+            tmem_cp_32x128b_x4(sfc + 16 + a * 4, sf_desc(st + F1_SW0 + a * 512));
+            tmem_cp_32x128b_x4(sfc + 32 + a * 4, sf_desc(st + F1_SW1 + a * 512));
           }
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks) {   // M = tokens (X tile), N = W13 rows
-            const uint64_t xd = smem_desc(smem_u32(st + F1_B) + ks * 32, 16, 1024, kLayoutSW128);
-            const uint64_t wd = smem_desc(smem_u32(st + F1_A) + ks * 32, 16, 1024, kLayoutSW128);
-            mma_mxf4nvf4(dcol, xd, wd, idesc, sfc + 16 + ks * 4, sfc + ks * 4, (kb | ks) ? 1u : 0u);
+            const uint64_t xd = smem_desc(smem_u32(st + F1_X) + ks * 32, 16, 1024, kLayoutSW128);
+            const uint64_t wd0 = smem_desc(smem_u32(st + F1_W0) + ks * 32, 16, 1024, kLayoutSW128);
+            const uint64_t wd1 = smem_desc(smem_u32(st + F1_W1) + ks * 32, 16, 1024, kLayoutSW128);
+            const uint32_t acc = (kb | ks) ? 1u : 0u;
+            mma_mxf4nvf4(tmem, xd, wd0, idesc, sfc + ks * 4, sfc + 16 + ks * 4, acc);
+            mma_mxf4nvf4(tmem + 128, xd, wd1, idesc, sfc + ks * 4, sfc + 32 + ks * 4, acc);
           }
           tc_commit(&bars->empty[stage]);
           if (++stage == kFc1Stages) {
@@ -290,7 +332,7 @@ __global__ void __launch_bounds__(kFc1Threads, 1)
             phase ^= 1u;
           }
         }
-        if (ok) tc_commit(&bars->tmem_full[buf]);
+        if (ok) tc_commit(&bars->tmem_full[0]);
         ++local;
       }
       tc_commit(&bars->drain);
@@ -298,54 +340,62 @@ __global__ void __launch_bounds__(kFc1Threads, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    // Warp w drains TMEM lanes 32*(w%4).. (its tokens) and the 32 accumulator
-    // columns of 16 features: group (w-2)/4 of the unit's 64.
-    const int q = warp & 3, grp = (warp - 2) >> 2;
+    // Warp w drains TMEM lanes 32*(w%4).. (its tokens); in each of the pair's
+    // two accumulators, the 32 columns of 16 features: group (w-4)/4 of 4.
+    const int q = warp & 3, grp = (warp - kFc1Epi0) >> 2;
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
     const int I2 = p.I / 2, KC = p.I / 16;
     const int r = q * 32 + lane;                      // token row within the tile
     int local = 0;
-    int4 nxt = next_tile(tiles, blockIdx.x, num_units, NIT);
+    int4 nxt = next_tile(tiles, blockIdx.x, num_units, NP);
     float4 sc_nxt = unit_scalars(p, nxt);
-    int4 nxt2 = next_tile(tiles, blockIdx.x + gridDim.x, num_units, NIT);
+    int4 nxt2 = next_tile(tiles, blockIdx.x + gridDim.x, num_units, NP);
     for (int unit = blockIdx.x; unit < num_units; unit += gridDim.x) {
       const int4 tl = nxt;
       const float4 sc = sc_nxt;
       nxt = nxt2;
-      sc_nxt = unit_scalars(p, nxt);                                   // one unit ahead
-      nxt2 = next_tile(tiles, unit + 2 * gridDim.x, num_units, NIT);  // two units ahead
+      sc_nxt = unit_scalars(p, nxt);                                  // one unit ahead
+      nxt2 = next_tile(tiles, unit + 2 * gridDim.x, num_units, NP);  // two units ahead
       if (!tile_ok(tl, p.E, p.max_rows)) continue;
-      const int it = unit % NIT;
       const int row0 = tl.y, rows = tl.z;
-      const uint32_t buf = (uint32_t)local & 1u;
-      if (!wait_or_abort(&bars->tmem_full[buf], ((uint32_t)local >> 1) & 1u, bars, p.status)) break;
+      if (!wait_or_abort(&bars->tmem_full[0], (uint32_t)local & 1u, bars, p.status)) break;
       tc_fence_after();
       const float s13 = sc.x, qa = sc.y, be = sc.z, la = sc.w;
       const float inv_be = 1.0f / be, inv_la = 1.0f / la;
-      // columns 2i / 2i+1 = gate / up of feature it*64 + 16*grp + i
-      uint32_t v0[16], v1[16];
-      const bool any = q * 32 < rows;                  // warp-uniform: this quarter holds tokens
+      const bool any = q * 32 < rows;                 // warp-uniform: this quarter holds tokens
+      const int64_t prow = row0 + r;
+      // read both accumulators, release them, then compute: the MMA of the next unit can start
+      // columns 2i / 2i+1 = gate / up of feature (2*pair + b)*64 + 16*grp + i
+      uint32_t v[2][2][16];
       if (any) {
-        tmem_ld16(tmem + lane_base + buf * 128 + grp * 32, v0);
-        tmem_ld16(tmem + lane_base + buf * 128 + grp * 32 + 16, v1);
+#pragma unroll
+        for (int b = 0; b < 2; ++b) {
+          tmem_ld16(tmem + lane_base + b * 128 + grp * 32, v[b][0]);
+          tmem_ld16(tmem + lane_base + b * 128 + grp * 32 + 16, v[b][1]);
+        }
         tmem_ld_wait();
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->tmem_empty[buf]);
+      if (lane == 0) {
+        mbar_arrive(&bars->tmem_empty[0]);
+        mbar_arrive(&bars->tmem_empty[1]);
+      }
       if (any && r < rows) {
-        float act[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const uint32_t g = i < 8 ? v0[2 * i] : v1[2 * i - 16], u = i < 8 ? v0[2 * i + 1] : v1[2 * i - 15];
-          act[i] = situ_f32(__fmul_rn(__uint_as_float(g), s13), __fmul_rn(__uint_as_float(u), s13), be, inv_be, la,
-                            inv_la);
+        for (int b = 0; b < 2; ++b) {
+          // SiTU in place: activation i overwrites the gate value it was computed from
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            v[b][i >> 3][(2 * i) & 15] = __float_as_uint(
+                situ_f32(__fmul_rn(__uint_as_float(v[b][i >> 3][(2 * i) & 15]), s13),
+                         __fmul_rn(__uint_as_float(v[b][i >> 3][(2 * i + 1) & 15]), s13), be, inv_be, la, inv_la));
+          uint2 packed;
+          const uint32_t sf = quant16_even(v[b][0], v[b][1], qa, packed);
+          const int it = 2 * (unit % NP) + b;
+          *reinterpret_cast<uint2*>(p.aq + (size_t)prow * I2 + it * 32 + grp * 8) = packed;
+          p.sfa[atom_offset(prow, it * 4 + grp, KC)] = (uint8_t)sf;
         }
-        uint2 packed;
-        const uint32_t sf = nvfp4_quant16(act, qa, packed);
-        const int64_t prow = row0 + r;
-        *reinterpret_cast<uint2*>(p.aq + (size_t)prow * I2 + it * 32 + grp * 8) = packed;
-        p.sfa[atom_offset(prow, it * 4 + grp, KC)] = (uint8_t)sf;
       }
       ++local;
     }
@@ -353,7 +403,7 @@ __global__ void __launch_bounds__(kFc1Threads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+  if (warp == kFc1Mma) tmem_dealloc(tmem, kTmemCols);
 }
 
 // ================================================================== FC2
@@ -374,7 +424,7 @@ __global__ void __launch_bounds__(kFc2Threads, 1)
     tma_prefetch_desc(&tm_aq.m16);
     tma_prefetch_desc(&tm_aq.m128);
   }
-  gemm_setup<kMaxStages, kFc2EpiWarps>(bars, warp);
+  gemm_setup<kMaxStages, kFc2EpiWarps>(bars, warp, 1);
   const uint32_t tmem = bars->tmem_base;
   pdl_wait();
   pdl_launch_dependents();
