@@ -31,7 +31,8 @@ cudaError_t launch_situ_requant(const float* z, int64_t rows, int I, float qA, f
 cudaError_t launch_requant_lanes(const float* act, int64_t rows, int I, float qA, uint8_t* packed, uint8_t* sf,
                                  cudaStream_t st);
 cudaError_t gemm_set_attributes();
-cudaError_t launch_fc1(const CUtensorMap& w13, const RowMaps& xq, const Fc1Args& a, int grid, cudaStream_t st);
+cudaError_t launch_fc1(const CUtensorMap& w13, const RowMaps& xq, const Fc1Args& a, int pair, int grid,
+                       cudaStream_t st);
 cudaError_t launch_fc2(const CUtensorMap& w2, const RowMaps& aq, const Fc2Args& a, int grid, cudaStream_t st);
 cudaError_t launch_mma_check(const CUtensorMap& a, const CUtensorMap& b, const uint8_t* sfa, const uint8_t* sfb,
                              int N, int K, float* d, int32_t* status, cudaStream_t st);
@@ -222,6 +223,19 @@ static RouteArgs route_args(const Shape& s, const WsLayout& L, uint8_t* ws, cons
 // Above this many routed pairs the X block scales are written token-major
 // and laid out in atoms by a second kernel.
 constexpr int64_t kSfTwoPassMin = 65536;
+// Largest batch for which FC1 works on one W13 tile per unit.
+constexpr int64_t kFc1SingleMaxTokens = 16;
+
+// W13 tiles per FC1 work unit: two (shared X loads and scale copies) unless
+// the batch is so small that single tiles are needed to keep the SMs busy
+// (NVFP4MOE_FC1_PAIR=1/2 overrides).
+static int fc1_pair(const Shape& s, int64_t T) {
+  if (const char* v = std::getenv("NVFP4MOE_FC1_PAIR")) {
+    if (v[0] == '1') return 1;
+    if (v[0] == '2') return 2;
+  }
+  return T <= kFc1SingleMaxTokens ? 1 : 2;
+}
 
 static int forward_launches(int64_t P) { return (P <= kRouteSmallMax ? 1 : 2) + 4 + (P > kSfTwoPassMin ? 1 : 0); }
 
@@ -443,9 +457,10 @@ moe_status_t moe_forward(const moe_shape_t* shape, int64_t num_tokens, const voi
   f1.E = s.E;
   f1.max_tiles = (int32_t)L.TTmax;
   f1.max_rows = L.PpadMax;
-  const int grid1 = (int)std::min<int64_t>(sms, tt * (s.I / 128));
+  const int pair = fc1_pair(s, T);
+  const int grid1 = (int)std::min<int64_t>(sms, tt * (s.I / 64 / pair));
   prof_mark(2, stream);
-  MOE_CUDA(launch_fc1(tm_w13, tm_xq, f1, grid1, stream));
+  MOE_CUDA(launch_fc1(tm_w13, tm_xq, f1, pair, grid1, stream));
 
   // 4. FC2 with the route-weighted combine into the fp32 accumulator
   Fc2Args f2{};

@@ -44,11 +44,23 @@ cudaError_t launch_with_pdl(const void* fn, dim3 grid, dim3 block, size_t smem, 
 
 constexpr uint32_t kTmemCols = 512;
 
-// FC1 stage: X [128 tokens x 128 B] | W0, W1 [128 interleaved gate/up rows x
-// 128 B] | X scale atoms | W0 scale atoms | W1 scale atoms (4 of 512 B each).
-constexpr int kFc1Stages = 4;
-constexpr int F1_X = 0, F1_W0 = 16384, F1_W1 = 32768, F1_SX = 49152, F1_SW0 = 51200, F1_SW1 = 53248;
-constexpr int kFc1StageBytes = 55296;
+// FC1 stage: X [128 tokens x 128 B] | W [PAIR tiles of 128 interleaved
+// gate/up rows x 128 B] | X scale atoms | W scale atoms (4 of 512 B per tile).
+// PAIR = 2 shares the X tile and its atoms between two W13 tiles (single-
+// buffered accumulators); PAIR = 1 keeps double-buffered accumulators and a
+// deeper ring, better when few units would leave SMs idle.
+template <int PAIR>
+struct Fc1Cfg {
+  static constexpr int kStage = 16384 * (1 + PAIR) + 2048 * (1 + PAIR);
+  static constexpr int kStages = 221184 / kStage;            // 6 or 4
+  static constexpr int kX = 0, kW = 16384, kSX = 16384 * (1 + PAIR), kSW = kSX + 2048;
+  static constexpr int kBufs = PAIR == 1 ? 2 : 1;            // accumulator buffers of PAIR x 128 columns
+  static constexpr int kSfCols = 16 * (1 + PAIR);            // TMEM scale columns per stage
+  static constexpr size_t kSmem = (size_t)kStages * kStage + 1024 + 1024;
+};
+static_assert(Fc1Cfg<1>::kBufs * 128 + Fc1Cfg<1>::kStages * Fc1Cfg<1>::kSfCols <= 512 &&
+                  Fc1Cfg<2>::kBufs * 256 + Fc1Cfg<2>::kStages * Fc1Cfg<2>::kSfCols <= 512,
+              "FC1 TMEM plan");
 constexpr int kFc1EpiWarps = 16;
 // FC1 warps: 2 TMA producer, 3 MMA issuer and TMEM owner, 4.. epilogue (0 and
 // 1 idle).  TMEM lane quarter q is read by warps w with w % 4 == q, which share
@@ -67,11 +79,13 @@ constexpr int kFc2Threads = 64 + 32 * kFc2EpiWarps;
 constexpr int kFc2MaxI = 512;
 constexpr uint32_t kFc2SfbCol = 448;   // TMEM column of the activation slots' scale factors
 
+constexpr int kMaxAccSlots = 16;
+
 struct Barriers {
   uint64_t full[kMaxStages];
   uint64_t empty[kMaxStages];
-  uint64_t tmem_full[2];
-  uint64_t tmem_empty[2];
+  uint64_t tmem_full[kMaxAccSlots];
+  uint64_t tmem_empty[kMaxAccSlots];
   uint64_t act_full[2];
   uint64_t act_empty[2];
   uint64_t drain;
@@ -80,7 +94,6 @@ struct Barriers {
 };
 static_assert(sizeof(Barriers) <= 1024, "barrier block");
 
-constexpr size_t kFc1Smem = (size_t)kFc1Stages * kFc1StageBytes + sizeof(Barriers) + 1024;
 constexpr size_t kFc2Smem = 232448;    // the opt-in maximum; carved up at run time
 
 __host__ __device__ constexpr int fc2_act_bytes(int I) { return (128 * (I / 2) + (I / 64) * 512 + 1023) / 1024 * 1024; }
@@ -125,9 +138,11 @@ __device__ void gemm_setup(Barriers* bars, int warp, int tmem_warp) {
       mbar_init(&bars->full[s], 1);
       mbar_init(&bars->empty[s], 1);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < kMaxAccSlots; ++b) {
       mbar_init(&bars->tmem_full[b], 1);
       mbar_init(&bars->tmem_empty[b], EPI_WARPS);
+    }
+    for (int b = 0; b < 2; ++b) {
       mbar_init(&bars->act_full[b], 1);
       mbar_init(&bars->act_empty[b], 1);
     }
@@ -181,17 +196,24 @@ __device__ __forceinline__ int4 fc2_next_tile(const int4* tiles, int unit, int n
   return unit < num_units ? tiles[unit % ntiles] : make_int4(-1, 0, 0, 0);
 }
 
-// Feature tiles per FC2 unit: the largest divisor of the pass width npu that
-// still leaves 8 units per CTA, so that an activation tile is loaded once per
-// group while every SM stays busy.
+// Feature tiles per FC2 unit: the divisor G of the pass width npu that
+// minimizes the busiest CTA's work, ceil(units / grid) * (G + 2), where each
+// unit streams G W2 tiles and costs about two more in activation loads and
+// hand-over.  Small batches get long units (few tiles, overhead dominates);
+// large batches short ones.
 __device__ __forceinline__ int fc2_group(int ntiles, int NMT, int npu, int grid) {
-  int G = npu;
-  while (G > 1 && (int64_t)ntiles * (NMT / G) < 8LL * grid) {
-    do {
-      --G;
-    } while (npu % G);
+  int best = 1;
+  int64_t best_cost = -1;
+  for (int G = 1; G <= npu; ++G) {
+    if (npu % G) continue;
+    const int64_t units = (int64_t)ntiles * (NMT / G);
+    const int64_t cost = (units + grid - 1) / grid * (G + 2);
+    if (best_cost < 0 || cost < best_cost) {
+      best_cost = cost;
+      best = G;
+    }
   }
-  return G;
+  return best;
 }
 
 // nvfp4_quant16 over 16 activations held in the even slots of two
@@ -215,24 +237,26 @@ __device__ __forceinline__ uint32_t quant16_even(const uint32_t (&lo)[16], const
 }
 
 // ================================================================== FC1
+template <int PAIR>
 __global__ void __launch_bounds__(kFc1Threads, 1)
     fc1_kernel(const __grid_constant__ CUtensorMap tm_w13, const __grid_constant__ RowMaps tm_xq,
                const Fc1Args p) {
+  using C = Fc1Cfg<PAIR>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = aligned_smem(smem_raw);
-  Barriers* bars = reinterpret_cast<Barriers*>(smem + kFc1Stages * kFc1StageBytes);
+  Barriers* bars = reinterpret_cast<Barriers*>(smem + C::kStages * C::kStage);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int NIT = p.I / 64, NP = p.I / 128, NKB = p.H / kFc1KBlock;
+  const int NIT = p.I / 64, NP = NIT / PAIR, NKB = p.H / kFc1KBlock;
   if (warp == kFc1Producer && lane == 0) {
     tma_prefetch_desc(&tm_w13);
     tma_prefetch_desc(&tm_xq.m16);
     tma_prefetch_desc(&tm_xq.m128);
   }
-  gemm_setup<kFc1Stages, kFc1EpiWarps>(bars, warp, kFc1Mma);
+  gemm_setup<C::kStages, kFc1EpiWarps>(bars, warp, kFc1Mma);
   const uint32_t tmem = bars->tmem_base;
   pdl_wait();
   pdl_launch_dependents();
-  const int num_units = clamp_tiles(p.hdr[HDR_NUM_TT], p.max_tiles) * NP;   // (token tile, W13 tile pair)
+  const int num_units = clamp_tiles(p.hdr[HDR_NUM_TT], p.max_tiles) * NP;   // (token tile, PAIR W13 tiles)
   const int4* tiles = reinterpret_cast<const int4*>(p.tt_list);
 
   if (warp < kFc1Producer) {
@@ -252,40 +276,42 @@ __global__ void __launch_bounds__(kFc1Threads, 1)
           continue;
         }
         const int e = tl.x, row0 = tl.y, rows = tl.z;
-        const int w0 = (e * NIT + 2 * (unit % NP)) * NKB;   // first W13 tile of the pair; the second is NKB later
+        const int w0 = (e * NIT + PAIR * (unit % NP)) * NKB;   // first W13 tile; the next is NKB later
         const int nch = (rows + kTokChunk - 1) / kTokChunk;
-        const uint32_t tx = (uint32_t)nch * 2048u + 2u * 16384u + 3u * 2048u;
+        const uint32_t tx = (uint32_t)nch * 2048u + (uint32_t)PAIR * 16384u + (1u + PAIR) * 2048u;
         for (int kb = 0; kb < NKB; ++kb) {
           if (!wait_or_abort(&bars->empty[stage], phase ^ 1u, bars, p.status)) {
             ok = false;
             break;
           }
-          uint8_t* st = smem + stage * kFc1StageBytes;
+          uint8_t* st = smem + stage * C::kStage;
           mbar_arrive_expect_tx(&bars->full[stage], tx);
           armed |= 1u << stage;
           last_phase = (last_phase & ~(1u << stage)) | (phase << stage);
-          load_rows(st + F1_X, tm_xq, kb * 128, row0, nch, 2048u, &bars->full[stage]);
-          tma_load_3d(st + F1_W0, &tm_w13, 0, 0, w0 + kb, &bars->full[stage]);
-          tma_load_3d(st + F1_W1, &tm_w13, 0, 0, w0 + NKB + kb, &bars->full[stage]);
-          bulk_g2s(st + F1_SX, p.sfx + ((size_t)(row0 >> 7) * (p.H / 64) + (size_t)kb * 4) * 512u, 2048u,
+          load_rows(st + C::kX, tm_xq, kb * 128, row0, nch, 2048u, &bars->full[stage]);
+          bulk_g2s(st + C::kSX, p.sfx + ((size_t)(row0 >> 7) * (p.H / 64) + (size_t)kb * 4) * 512u, 2048u,
                    &bars->full[stage]);
-          bulk_g2s(st + F1_SW0, p.sf13p + (size_t)(w0 + kb) * 2048u, 2048u, &bars->full[stage]);
-          bulk_g2s(st + F1_SW1, p.sf13p + (size_t)(w0 + NKB + kb) * 2048u, 2048u, &bars->full[stage]);
-          if (++stage == kFc1Stages) {
+#pragma unroll
+          for (int j = 0; j < PAIR; ++j) {
+            tma_load_3d(st + C::kW + j * 16384, &tm_w13, 0, 0, w0 + j * NKB + kb, &bars->full[stage]);
+            bulk_g2s(st + C::kSW + j * 2048, p.sf13p + (size_t)(w0 + j * NKB + kb) * 2048u, 2048u, &bars->full[stage]);
+          }
+          if (++stage == C::kStages) {
             stage = 0;
             phase ^= 1u;
           }
         }
       }
       // every issued copy has landed before the CTA may exit
-      for (int s = 0; s < kFc1Stages; ++s)
+      for (int s = 0; s < C::kStages; ++s)
         if (armed & (1u << s)) mbar_wait(&bars->full[s], (last_phase >> s) & 1u, p.status);
     }
   } else if (warp == kFc1Mma) {
     if (lane == 0) {
       // --------------------------------------------------------------- MMA
-      // TMEM: accumulators of the pair at columns 0 and 128; the scale atoms
-      // of stage s at 256 + 48 s (X, W0, W1: 16 columns each).
+      // TMEM: accumulator buffer b holds the unit's PAIR blocks at columns
+      // (b*PAIR + j)*128; the scale atoms of stage s at 256 + kSfCols*s (X, then
+      // each W tile: 16 columns each).
       uint32_t stage = 0, phase = 0;
       int local = 0;
       bool ok = true;
@@ -295,44 +321,46 @@ __global__ void __launch_bounds__(kFc1Threads, 1)
         const int4 tl = nxt;
         nxt = next_tile(tiles, unit + gridDim.x, num_units, NP);
         if (!tile_ok(tl, p.E, p.max_rows)) continue;
-        const uint32_t par = ((uint32_t)local & 1u) ^ 1u;
+        const uint32_t buf = (uint32_t)local % C::kBufs, par = (((uint32_t)local / C::kBufs) & 1u) ^ 1u;
+        const uint32_t dcol = tmem + buf * PAIR * 128;
         for (int kb = 0; kb < NKB; ++kb) {
           if (!wait_or_abort(&bars->full[stage], phase, bars, p.status)) {
             ok = false;
             break;
           }
-          if (kb == 0) {   // both accumulators drained by the previous unit's epilogue
-            if (!wait_or_abort(&bars->tmem_empty[0], par, bars, p.status) ||
-                !wait_or_abort(&bars->tmem_empty[1], par, bars, p.status)) {
-              ok = false;
-              break;
-            }
+          if (kb == 0) {   // the buffer's blocks drained by the epilogue of its previous unit
+#pragma unroll
+            for (int j = 0; j < PAIR; ++j)
+              if (!wait_or_abort(&bars->tmem_empty[buf * PAIR + j], par, bars, p.status)) ok = false;
+            if (!ok) break;
           }
           tc_fence_after();
-          const uint8_t* st = smem + stage * kFc1StageBytes;
-          const uint32_t sfc = tmem + 256 + stage * 48;
+          const uint8_t* st = smem + stage * C::kStage;
+          const uint32_t sfc = tmem + 256 + stage * C::kSfCols;
 #pragma unroll
           for (int a = 0; a < 4; ++a) {
-            tmem_cp_32x128b_x4(sfc + a * 4, sf_desc(st + F1_SX + a * 512));
-            tmem_cp_32x128b_x4(sfc + 16 + a * 4, sf_desc(st + F1_SW0 + a * 512));
-            tmem_cp_32x128b_x4(sfc + 32 + a * 4, sf_desc(st + F1_SW1 + a * 512));
+            tmem_cp_32x128b_x4(sfc + a * 4, sf_desc(st + C::kSX + a * 512));
+#pragma unroll
+            for (int j = 0; j < PAIR; ++j)
+              tmem_cp_32x128b_x4(sfc + 16 * (1 + j) + a * 4, sf_desc(st + C::kSW + j * 2048 + a * 512));
           }
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks) {   // M = tokens (X tile), N = W13 rows
-            const uint64_t xd = smem_desc(smem_u32(st + F1_X) + ks * 32, 16, 1024, kLayoutSW128);
-            const uint64_t wd0 = smem_desc(smem_u32(st + F1_W0) + ks * 32, 16, 1024, kLayoutSW128);
-            const uint64_t wd1 = smem_desc(smem_u32(st + F1_W1) + ks * 32, 16, 1024, kLayoutSW128);
+            const uint64_t xd = smem_desc(smem_u32(st + C::kX) + ks * 32, 16, 1024, kLayoutSW128);
             const uint32_t acc = (kb | ks) ? 1u : 0u;
-            mma_mxf4nvf4(tmem, xd, wd0, idesc, sfc + ks * 4, sfc + 16 + ks * 4, acc);
-            mma_mxf4nvf4(tmem + 128, xd, wd1, idesc, sfc + ks * 4, sfc + 32 + ks * 4, acc);
+#pragma unroll
+            for (int j = 0; j < PAIR; ++j) {
+              const uint64_t wd = smem_desc(smem_u32(st + C::kW + j * 16384) + ks * 32, 16, 1024, kLayoutSW128);
+              mma_mxf4nvf4(dcol + j * 128, xd, wd, idesc, sfc + ks * 4, sfc + 16 * (1 + j) + ks * 4, acc);
+            }
           }
           tc_commit(&bars->empty[stage]);
-          if (++stage == kFc1Stages) {
+          if (++stage == C::kStages) {
             stage = 0;
             phase ^= 1u;
           }
         }
-        if (ok) tc_commit(&bars->tmem_full[0]);
+        if (ok) tc_commit(&bars->tmem_full[buf]);
         ++local;
       }
       tc_commit(&bars->drain);
@@ -358,32 +386,34 @@ __global__ void __launch_bounds__(kFc1Threads, 1)
       nxt2 = next_tile(tiles, unit + 2 * gridDim.x, num_units, NP);  // two units ahead
       if (!tile_ok(tl, p.E, p.max_rows)) continue;
       const int row0 = tl.y, rows = tl.z;
-      if (!wait_or_abort(&bars->tmem_full[0], (uint32_t)local & 1u, bars, p.status)) break;
+      const uint32_t buf = (uint32_t)local % C::kBufs;
+      if (!wait_or_abort(&bars->tmem_full[buf], ((uint32_t)local / C::kBufs) & 1u, bars, p.status)) break;
       tc_fence_after();
       const float s13 = sc.x, qa = sc.y, be = sc.z, la = sc.w;
       const float inv_be = 1.0f / be, inv_la = 1.0f / la;
       const bool any = q * 32 < rows;                 // warp-uniform: this quarter holds tokens
       const int64_t prow = row0 + r;
-      // read both accumulators, release them, then compute: the MMA of the next unit can start
-      // columns 2i / 2i+1 = gate / up of feature (2*pair + b)*64 + 16*grp + i
-      uint32_t v[2][2][16];
+      // read the unit's accumulators, release them, then compute: the MMA of a
+      // later unit can start.  Columns 2i / 2i+1 = gate / up of feature
+      // (PAIR*u + b)*64 + 16*grp + i.
+      uint32_t v[PAIR][2][16];
       if (any) {
 #pragma unroll
-        for (int b = 0; b < 2; ++b) {
-          tmem_ld16(tmem + lane_base + b * 128 + grp * 32, v[b][0]);
-          tmem_ld16(tmem + lane_base + b * 128 + grp * 32 + 16, v[b][1]);
+        for (int b = 0; b < PAIR; ++b) {
+          tmem_ld16(tmem + lane_base + (buf * PAIR + b) * 128 + grp * 32, v[b][0]);
+          tmem_ld16(tmem + lane_base + (buf * PAIR + b) * 128 + grp * 32 + 16, v[b][1]);
         }
         tmem_ld_wait();
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
-        mbar_arrive(&bars->tmem_empty[0]);
-        mbar_arrive(&bars->tmem_empty[1]);
+#pragma unroll
+        for (int b = 0; b < PAIR; ++b) mbar_arrive(&bars->tmem_empty[buf * PAIR + b]);
       }
       if (any && r < rows) {
 #pragma unroll
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < PAIR; ++b) {
           // SiTU in place: activation i overwrites the gate value it was computed from
 #pragma unroll
           for (int i = 0; i < 16; ++i)
@@ -392,7 +422,7 @@ __global__ void __launch_bounds__(kFc1Threads, 1)
                          __fmul_rn(__uint_as_float(v[b][i >> 3][(2 * i + 1) & 15]), s13), be, inv_be, la, inv_la));
           uint2 packed;
           const uint32_t sf = quant16_even(v[b][0], v[b][1], qa, packed);
-          const int it = 2 * (unit % NP) + b;
+          const int it = PAIR * (unit % NP) + b;
           *reinterpret_cast<uint2*>(p.aq + (size_t)prow * I2 + it * 32 + grp * 8) = packed;
           p.sfa[atom_offset(prow, it * 4 + grp, KC)] = (uint8_t)sf;
         }
@@ -431,6 +461,13 @@ __global__ void __launch_bounds__(kFc2Threads, 1)
   const int ntiles = clamp_tiles(p.hdr[HDR_NUM_TT], p.max_tiles);
   const int G = fc2_group(ntiles, NMT, npu, gridDim.x);
   const int num_units = ntiles * (NMT / G);
+  // Accumulator slots: the 256 accumulator columns split into slots as wide as
+  // the widest token tile of this call, at least 32 columns (8 slots when
+  // decoding), so that many narrow sub-units can be in flight between MMA and
+  // epilogue.
+  const int maxrows = min(max(p.hdr[HDR_MAXROWS], 1), kTileRows);
+  const uint32_t slot_cols = maxrows <= 32 ? 32u : maxrows <= 64 ? 64u : 128u;
+  const uint32_t nslots = 256u / slot_cols;
   const int4* tiles = reinterpret_cast<const int4*>(p.tt_list);
 
   if (warp == 0) {
@@ -511,13 +548,13 @@ __global__ void __launch_bounds__(kFc2Threads, 1)
         const uint32_t sfb = tmem + kFc2SfbCol + slot * (uint32_t)(NA * 4);
         for (int a = 0; a < NA; ++a) tmem_cp_32x128b_x4(sfb + a * 4, sf_desc(as + act_sf + a * 512));
         for (int g = 0; g < G && ok; ++g, ++sub) {
-          const uint32_t buf = (uint32_t)sub & 1u;
-          if (!wait_or_abort(&bars->tmem_empty[buf], (((uint32_t)sub >> 1) & 1u) ^ 1u, bars, p.status)) {
+          const uint32_t buf = (uint32_t)sub % nslots, use = (uint32_t)sub / nslots;
+          if (!wait_or_abort(&bars->tmem_empty[buf], (use & 1u) ^ 1u, bars, p.status)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t dcol = tmem + buf * 128;
+          const uint32_t dcol = tmem + buf * slot_cols;
           for (int kb = 0; kb < NKB; ++kb) {
             if (!wait_or_abort(&bars->full[stage], phase, bars, p.status)) {
               ok = false;
@@ -554,48 +591,62 @@ __global__ void __launch_bounds__(kFc2Threads, 1)
     const int q = warp & 3, grp = (warp - 2) >> 2;
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
     int sub = 0;
+    // Route weight and token (-1 if none) of this warp's columns of a tile,
+    // fetched one unit ahead so their latency hides under the current unit.
+    auto columns = [&](const int4& t, float (&w)[NI], int (&tk)[NI]) {
+#pragma unroll
+      for (int i = 0; i < NI; ++i) {
+        const int col = (grp + i * NGRP) * 16 + (lane & 15);
+        w[i] = 0.0f;
+        tk[i] = -1;
+        if (t.x >= 0 && col < t.z) {
+          const int f = __ldg(p.prow_pair + t.y + col);
+          if (f >= 0 && f < p.num_pairs) {
+            w[i] = __ldg(p.wrow + t.y + col);
+            tk[i] = f / p.k;
+          }
+        }
+      }
+    };
     int4 nxt = fc2_next_tile(tiles, blockIdx.x, num_units, ntiles);
     float s2_nxt = (nxt.x >= 0 && nxt.x < p.E) ? __ldg(p.dAdW2 + nxt.x) : 0.0f;
+    float wgt_nxt[NI];
+    int tok_nxt[NI];
+    if (tile_ok(nxt, p.E, p.max_rows)) columns(nxt, wgt_nxt, tok_nxt);
+    else columns(make_int4(-1, 0, 0, 0), wgt_nxt, tok_nxt);
     int4 nxt2 = fc2_next_tile(tiles, blockIdx.x + gridDim.x, num_units, ntiles);
     bool ok = true;
     for (int unit = blockIdx.x; unit < num_units && ok; unit += gridDim.x) {
       const int4 tl = nxt;
       const float s2 = s2_nxt;
-      nxt = nxt2;
-      s2_nxt = (nxt.x >= 0 && nxt.x < p.E) ? __ldg(p.dAdW2 + nxt.x) : 0.0f;
-      nxt2 = fc2_next_tile(tiles, unit + 2 * gridDim.x, num_units, ntiles);
-      if (!tile_ok(tl, p.E, p.max_rows)) continue;
-      const int mt0 = (unit / ntiles) * G;
-      const int row0 = tl.y, rows = tl.z;
-      const int nch = (rows + kTokChunk - 1) / kTokChunk;
-      // route weight and token (-1 if none) of this warp's columns, once per unit
       float wgt[NI];
       int tok[NI];
 #pragma unroll
       for (int i = 0; i < NI; ++i) {
-        const int col = (grp + i * NGRP) * 16 + (lane & 15);
-        wgt[i] = 0.0f;
-        tok[i] = -1;
-        if (col < rows) {
-          const int f = __ldg(p.prow_pair + row0 + col);
-          if (f >= 0 && f < p.num_pairs) {
-            wgt[i] = __ldg(p.wrow + row0 + col);
-            tok[i] = f / p.k;
-          }
-        }
+        wgt[i] = wgt_nxt[i];
+        tok[i] = tok_nxt[i];
       }
+      nxt = nxt2;
+      s2_nxt = (nxt.x >= 0 && nxt.x < p.E) ? __ldg(p.dAdW2 + nxt.x) : 0.0f;
+      if (tile_ok(nxt, p.E, p.max_rows)) columns(nxt, wgt_nxt, tok_nxt);
+      else columns(make_int4(-1, 0, 0, 0), wgt_nxt, tok_nxt);
+      nxt2 = fc2_next_tile(tiles, unit + 2 * gridDim.x, num_units, ntiles);
+      if (!tile_ok(tl, p.E, p.max_rows)) continue;
+      const int mt0 = (unit / ntiles) * G;
+      const int rows = tl.z;
+      const int nch = (rows + kTokChunk - 1) / kTokChunk;
       for (int g = 0; g < G; ++g, ++sub) {
-        const uint32_t buf = (uint32_t)sub & 1u;
-        if (!wait_or_abort(&bars->tmem_full[buf], ((uint32_t)sub >> 1) & 1u, bars, p.status)) {
+        const uint32_t buf = (uint32_t)sub % nslots, use = (uint32_t)sub / nslots;
+        if (!wait_or_abort(&bars->tmem_full[buf], use & 1u, bars, p.status)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        // drain this warp's columns from TMEM first, so the MMA can refill the buffer under the reductions
+        // drain this warp's columns from TMEM first, so the MMA can refill the slot under the reductions
         uint32_t r[NI][16];
 #pragma unroll
         for (int i = 0; i < NI; ++i)
-          if (grp + i * NGRP < nch) tmem_ld16(tmem + lane_base + buf * 128 + (grp + i * NGRP) * 16, r[i]);
+          if (grp + i * NGRP < nch) tmem_ld16(tmem + lane_base + buf * slot_cols + (grp + i * NGRP) * 16, r[i]);
         tmem_ld_wait();
         tc_fence_before();
         __syncwarp();
@@ -710,7 +761,11 @@ constexpr size_t kMmaCheckSmem = 36864 + sizeof(Barriers) + 1024;
 
 cudaError_t gemm_set_attributes() {
   cudaError_t err =
-      cudaFuncSetAttribute((const void*)fc1_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kFc1Smem);
+      cudaFuncSetAttribute((const void*)fc1_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)Fc1Cfg<1>::kSmem);
+  if (err != cudaSuccess) return err;
+  err = cudaFuncSetAttribute((const void*)fc1_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)Fc1Cfg<2>::kSmem);
   if (err != cudaSuccess) return err;
   err = cudaFuncSetAttribute((const void*)fc2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kFc2Smem);
   if (err != cudaSuccess) return err;
@@ -718,12 +773,15 @@ cudaError_t gemm_set_attributes() {
                               (int)kMmaCheckSmem);
 }
 
-cudaError_t launch_fc1(const CUtensorMap& w13, const RowMaps& xq, const Fc1Args& a, int grid, cudaStream_t st) {
+cudaError_t launch_fc1(const CUtensorMap& w13, const RowMaps& xq, const Fc1Args& a, int pair, int grid,
+                       cudaStream_t st) {
   CUtensorMap m0 = w13;
   RowMaps m1 = xq;
   Fc1Args args = a;
   void* kargs[] = {&m0, &m1, &args};
-  return launch_with_pdl((const void*)fc1_kernel, dim3(grid), dim3(kFc1Threads), kFc1Smem, st, kargs);
+  if (pair == 2)
+    return launch_with_pdl((const void*)fc1_kernel<2>, dim3(grid), dim3(kFc1Threads), Fc1Cfg<2>::kSmem, st, kargs);
+  return launch_with_pdl((const void*)fc1_kernel<1>, dim3(grid), dim3(kFc1Threads), Fc1Cfg<1>::kSmem, st, kargs);
 }
 
 cudaError_t launch_fc2(const CUtensorMap& w2, const RowMaps& aq, const Fc2Args& a, int grid, cudaStream_t st) {

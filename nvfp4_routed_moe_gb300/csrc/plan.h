@@ -26,6 +26,7 @@ enum : int {
   HDR_PPAD = 3,        // padded rows this call
   HDR_DONE = 4,        // last-arriver ticket of the multi-CTA routing
   HDR_NVALID = 5,      // routed pairs this call
+  HDR_MAXROWS = 6,     // largest number of pairs routed to one expert this call
   HDR_WORDS = 64,
 };
 

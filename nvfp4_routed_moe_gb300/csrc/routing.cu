@@ -123,6 +123,10 @@ __device__ void scan_experts(const RouteArgs& a, const int* cnt_s, int* s_offs, 
     s_tmp[warp * 3 + 1] = i1;
     s_tmp[warp * 3 + 2] = i2;
   }
+  int mx = 0;   // largest expert group, for the GEMMs' accumulator sizing
+  for (int i = 0; i < per; ++i) mx = max(mx, c[i]);
+  mx = __reduce_max_sync(0xffffffffu, mx);
+  if (lane == 0) s_tmp[208 + warp] = mx;
   __syncthreads();
   if (warp == 0) {
     int w0 = lane < NWARP ? s_tmp[lane * 3 + 0] : 0;
@@ -180,6 +184,9 @@ __device__ void scan_experts(const RouteArgs& a, const int* cnt_s, int* s_offs, 
     a.hdr[HDR_NVALID] = o0;
     a.hdr[HDR_PPAD] = o1;
     a.hdr[HDR_NUM_TT] = o2;
+    int m = 0;
+    for (int w = 0; w < NWARP; ++w) m = max(m, s_tmp[208 + w]);
+    a.hdr[HDR_MAXROWS] = m;
     s_tmp[200] = o0;
   }
   __syncthreads();
