@@ -11,9 +11,9 @@ namespace moe {
 cudaError_t launch_with_pdl(const void* fn, dim3 grid, dim3 block, size_t smem, cudaStream_t st, void** args);
 
 // ------------------------------------------------------------ X quantization
-// One warp per token: each lane quantizes 16-element groups g = lane + 32*i
-// of the token ("Cake SiTU backend": group-16 NVFP4 input quantization with
-// qX) once, and writes the codes and block scales to the padded expanded row
+// Each lane quantizes one 16-element group of a token ("Cake SiTU backend":
+// group-16 NVFP4 input quantization with qX) once, and writes the codes and
+// block scales to the padded expanded row
 // of every pair the token is routed to ("npu_moe_init_routing_v2", formula 5,
 // gather form: expandedX[gatherRowIdx[i]] = quantResult[i // k]).  It also
 // stores each pair's route weight (fp32) at the pair's padded row for FC2,
@@ -24,47 +24,50 @@ cudaError_t launch_with_pdl(const void* fn, dim3 grid, dim3 block, size_t smem, 
 // with whole-atom writes (a token's scales land in 56 different atoms, and
 // scattered 4-byte writes cost more than the extra pass).
 __global__ void __launch_bounds__(256) quant_x_kernel(const QuantXArgs a) {
+  // Warp w takes 32 groups (512 elements) of token w / S, S = ceil(H/512)
+  // slices per token, so a token's slices run in parallel warps.
   const int lane = threadIdx.x & 31;
-  const int64_t t = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int H = a.H, G = H / 16, KC = H / 16, S = (G + 31) / 32;
+  const int64_t w = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int64_t t = w / S;
+  const int sl = (int)(w - t * S);
   pdl_wait();
   pdl_launch_dependents();
   if (t >= a.T) return;
-  const int H = a.H, G = H / 16, KC = H / 16;
   const float q = __ldg(a.qX);
   const int rp = (lane < a.k) ? a.row_pos[t * a.k + lane] : -1;
-  if (rp >= 0 && rp < a.max_rows) a.wrow[rp] = bf16_bits_to_f32(a.route_w[t * a.k + lane]);
+  if (sl == 0 && rp >= 0 && rp < a.max_rows) a.wrow[rp] = bf16_bits_to_f32(a.route_w[t * a.k + lane]);
+  // this slice's share of the token's accumulator row
   float4* accr = reinterpret_cast<float4*>(a.acc + t * H);
-  for (int i = lane; i < H / 4; i += 32) accr[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int i = sl * 32 * 4 + lane; i < min(H / 4, (sl + 1) * 32 * 4); i += 32) accr[i] = make_float4(0.f, 0.f, 0.f, 0.f);
   const uint4* xr = reinterpret_cast<const uint4*>(a.x + t * H);
-  for (int g0 = 0; g0 < G; g0 += 32) {
-    const int g = g0 + lane;
-    const bool valid = g < G;
-    float v[16];
-    if (valid) {
-      const uint4 u0 = __ldg(xr + 2 * g), u1 = __ldg(xr + 2 * g + 1);
-      const uint32_t w[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+  const int g = sl * 32 + lane;
+  const bool valid = g < G;
+  float v[16];
+  if (valid) {
+    const uint4 u0 = __ldg(xr + 2 * g), u1 = __ldg(xr + 2 * g + 1);
+    const uint32_t wd[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        v[2 * i] = bf16_bits_to_f32(w[i] & 0xFFFFu);
-        v[2 * i + 1] = bf16_bits_to_f32(w[i] >> 16);
-      }
-    } else {
+    for (int i = 0; i < 8; ++i) {
+      v[2 * i] = bf16_bits_to_f32(wd[i] & 0xFFFFu);
+      v[2 * i + 1] = bf16_bits_to_f32(wd[i] >> 16);
+    }
+  } else {
 #pragma unroll
-      for (int i = 0; i < 16; ++i) v[i] = 0.f;
-    }
-    uint2 packed;
-    const uint32_t sf = nvfp4_quant16(v, q, packed);
-    // four consecutive groups share one 32-bit word of a scale atom row
-    uint32_t word = sf << (8 * (lane & 3));
-    word |= __shfl_xor_sync(0xffffffffu, word, 1);
-    word |= __shfl_xor_sync(0xffffffffu, word, 2);
-    if (a.sft && valid && (lane & 3) == 0) *reinterpret_cast<uint32_t*>(a.sft + t * G + g) = word;
-    for (int j = 0; j < a.k; ++j) {
-      const int row = __shfl_sync(0xffffffffu, rp, j);
-      if (row < 0 || row >= a.max_rows || !valid) continue;
-      *reinterpret_cast<uint2*>(a.xq + (size_t)row * (H / 2) + g * 8) = packed;
-      if (!a.sft && (lane & 3) == 0) *reinterpret_cast<uint32_t*>(a.sfx + atom_offset(row, g, KC)) = word;
-    }
+    for (int i = 0; i < 16; ++i) v[i] = 0.f;
+  }
+  uint2 packed;
+  const uint32_t sf = nvfp4_quant16(v, q, packed);
+  // four consecutive groups share one 32-bit word of a scale atom row
+  uint32_t word = sf << (8 * (lane & 3));
+  word |= __shfl_xor_sync(0xffffffffu, word, 1);
+  word |= __shfl_xor_sync(0xffffffffu, word, 2);
+  if (a.sft && valid && (lane & 3) == 0) *reinterpret_cast<uint32_t*>(a.sft + t * G + g) = word;
+  for (int j = 0; j < a.k; ++j) {
+    const int row = __shfl_sync(0xffffffffu, rp, j);
+    if (row < 0 || row >= a.max_rows || !valid) continue;
+    *reinterpret_cast<uint2*>(a.xq + (size_t)row * (H / 2) + g * 8) = packed;
+    if (!a.sft && (lane & 3) == 0) *reinterpret_cast<uint32_t*>(a.sfx + atom_offset(row, g, KC)) = word;
   }
 }
 
@@ -255,7 +258,8 @@ __global__ void __launch_bounds__(256) requant_lanes_kernel(const float* act, in
 cudaError_t launch_quant_x(const QuantXArgs& a, cudaStream_t st) {
   QuantXArgs args = a;
   void* kargs[] = {&args};
-  const unsigned blocks = (unsigned)((a.T + 7) / 8);
+  const int64_t warps = a.T * ((a.H / 16 + 31) / 32);
+  const unsigned blocks = (unsigned)((warps + 7) / 8);
   return launch_with_pdl((const void*)quant_x_kernel, dim3(blocks), dim3(256), 0, st, kargs);
 }
 
