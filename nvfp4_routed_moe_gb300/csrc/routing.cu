@@ -36,13 +36,13 @@ __device__ __forceinline__ uint32_t lanemask_lt() {
 }
 
 // Pass 1: per-warp histogram of ids[begin, end) into hist_w[E] (shared).
-__device__ __forceinline__ void warp_histogram(const int32_t* __restrict__ ids, int64_t begin, int64_t end, int E,
+__device__ __forceinline__ void warp_histogram(const int32_t* ids, int64_t begin, int64_t end, int E,
                                                int* hist_w) {
   const int lane = threadIdx.x & 31;
   for (int64_t base = begin; base < end; base += 32) {
     const int64_t f = base + lane;
     const bool in = f < end;
-    const int id = in ? __ldg(ids + f) : -1;
+    const int id = in ? ids[f] : -1;
     const bool ok = in && id >= 0 && id < E;
     const uint32_t okmask = __ballot_sync(0xffffffffu, ok);
     if (ok) {
@@ -55,14 +55,14 @@ __device__ __forceinline__ void warp_histogram(const int32_t* __restrict__ ids, 
 
 // Pass 2: hand out sorted slots.  base_w[e] holds the next slot of expert e
 // for this warp; offs/poffs are the expert's first dropless / padded row.
-__device__ __forceinline__ int warp_rank(const RouteArgs& a, int64_t begin, int64_t end, int* base_w,
-                                         const int* s_offs, const int* s_poffs) {
+__device__ __forceinline__ int warp_rank(const RouteArgs& a, const int32_t* ids, int64_t begin, int64_t end,
+                                         int* base_w, const int* s_offs, const int* s_poffs) {
   const int lane = threadIdx.x & 31;
   int invalid = 0;
   for (int64_t base = begin; base < end; base += 32) {
     const int64_t f = base + lane;
     const bool in = f < end;
-    const int id = in ? __ldg(a.ids + f) : -1;
+    const int id = in ? ids[f] : -1;
     const bool ok = in && id >= 0 && id < a.E;
     const uint32_t okmask = __ballot_sync(0xffffffffu, ok);
     if (ok) {
@@ -194,26 +194,31 @@ __device__ void scan_experts(const RouteArgs& a, const int* cnt_s, int* s_offs, 
 
 // ---------------------------------------------------------------- small path
 // One CTA of 1024 threads sorts up to kRouteSmallMax pairs in one launch.
+// The ids are staged in shared memory once; as many warps as there are
+// 32-pair chunks (at most 32) keep per-warp histograms.
 __global__ void __launch_bounds__(1024, 1) route_small_kernel(const RouteArgs a) {
   extern __shared__ int sm[];
   const int E = a.E;
-  int* hist = sm;                  // [32][E]
-  int* s_cnt = hist + 32 * E;      // [E]
+  const int NHW = a.P >= 1024 ? 32 : (int)((a.P + 31) / 32 > 0 ? (a.P + 31) / 32 : 1);   // histogram warps
+  int* hist = sm;                  // [NHW][E]
+  int* s_cnt = hist + NHW * E;     // [E]
   int* s_offs = s_cnt + E;         // [E]
   int* s_poffs = s_offs + E;       // [E]
   int* s_tmp = s_poffs + E;        // [256]
+  int* s_ids = s_tmp + 256;        // [P]
   const int tid = threadIdx.x, warp = tid >> 5;
   pdl_wait();
   pdl_launch_dependents();
-  for (int i = tid; i < 32 * E; i += 1024) hist[i] = 0;
+  for (int i = tid; i < NHW * E; i += 1024) hist[i] = 0;
+  for (int64_t i = tid; i < a.P; i += 1024) s_ids[i] = __ldg(a.ids + i);
   __syncthreads();
-  const int64_t per = (a.P + 31) / 32;
-  const int64_t b = warp * per, en = min(a.P, b + per);
-  warp_histogram(a.ids, b, en, E, hist + warp * E);
+  const int64_t per = (a.P + NHW - 1) / NHW;
+  const int64_t b = min(a.P, (int64_t)warp * per), en = min(a.P, b + per);
+  if (warp < NHW) warp_histogram(s_ids, b, en, E, hist + warp * E);
   __syncthreads();
   for (int e = tid; e < E; e += 1024) {
     int run = 0;
-    for (int w = 0; w < 32; ++w) {
+    for (int w = 0; w < NHW; ++w) {
       const int c = hist[w * E + e];
       hist[w * E + e] = run;
       run += c;
@@ -222,9 +227,9 @@ __global__ void __launch_bounds__(1024, 1) route_small_kernel(const RouteArgs a)
   }
   __syncthreads();
   scan_experts<1024>(a, s_cnt, s_offs, s_poffs, s_tmp);
-  for (int i = tid; i < 32 * E; i += 1024) hist[i] += s_offs[i % E];
+  for (int i = tid; i < NHW * E; i += 1024) hist[i] += s_offs[i % E];
   __syncthreads();
-  const int invalid = warp_rank(a, b, en, hist + warp * E, s_offs, s_poffs);
+  const int invalid = warp < NHW ? warp_rank(a, s_ids, b, en, hist + warp * E, s_offs, s_poffs) : 0;
   const int nvalid = s_tmp[200];
   for (int64_t i = nvalid + tid; i < a.P; i += 1024) a.sorted_row[i] = -1;
   if (invalid) {
@@ -311,7 +316,7 @@ __global__ void __launch_bounds__(256) route_rank_kernel(const RouteArgs a) {
     }
   }
   __syncthreads();
-  const int invalid = warp_rank(a, b, en, hist + warp * E, s_offs, s_poffs);
+  const int invalid = warp_rank(a, a.ids, b, en, hist + warp * E, s_offs, s_poffs);
   const int nvalid = a.offs[E];
   const int64_t t0 = max((int64_t)nvalid, cb), t1 = min(a.P, cb + kRouteChunk);
   for (int64_t i = t0 + tid; i < t1; i += 256) a.sorted_row[i] = -1;
@@ -425,7 +430,7 @@ __global__ void __launch_bounds__(256) init_finish_kernel(const InitFinishArgs a
 }
 
 // ------------------------------------------------------------------ launchers
-size_t route_small_smem(int E) { return (size_t)(32 * E + 3 * E + 256) * 4; }
+size_t route_small_smem(int E) { return (size_t)(32 * E + 3 * E + 256 + kRouteSmallMax) * 4; }
 size_t route_big_smem(int E) { return (size_t)(8 * E + 3 * E + 256) * 4; }
 
 cudaError_t launch_routing(const RouteArgs& a, cudaStream_t st, int* launches) {
