@@ -216,7 +216,11 @@ static RouteArgs route_args(const Shape& s, const WsLayout& L, uint8_t* ws, cons
   a.prow_pair = reinterpret_cast<int32_t*>(ws + L.prow_pair);
   a.tt_list = reinterpret_cast<int32_t*>(ws + L.tt_list);
   a.blockhist = reinterpret_cast<int32_t*>(ws + L.blockhist);
-  a.nblk = (int32_t)((a.P + kRouteChunk - 1) / kRouteChunk);
+  // about 32 routing CTAs (the last one's prefix over the per-CTA histograms
+  // grows with their number): chunk = ceil(P / 32) rounded up to 256, within [512, 4096]
+  int64_t chunk = ((a.P + 31) / 32 + 255) / 256 * 256;
+  a.chunk = (int32_t)(chunk < kRouteChunkMin ? kRouteChunkMin : chunk > kRouteChunk ? kRouteChunk : chunk);
+  a.nblk = (int32_t)((a.P + a.chunk - 1) / a.chunk);
   return a;
 }
 

@@ -13,7 +13,8 @@ constexpr int kFc1KBlock = 256;     // FP4 elements per FC1 k-block (128 B per r
 constexpr int kFc2KBlock = 128;     // FP4 elements per FC2 k-sub-block (64 B per row, 64B swizzle)
 constexpr int kTokChunk = 16;       // rows per activation TMA box (and MMA N granule)
 constexpr int kRouteSmallMax = 4096;  // pairs handled by the one-CTA routing kernel
-constexpr int kRouteChunk = 4096;     // pairs per CTA of the multi-CTA routing kernels
+constexpr int kRouteChunk = 4096;     // largest number of pairs per CTA of the multi-CTA routing kernels
+constexpr int kRouteChunkMin = 512;   // smallest (more CTAs for mid-size batches)
 constexpr int kMaxExperts = 1024;
 constexpr int kMaxTopK = 32;
 constexpr size_t kAccPassBytes = 64u << 20;  // default L2 budget of one combine pass over H
@@ -61,7 +62,7 @@ inline WsLayout make_layout(const Shape& s, int64_t max_tokens) {
   const int64_t padded = L.Pmax + (int64_t)(kTileRows - 1) * (L.Pmax < s.E ? L.Pmax : s.E);
   L.PpadMax = (int64_t)align_up((size_t)padded, kTileRows);
   L.TTmax = tt_bound(L.Pmax, s.E);
-  L.nblkMax = (L.Pmax + kRouteChunk - 1) / kRouteChunk;
+  L.nblkMax = (L.Pmax + kRouteChunkMin - 1) / kRouteChunkMin;
   size_t o = 0;
   auto take = [&](size_t bytes) {
     size_t at = o;
@@ -111,6 +112,7 @@ struct RouteArgs {
   int32_t* tt_list;   // int4 {expert, row0, rows, 0}
   int32_t* blockhist;
   int32_t nblk;
+  int32_t chunk;      // pairs per CTA of the multi-CTA kernels (a multiple of 256)
 };
 
 struct Fc1Args {

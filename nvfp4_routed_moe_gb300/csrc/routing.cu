@@ -241,7 +241,7 @@ __global__ void __launch_bounds__(1024, 1) route_small_kernel(const RouteArgs a)
 // ---------------------------------------------------------------- large path
 // Kernel 1: per-block histograms; the last block to finish (ticket counter,
 // no waiting) scans them into per-(block, expert) bases and per-expert
-// offsets, and writes the tile list.  256 threads, kRouteChunk pairs per block.
+// offsets, and writes the tile list.  256 threads, a.chunk pairs per block.
 __global__ void __launch_bounds__(256) route_hist_kernel(const RouteArgs a) {
   extern __shared__ int sm[];
   const int E = a.E;
@@ -256,9 +256,9 @@ __global__ void __launch_bounds__(256) route_hist_kernel(const RouteArgs a) {
   pdl_launch_dependents();
   for (int i = tid; i < 8 * E; i += 256) hist[i] = 0;
   __syncthreads();
-  const int64_t cb = (int64_t)blockIdx.x * kRouteChunk;
-  const int64_t wb = cb + (int64_t)warp * (kRouteChunk / 8);
-  warp_histogram(a.ids, min(wb, a.P), min(wb + kRouteChunk / 8, a.P), E, hist + warp * E);
+  const int64_t cb = (int64_t)blockIdx.x * a.chunk;
+  const int64_t wb = cb + (int64_t)warp * (a.chunk / 8);
+  warp_histogram(a.ids, min(wb, a.P), min(wb + a.chunk / 8, a.P), E, hist + warp * E);
   __syncthreads();
   for (int e = tid; e < E; e += 256) {
     int s = 0;
@@ -273,11 +273,15 @@ __global__ void __launch_bounds__(256) route_hist_kernel(const RouteArgs a) {
   __threadfence();
   for (int e = tid; e < E; e += 256) {
     int run = 0;
-    for (int blk = 0; blk < a.nblk; ++blk) {
-      int* p = &a.blockhist[(size_t)blk * E + e];
-      const int c = __ldcg(p);
-      *p = run;
-      run += c;
+    for (int blk0 = 0; blk0 < a.nblk; blk0 += 8) {   // 8 loads in flight per thread
+      int c[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) c[j] = blk0 + j < a.nblk ? __ldcg(&a.blockhist[(size_t)(blk0 + j) * E + e]) : 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        if (blk0 + j < a.nblk) a.blockhist[(size_t)(blk0 + j) * E + e] = run;
+        run += c[j];
+      }
     }
     s_cnt[e] = run;
   }
@@ -302,9 +306,9 @@ __global__ void __launch_bounds__(256) route_rank_kernel(const RouteArgs a) {
     s_poffs[e] = a.poffs[e];
   }
   __syncthreads();
-  const int64_t cb = (int64_t)blockIdx.x * kRouteChunk;
-  const int64_t wb = cb + (int64_t)warp * (kRouteChunk / 8);
-  const int64_t b = min(wb, a.P), en = min(wb + kRouteChunk / 8, a.P);
+  const int64_t cb = (int64_t)blockIdx.x * a.chunk;
+  const int64_t wb = cb + (int64_t)warp * (a.chunk / 8);
+  const int64_t b = min(wb, a.P), en = min(wb + a.chunk / 8, a.P);
   warp_histogram(a.ids, b, en, E, hist + warp * E);
   __syncthreads();
   for (int e = tid; e < E; e += 256) {
@@ -318,7 +322,7 @@ __global__ void __launch_bounds__(256) route_rank_kernel(const RouteArgs a) {
   __syncthreads();
   const int invalid = warp_rank(a, a.ids, b, en, hist + warp * E, s_offs, s_poffs);
   const int nvalid = a.offs[E];
-  const int64_t t0 = max((int64_t)nvalid, cb), t1 = min(a.P, cb + kRouteChunk);
+  const int64_t t0 = max((int64_t)nvalid, cb), t1 = min(a.P, cb + a.chunk);
   for (int64_t i = t0 + tid; i < t1; i += 256) a.sorted_row[i] = -1;
   if (invalid) {
     atomicAdd(&a.hdr[HDR_INVALID], invalid);

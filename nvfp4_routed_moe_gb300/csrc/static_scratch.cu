@@ -154,6 +154,7 @@ extern "C" moe_status_t moe_init_routing_static(const moe_shape_t* shape, int64_
   ra.prow_pair = reinterpret_cast<int32_t*>(w + L.prow_pair);
   ra.tt_list = reinterpret_cast<int32_t*>(w + L.tt_list);
   ra.blockhist = reinterpret_cast<int32_t*>(w + L.blockhist);
+  ra.chunk = kRouteChunk;
   ra.nblk = (int32_t)((ra.P + kRouteChunk - 1) / kRouteChunk);
   int nl = 0;
   if (launch_routing(ra, stream, &nl) != cudaSuccess) return MOE_ERR_CUDA;
