@@ -75,6 +75,9 @@ def _load():
         lib.oracle_dynamic_int8_row.argtypes = [P, i64, P, P]
         lib.oracle_init_routing.restype = i64
         lib.oracle_init_routing.argtypes = [P, P, i64, i32, i32, i64, i32, i32, i32, i32, i32, P, P, P, P]
+        lib.oracle_init_routing_ex.restype = i64
+        lib.oracle_init_routing_ex.argtypes = [P, P, i64, i32, i32, i64, i32, i32, i64, i32, i32, i32, i32, i32,
+                                               P, i32, P, P, P, P, P]
         lib.oracle_situ.restype = ctypes.c_double
         lib.oracle_situ.argtypes = [ctypes.c_double] * 4
         lib.oracle_moe_forward_tokens.restype = None
@@ -254,6 +257,47 @@ def init_routing(x_bf16_bits, expert_ids, num_experts: int, *, drop_pad: int = 0
     if scale is not None:
         scale = scale[:rows]
     return ex, ridx[:P], tok, scale, int(nvalid)
+
+
+def init_routing_ex(x_bf16_bits, expert_ids, num_experts: int, *, expert_start: int = 0, expert_end=None,
+                    active_num: int = 0, drop_pad: int = 0, expert_capacity: int = 0, row_idx_type: int = 0,
+                    tokens_num_type: int = 0, quant_mode: int = 1, scale=None, offset=None):
+    """Init-routing with every option of the page's parameter list
+    ("npu_moe_init_routing_v2": active_expert_range, active_num,
+    expert_tokens_num_type 0/1/2, quant_mode -1/0/1 with scale / offset).
+    Returns (expanded_x, expanded_row_idx, tokens_out, expanded_scale,
+    available); tokens_out is [end-start] (cumsum or count) or [E, 2]
+    (key_value)."""
+    x = _c(x_bf16_bits, np.uint16)
+    ids = _c(expert_ids, np.int32)
+    T, H = x.shape
+    k = ids.shape[1]
+    P = T * k
+    end = num_experts if expert_end is None else expert_end
+    R = end - expert_start
+    rows = R * expert_capacity if drop_pad else P
+    ex = np.zeros((rows, H), np.uint16 if quant_mode == -1 else np.int8)
+    want_scale = quant_mode == 1 or (quant_mode == -1 and scale is not None)
+    sc_out = np.zeros(max(rows, 1), np.float32) if want_scale else None
+    if scale is None:
+        sc_in, scale_rows = None, 0
+    elif quant_mode == 1:                       # smooth scale rows [1 or end-start, H]
+        sc_in = _c(np.asarray(scale, np.float32).reshape(-1, H), np.float32)
+        scale_rows = sc_in.shape[0]
+    else:                                       # [T] (no quant) or [1] (static)
+        sc_in, scale_rows = _c(np.asarray(scale, np.float32).ravel(), np.float32), 1
+    off = None if offset is None else _c(np.asarray(offset, np.float32).ravel(), np.float32)
+    ridx = np.empty(max(P, 1), np.int32)
+    tok = np.zeros(2 * num_experts if tokens_num_type == 2 else max(R, 1), np.int32)
+    avail = _load().oracle_init_routing_ex(_ptr(x), _ptr(ids), T, k, num_experts, H, expert_start, end, active_num,
+                                           drop_pad, expert_capacity, row_idx_type, tokens_num_type, quant_mode,
+                                           _ptr(sc_in), scale_rows, _ptr(off), _ptr(ex), _ptr(ridx), _ptr(tok),
+                                           _ptr(sc_out))
+    if tokens_num_type == 2:
+        tok = tok.reshape(num_experts, 2)
+    else:
+        tok = tok[:R]
+    return ex, ridx[:P], tok, (None if sc_out is None else sc_out[:rows]), int(avail)
 
 
 # ----------------------------------------------------------------- the forward

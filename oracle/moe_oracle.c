@@ -339,6 +339,141 @@ int64_t oracle_init_routing(const uint16_t* x, const int32_t* ids, int64_t T, in
     return nvalid;
 }
 
+/* Init-routing with every option of the page's parameter list ([Ascend]
+ * formulas 1-6 and the parameters active_expert_range, active_num,
+ * expert_tokens_num_type, quant_mode, scale, offset).  Readings where the
+ * page is loose are marked (r).
+ *   expert_start, expert_end   active range [start, end) of expert ids; pairs
+ *                              whose id lies outside it are not routed (ids
+ *                              outside [0, E) are not routed either)
+ *   active_num                 > 0: only the first min(active_num, available)
+ *                              sorted rows are moved (Active); <= 0 dropless
+ *   drop_pad, C                as in oracle_init_routing (full range only)
+ *   row_idx_type               0 gather form, 1 scatter form
+ *   tokens_num_type            0 inclusive cumsum, 1 count, over the range
+ *                              (end-start entries); 2 key_value: rows
+ *                              (expert id, count) of the in-range experts
+ *                              with a non-zero count, in expert order, at the
+ *                              head of [E, 2]; the remaining rows 0 (r)
+ *   quant_mode -1              bf16 copy; scale [T] or NULL: expanded_scale
+ *                              of a row = scale of its token
+ *   quant_mode 0 (static)      q = rint(x*scale[0] + offset[0]) in fp32, half
+ *                              to even, saturated to [-128, 127] (r); no
+ *                              expanded_scale
+ *   quant_mode 1 (dynamic)     smooth = scale [nsr, H] or NULL (nsr 1 or
+ *                              end-start): xs = x * smooth[row of the pair's
+ *                              expert - start, or 0]; s = row_max|xs|/127;
+ *                              q = rint(xs / s) clamped to +-127 (r: the
+ *                              page's quotient omits the smooth factor, which
+ *                              it used to compute s); expanded_scale = s
+ * expanded_row_idx gather form: the moved row of a pair, else -1; scatter
+ * form: sorted_row for the available pairs, then -1.
+ * Returns availableIdxNum, the number of pairs with an id in the range. */
+int64_t oracle_init_routing_ex(const uint16_t* x, const int32_t* ids, int64_t T, int32_t k, int32_t E, int64_t H,
+                               int32_t expert_start, int32_t expert_end, int64_t active_num, int32_t drop_pad,
+                               int32_t C, int32_t row_idx_type, int32_t tokens_num_type, int32_t quant_mode,
+                               const float* scale, int32_t scale_rows, const float* offset, void* expanded_x,
+                               int32_t* expanded_row_idx, int32_t* tokens_out, float* expanded_scale) {
+    int64_t P = T * (int64_t)k;
+    int32_t R = expert_end - expert_start;
+    int32_t* sorted_row = (int32_t*)malloc(sizeof(int32_t) * (size_t)(P > 0 ? P : 1));
+    int32_t* sorted_expert = (int32_t*)malloc(sizeof(int32_t) * (size_t)(P > 0 ? P : 1));
+    int32_t* count = (int32_t*)calloc((size_t)(R > 0 ? R : 1), sizeof(int32_t));
+    int32_t* cumsum = (int32_t*)calloc((size_t)(R > 0 ? R : 1), sizeof(int32_t));
+    /* formulas 1 and 3 over the active range: stable by (expert, flat index) */
+    int64_t avail = 0;
+    for (int32_t e = expert_start; e < expert_end; ++e) {
+        for (int64_t f = 0; f < P; ++f)
+            if (ids[f] == e) {
+                sorted_row[avail] = (int32_t)f;
+                sorted_expert[avail] = e;
+                ++avail;
+                ++count[e - expert_start];
+            }
+        cumsum[e - expert_start] = (int32_t)avail;
+    }
+    int64_t nmove = (active_num > 0 && active_num < avail) ? active_num : avail;
+    size_t esz = (quant_mode == -1) ? 2 : 1;
+    /* destination row of sorted position i */
+    int32_t* dest = (int32_t*)malloc(sizeof(int32_t) * (size_t)(P > 0 ? P : 1));
+    for (int64_t i = 0; i < avail; ++i) {
+        if (!drop_pad) {
+            dest[i] = (i < nmove) ? (int32_t)i : -1;
+        } else {
+            int32_t e = sorted_expert[i] - expert_start;
+            int64_t r = i - (cumsum[e] - count[e]);
+            dest[i] = (r < C) ? (int32_t)(e * (int64_t)C + r) : -1;
+        }
+    }
+    if (drop_pad) {
+        memset(expanded_x, 0, (size_t)R * (size_t)C * (size_t)H * esz);
+        if (expanded_scale) memset(expanded_scale, 0, sizeof(float) * (size_t)R * (size_t)C);
+    }
+    /* formulas 4 and 5, one moved row at a time */
+    float* xs = (float*)malloc(sizeof(float) * (size_t)(H > 0 ? H : 1));
+    for (int64_t i = 0; i < avail; ++i) {
+        if (dest[i] < 0) continue;
+        int64_t t = sorted_row[i] / k;
+        const uint16_t* xr = x + t * H;
+        if (quant_mode == -1) {
+            memcpy((uint16_t*)expanded_x + (int64_t)dest[i] * H, xr, (size_t)H * 2);
+            if (expanded_scale && scale) expanded_scale[dest[i]] = scale[t];
+        } else if (quant_mode == 0) {
+            int8_t* q = (int8_t*)expanded_x + (int64_t)dest[i] * H;
+            for (int64_t h = 0; h < H; ++h) {
+                float v = oracle_bf16_to_float(xr[h]) * scale[0];
+                v = v + offset[0];
+                float rr = nearbyintf(v);
+                if (rr > 127.0f) rr = 127.0f;
+                if (rr < -128.0f) rr = -128.0f;
+                q[h] = (int8_t)rr;
+            }
+        } else {
+            const float* sm = NULL;
+            if (scale && scale_rows > 0) sm = scale + (scale_rows == 1 ? 0 : (int64_t)(sorted_expert[i] - expert_start)) * H;
+            float amax = 0.0f;
+            for (int64_t h = 0; h < H; ++h) {
+                float v = oracle_bf16_to_float(xr[h]);
+                if (sm) v = v * sm[h];
+                xs[h] = v;
+                if (fabsf(v) > amax) amax = fabsf(v);
+            }
+            float sc = amax / 127.0f;
+            int8_t* q = (int8_t*)expanded_x + (int64_t)dest[i] * H;
+            for (int64_t h = 0; h < H; ++h) {
+                if (sc == 0.0f) { q[h] = 0; continue; }
+                float rr = nearbyintf(xs[h] / sc);
+                if (rr > 127.0f) rr = 127.0f;
+                if (rr < -127.0f) rr = -127.0f;
+                q[h] = (int8_t)rr;
+            }
+            if (expanded_scale) expanded_scale[dest[i]] = sc;
+        }
+    }
+    /* formula 2 */
+    if (row_idx_type == 1) {
+        for (int64_t i = 0; i < P; ++i) expanded_row_idx[i] = (i < avail) ? sorted_row[i] : -1;
+    } else {
+        for (int64_t f = 0; f < P; ++f) expanded_row_idx[f] = -1;
+        for (int64_t i = 0; i < avail; ++i) expanded_row_idx[sorted_row[i]] = dest[i];
+    }
+    /* formula 3 output */
+    if (tokens_num_type == 2) {
+        for (int64_t j = 0; j < 2 * (int64_t)E; ++j) tokens_out[j] = 0;
+        int64_t n = 0;
+        for (int32_t e = 0; e < R; ++e)
+            if (count[e] > 0) {
+                tokens_out[2 * n] = expert_start + e;
+                tokens_out[2 * n + 1] = count[e];
+                ++n;
+            }
+    } else {
+        for (int32_t e = 0; e < R; ++e) tokens_out[e] = (tokens_num_type == 1) ? count[e] : cumsum[e];
+    }
+    free(xs); free(dest); free(sorted_row); free(sorted_expert); free(count); free(cumsum);
+    return avail;
+}
+
 /* ------------------------------------------------------------------------ */
 /* SiTU ([Cake] "Default SiTU is (4*tanh(g/4)*sigmoid(g))*(25*tanh(u/25))",  */
 /* per-expert beta / linear beta optional).                                   */
