@@ -109,29 +109,48 @@ moe_status_t moe_forward(const moe_shape_t* shape, int64_t num_tokens, const voi
 
 /* Options of moe_init_routing (torch_npu "npu_moe_init_routing_v2",
  * parameter list: drop_pad_mode, expert_capacity, row_idx_type,
- * expert_tokens_num_type, quant_mode). */
+ * expert_tokens_num_type, quant_mode, active_expert_range, active_num,
+ * scale, offset).  With the fields after quant_mode zero, the op routes every
+ * expert, dropless, with no input scale. */
 typedef struct {
   int32_t drop_pad;         /* 0 dropless, 1 pad/drop every expert to expert_capacity rows */
   int32_t expert_capacity;  /* C, used when drop_pad == 1 */
   int32_t row_idx_type;     /* 0 gather form (default), 1 scatter form */
-  int32_t tokens_num_type;  /* 0 inclusive cumsum (default), 1 count; 2 (key_value) unsupported */
-  int32_t quant_mode;       /* -1 no quant (bf16 rows), 1 dynamic int8; 0 (static) unsupported */
+  int32_t tokens_num_type;  /* 0 inclusive cumsum (default), 1 count, 2 key_value */
+  int32_t quant_mode;       /* -1 no quant (bf16 rows), 0 static int8, 1 dynamic int8 */
+  int32_t expert_start;     /* active expert range [expert_start, expert_end); */
+  int32_t expert_end;       /*   both 0 = every expert; drop/pad needs every expert */
+  int64_t active_num;       /* > 0 (dropless only): move only the first active_num sorted rows */
+  const float* scale;       /* device; quant -1: [num_rows] carried to expanded_scale, or NULL;
+                               quant 0: [1] (required); quant 1: smooth scale [scale_rows, hidden] or NULL */
+  int32_t scale_rows;       /* quant 1 with a smooth scale: 1 (shared) or expert_end - expert_start */
+  const float* offset;      /* device; quant 0: [1] (required) */
+  int32_t* available_out;   /* device [1] or NULL: availableIdxNum, the pairs whose id is in the range */
 } moe_routing_opts_t;
 
-/* Init-routing alone ("npu_moe_init_routing_v2", formulas 1-5):
+/* Init-routing alone ("npu_moe_init_routing_v2", formulas 1-6):
  *   x [num_rows, hidden] bf16; expert_ids [num_rows, k] int32;
- *   expanded_x: dropless [num_rows*k, hidden], drop/pad [E*C, hidden]
- *     (int8 when quant_mode == 1, else bf16); rows of valid pairs in expert-
- *     sorted order; drop/pad slots beyond an expert's count are zero;
+ *   Only pairs whose id lies in the active range are routed (ids outside
+ *   [0, E) are also skipped, and flagged in the status word).
+ *   expanded_x: dropless [num_rows*k, hidden] (Active: its first
+ *     min(active_num, available) rows), drop/pad [E*C, hidden] (int8 when
+ *     quant_mode is 0 or 1, else bf16); rows in expert-sorted order; drop/pad
+ *     slots beyond an expert's count are zero;
+ *     quant 0: rint(x*scale + offset), half to even, saturated to [-128, 127];
+ *     quant 1: xs = x (times the smooth row of the pair's expert, or the shared
+ *     row), s = row_max|xs|/127, rint(xs / s) clamped to +-127;
  *   expanded_row_idx [num_rows*k] int32: gather form out[sortedRowIdx[i]] = i
- *     (drop/pad: e*C + rank, -1 for dropped or invalid pairs), or scatter form
- *     out[i] = sortedRowIdx[i] (-1 past the valid count);
- *   tokens_cumsum_or_count [E] int32 (not clipped by the capacity);
- *   expanded_scale [rows of expanded_x] fp32 (quant_mode 1, else may be NULL):
- *     row_max(|x|)/127 of the source row, 0 on unfilled slots.
+ *     for moved rows (drop/pad: e*C + rank), -1 for pairs not moved; or
+ *     scatter form out[i] = sortedRowIdx[i] for the available pairs, then -1;
+ *   tokens_cumsum_or_count: cumsum or count [expert_end - expert_start] int32
+ *     (not clipped by the capacity), or key_value [E, 2]: (expert id, count) of
+ *     the in-range experts with a non-zero count in expert order, then zeros;
+ *   expanded_scale [rows of expanded_x] fp32: quant 1 the row scale s; quant
+ *     -1 with a scale: the token's scale; 0 on unfilled slots; else may be NULL.
  * The sort is stable (ties by flat row index t*k+j).  ws: a workspace of
  * moe_workspace_size(shape) for at least num_rows tokens (shape.inter is
- * used only for that size), prepared for num_rows. */
+ * used only for that size), prepared for num_rows.  Options out of range
+ * return MOE_ERR_INVALID_ARG. */
 moe_status_t moe_init_routing(const moe_shape_t* shape, int64_t num_rows, const void* x, const int32_t* expert_ids,
                               const moe_routing_opts_t* opts, void* expanded_x, int32_t* expanded_row_idx,
                               int32_t* tokens_cumsum_or_count, float* expanded_scale, void* ws, size_t ws_bytes,

@@ -42,7 +42,9 @@ class moe_shape_t(ctypes.Structure):
 
 class moe_routing_opts_t(ctypes.Structure):
     _fields_ = [("drop_pad", ctypes.c_int32), ("expert_capacity", ctypes.c_int32), ("row_idx_type", ctypes.c_int32),
-                ("tokens_num_type", ctypes.c_int32), ("quant_mode", ctypes.c_int32)]
+                ("tokens_num_type", ctypes.c_int32), ("quant_mode", ctypes.c_int32), ("expert_start", ctypes.c_int32),
+                ("expert_end", ctypes.c_int32), ("active_num", ctypes.c_int64), ("scale", ctypes.c_void_p),
+                ("scale_rows", ctypes.c_int32), ("offset", ctypes.c_void_p), ("available_out", ctypes.c_void_p)]
 
 
 class moe_ws_layout_t(ctypes.Structure):
@@ -151,6 +153,14 @@ def moe_forward(shp, num_tokens, x, expert_ids, route_weights, w13, sf13, w2, sf
     _check(lib().moe_forward(ctypes.byref(shp), num_tokens, _p(x), _p(expert_ids), _p(route_weights), _p(w13),
                              _p(sf13), _p(w2), _p(sf2), _p(qX), _p(dX_dW13), _p(qA), _p(dA_dW2), _p(situ_beta),
                              _p(situ_linear_beta), _p(ws), _nbytes(ws), _p(out), _stream(stream)), "moe_forward")
+
+
+def routing_opts(drop_pad=0, expert_capacity=0, row_idx_type=0, tokens_num_type=0, quant_mode=1, expert_start=0,
+                 expert_end=0, active_num=0, scale=None, scale_rows=0, offset=None, available_out=None):
+    """moe_routing_opts_t with device tensors (or None) for scale, offset, available_out."""
+    ptr = lambda t: None if t is None else t.data_ptr()
+    return moe_routing_opts_t(drop_pad, expert_capacity, row_idx_type, tokens_num_type, quant_mode, expert_start,
+                              expert_end, active_num, ptr(scale), scale_rows, ptr(offset), ptr(available_out))
 
 
 def moe_init_routing(shp, num_rows, x, expert_ids, opts: moe_routing_opts_t, expanded_x, expanded_row_idx,

@@ -18,6 +18,7 @@ cudaError_t launch_routing(const RouteArgs& a, cudaStream_t st, int* launches);
 cudaError_t routing_set_attributes(int E);
 cudaError_t launch_init_move(const InitMoveArgs& a, cudaStream_t st);
 cudaError_t launch_init_finish(const InitFinishArgs& a, cudaStream_t st, int num_sms);
+cudaError_t launch_init_rows(const InitRowsArgs& a, int64_t P, cudaStream_t st, int num_sms);
 cudaError_t launch_quant_x(const QuantXArgs& a, cudaStream_t st);
 cudaError_t launch_sf_atoms(const SfAtomArgs& a, int64_t max_words, int num_sms, cudaStream_t st);
 cudaError_t launch_finalize(const float* acc, uint16_t* out, int64_t T, int H, int num_sms, cudaStream_t st);
@@ -204,6 +205,8 @@ static RouteArgs route_args(const Shape& s, const WsLayout& L, uint8_t* ws, cons
   a.P = T * s.k;
   a.k = s.k;
   a.E = s.E;
+  a.id_base = 0;
+  a.E_all = s.E;
   a.hdr = reinterpret_cast<int32_t*>(ws + L.header);
   a.count = reinterpret_cast<int32_t*>(ws + L.count);
   a.cumsum = reinterpret_cast<int32_t*>(ws + L.cumsum);
@@ -277,6 +280,109 @@ static void prof_end_call(cudaStream_t st) {
   if (!g_prof.on || g_prof.calls >= g_prof.max_calls) return;
   prof_mark(kStages, st);
   ++g_prof.calls;
+}
+
+moe_status_t init_routing_check(const moe_shape_t* shape, const moe_routing_opts_t* o, int32_t* base,
+                                int32_t* range) {
+  if (o->drop_pad != 0 && o->drop_pad != 1) return MOE_ERR_INVALID_ARG;
+  if (o->drop_pad && o->expert_capacity < 1) return MOE_ERR_INVALID_ARG;
+  if (o->row_idx_type != 0 && o->row_idx_type != 1) return MOE_ERR_INVALID_ARG;
+  if (o->tokens_num_type < 0 || o->tokens_num_type > 2) return MOE_ERR_INVALID_ARG;
+  if (o->quant_mode < -1 || o->quant_mode > 1) return MOE_ERR_INVALID_ARG;
+  int32_t lo = o->expert_start, hi = o->expert_end;
+  if (lo == 0 && hi == 0) hi = shape->num_experts;
+  if (lo < 0 || hi <= lo || hi > shape->num_experts) return MOE_ERR_INVALID_ARG;
+  if (o->drop_pad && (lo != 0 || hi != shape->num_experts || o->active_num > 0)) return MOE_ERR_INVALID_ARG;
+  if (o->quant_mode == 0 && (!o->scale || !o->offset)) return MOE_ERR_INVALID_ARG;
+  if (o->quant_mode == 1 && o->scale && o->scale_rows != 1 && o->scale_rows != hi - lo) return MOE_ERR_INVALID_ARG;
+  *base = lo;
+  *range = hi - lo;
+  return MOE_OK;
+}
+
+cudaError_t init_routing_enqueue(RouteArgs ra, int32_t base, int32_t range, const moe_shape_t* shape, int64_t T,
+                                 const void* x, const int32_t* ids, const moe_routing_opts_t* o, void* expanded_x,
+                                 int32_t* expanded_row_idx, int32_t* tokens_out, float* expanded_scale, int sms,
+                                 cudaStream_t st) {
+  ra.id_base = base;
+  ra.E = range;
+  ra.E_all = shape->num_experts;
+  int nl = 0;
+  cudaError_t err = launch_routing(ra, st, &nl);
+  if (err != cudaSuccess) return err;
+  // Token-driven move (each token quantized once, written to its pairs' rows)
+  // for the plain options; row-driven (scatter form) for the others.
+  const bool plain = base == 0 && range == shape->num_experts && o->active_num <= 0 && !o->scale &&
+                     o->quant_mode != 0;
+  float* sc_out = (o->quant_mode == 1 || (o->quant_mode == -1 && o->scale)) ? expanded_scale : nullptr;
+  if (plain) {
+    InitMoveArgs ma{};
+    ma.x = static_cast<const uint16_t*>(x);
+    ma.ids = ids;
+    ma.gather = ra.gather;
+    ma.offs = ra.offs;
+    ma.T = T;
+    ma.k = shape->top_k;
+    ma.E = range;
+    ma.H = shape->hidden;
+    ma.drop_pad = o->drop_pad;
+    ma.C = o->expert_capacity;
+    ma.quant_mode = o->quant_mode;
+    ma.row_idx_type = o->row_idx_type;
+    ma.expanded_x = expanded_x;
+    ma.expanded_scale = sc_out;
+    ma.expanded_row_idx = expanded_row_idx;
+    err = launch_init_move(ma, st);
+  } else {
+    InitRowsArgs wa{};
+    wa.x = static_cast<const uint16_t*>(x);
+    wa.ids = ids;
+    wa.sorted_row = ra.sorted_row;
+    wa.count = ra.count;
+    wa.cumsum = ra.cumsum;
+    wa.hdr = ra.hdr;
+    wa.T = T;
+    wa.active_num = o->active_num;
+    wa.k = shape->top_k;
+    wa.E = range;
+    wa.id_base = base;
+    wa.H = shape->hidden;
+    wa.drop_pad = o->drop_pad;
+    wa.C = o->expert_capacity;
+    wa.quant_mode = o->quant_mode;
+    wa.scale = o->scale;
+    wa.scale_rows = o->scale_rows;
+    wa.offset = o->offset;
+    wa.expanded_x = expanded_x;
+    wa.expanded_scale = sc_out;
+    err = launch_init_rows(wa, ra.P, st, sms);
+  }
+  if (err != cudaSuccess) return err;
+  InitFinishArgs fa{};
+  fa.count = ra.count;
+  fa.cumsum = ra.cumsum;
+  fa.sorted_row = ra.sorted_row;
+  fa.gather = ra.gather;
+  fa.ids = ids;
+  fa.hdr = ra.hdr;
+  fa.P = ra.P;
+  fa.active_num = o->active_num;
+  fa.E = range;
+  fa.H = shape->hidden;
+  fa.C = o->expert_capacity;
+  fa.drop_pad = o->drop_pad;
+  fa.row_idx_type = o->row_idx_type;
+  fa.tokens_num_type = o->tokens_num_type;
+  fa.esize = o->quant_mode == -1 ? 2 : 1;
+  fa.E_all = shape->num_experts;
+  fa.id_base = base;
+  fa.gather_idx = plain ? 0 : 1;
+  fa.expanded_x = expanded_x;
+  fa.expanded_scale = sc_out;
+  fa.expanded_row_idx = expanded_row_idx;
+  fa.tokens_out = tokens_out;
+  fa.available_out = o->available_out;
+  return launch_init_finish(fa, st, sms);
 }
 
 }  // namespace moe
@@ -506,12 +612,9 @@ moe_status_t moe_init_routing(const moe_shape_t* shape, int64_t num_rows, const 
   if (!x || !expert_ids || !opts || !expanded_x || !expanded_row_idx || !tokens_cumsum_or_count || !ws ||
       num_rows < 1)
     return MOE_ERR_INVALID_ARG;
-  if (opts->drop_pad != 0 && opts->drop_pad != 1) return MOE_ERR_INVALID_ARG;
-  if (opts->drop_pad && opts->expert_capacity < 1) return MOE_ERR_INVALID_ARG;
-  if (opts->row_idx_type != 0 && opts->row_idx_type != 1) return MOE_ERR_INVALID_ARG;
-  if (opts->tokens_num_type == 2 || opts->quant_mode == 0) return MOE_ERR_UNSUPPORTED;
-  if (opts->tokens_num_type != 0 && opts->tokens_num_type != 1) return MOE_ERR_INVALID_ARG;
-  if (opts->quant_mode != -1 && opts->quant_mode != 1) return MOE_ERR_INVALID_ARG;
+  int32_t base = 0, range = 0;
+  st = init_routing_check(shape, opts, &base, &range);
+  if (st != MOE_OK) return st;
   if (!aligned(x, 16) || !aligned(expanded_x, 16) || !aligned(ws, 256)) return MOE_ERR_INVALID_ARG;
   const Shape s = to_shape(shape);
   const int64_t cap = capacity_tokens(s, ws_bytes);
@@ -520,44 +623,9 @@ moe_status_t moe_init_routing(const moe_shape_t* shape, int64_t num_rows, const 
   const WsLayout L = make_layout(s, cap);
   int sms = 0;
   MOE_CUDA(device_ready(&sms));
-  uint8_t* w = static_cast<uint8_t*>(ws);
-  RouteArgs ra = route_args(s, L, w, expert_ids, num_rows);
-  int nl = 0;
-  MOE_CUDA(launch_routing(ra, stream, &nl));
-  InitMoveArgs ma{};
-  ma.x = static_cast<const uint16_t*>(x);
-  ma.ids = expert_ids;
-  ma.gather = ra.gather;
-  ma.offs = ra.offs;
-  ma.T = num_rows;
-  ma.k = s.k;
-  ma.E = s.E;
-  ma.H = s.H;
-  ma.drop_pad = opts->drop_pad;
-  ma.C = opts->expert_capacity;
-  ma.quant_mode = opts->quant_mode;
-  ma.row_idx_type = opts->row_idx_type;
-  ma.expanded_x = expanded_x;
-  ma.expanded_scale = opts->quant_mode == 1 ? expanded_scale : nullptr;
-  ma.expanded_row_idx = expanded_row_idx;
-  MOE_CUDA(launch_init_move(ma, stream));
-  InitFinishArgs fa{};
-  fa.count = ra.count;
-  fa.cumsum = ra.cumsum;
-  fa.sorted_row = ra.sorted_row;
-  fa.P = ra.P;
-  fa.E = s.E;
-  fa.H = s.H;
-  fa.C = opts->expert_capacity;
-  fa.drop_pad = opts->drop_pad;
-  fa.row_idx_type = opts->row_idx_type;
-  fa.tokens_num_type = opts->tokens_num_type;
-  fa.esize = opts->quant_mode == 1 ? 1 : 2;
-  fa.expanded_x = expanded_x;
-  fa.expanded_scale = ma.expanded_scale;
-  fa.expanded_row_idx = expanded_row_idx;
-  fa.tokens_out = tokens_cumsum_or_count;
-  MOE_CUDA(launch_init_finish(fa, stream, sms));
+  RouteArgs ra = route_args(s, L, static_cast<uint8_t*>(ws), expert_ids, num_rows);
+  MOE_CUDA(init_routing_enqueue(ra, base, range, shape, num_rows, x, expert_ids, opts, expanded_x, expanded_row_idx,
+                                tokens_cumsum_or_count, expanded_scale, sms, stream));
   return MOE_OK;
 }
 

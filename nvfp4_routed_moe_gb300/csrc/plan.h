@@ -5,6 +5,8 @@
 #include <cstdint>
 #include <cuda.h>
 
+#include "nvfp4moe.h"
+
 namespace moe {
 
 // Tile geometry (fixed by the kernels).
@@ -98,7 +100,9 @@ inline WsLayout make_layout(const Shape& s, int64_t max_tokens) {
 struct RouteArgs {
   const int32_t* ids;
   int64_t P;
-  int32_t k, E;
+  int32_t k, E;       // E: experts routed, ids id_base .. id_base + E - 1
+  int32_t id_base;    // first routed expert id
+  int32_t E_all;      // ids outside [0, E_all) are flagged as invalid; in-range ids outside the routed range are skipped silently
   int32_t* hdr;
   int32_t* count;
   int32_t* cumsum;
@@ -165,12 +169,35 @@ struct InitFinishArgs {
   const int32_t* count;
   const int32_t* cumsum;
   const int32_t* sorted_row;
-  int64_t P;
+  const int32_t* gather;    // sorted position of each pair, -1 if not routed
+  const int32_t* ids;
+  const int32_t* hdr;
+  int64_t P, active_num;
   int32_t E, H, C, drop_pad, row_idx_type, tokens_num_type, esize;
+  int32_t E_all, id_base;
+  int32_t gather_idx;       // write the gather form of expanded_row_idx here (row-driven move)
   void* expanded_x;
   float* expanded_scale;
   int32_t* expanded_row_idx;
   int32_t* tokens_out;
+  int32_t* available_out;   // [1] or null
+};
+
+// Row-driven init-routing move: one warp per moved row, every option.
+struct InitRowsArgs {
+  const uint16_t* x;
+  const int32_t* ids;
+  const int32_t* sorted_row;
+  const int32_t* count;
+  const int32_t* cumsum;
+  const int32_t* hdr;
+  int64_t T, active_num;
+  int32_t k, E, id_base, H, drop_pad, C, quant_mode;
+  const float* scale;       // quant -1: [T] or null; quant 0: [1]; quant 1: smooth [scale_rows, H] or null
+  int32_t scale_rows;
+  const float* offset;      // quant 0: [1]
+  void* expanded_x;
+  float* expanded_scale;
 };
 
 struct QuantXArgs {
@@ -204,5 +231,15 @@ struct PrepArgs {
   uint8_t *w13o, *sf13o, *w2o, *sf2o;
   int32_t H, I, E;
 };
+
+// Init-routing shared by moe_init_routing and moe_init_routing_static: the
+// host check of the options (fills the routed expert range) and the
+// launches that follow the routing arrays' placement in `ra`.
+moe_status_t init_routing_check(const moe_shape_t* shape, const moe_routing_opts_t* o, int32_t* base,
+                                int32_t* range);
+cudaError_t init_routing_enqueue(RouteArgs ra, int32_t base, int32_t range, const moe_shape_t* shape, int64_t T,
+                                 const void* x, const int32_t* ids, const moe_routing_opts_t* o, void* expanded_x,
+                                 int32_t* expanded_row_idx, int32_t* tokens_out, float* expanded_scale, int sms,
+                                 cudaStream_t st);
 
 }  // namespace moe

@@ -37,12 +37,12 @@ __device__ __forceinline__ uint32_t lanemask_lt() {
 
 // Pass 1: per-warp histogram of ids[begin, end) into hist_w[E] (shared).
 __device__ __forceinline__ void warp_histogram(const int32_t* ids, int64_t begin, int64_t end, int E,
-                                               int* hist_w) {
+                                               int* hist_w, int id_base) {
   const int lane = threadIdx.x & 31;
   for (int64_t base = begin; base < end; base += 32) {
     const int64_t f = base + lane;
     const bool in = f < end;
-    const int id = in ? ids[f] : -1;
+    const int id = in ? ids[f] - id_base : -1;
     const bool ok = in && id >= 0 && id < E;
     const uint32_t okmask = __ballot_sync(0xffffffffu, ok);
     if (ok) {
@@ -62,7 +62,8 @@ __device__ __forceinline__ int warp_rank(const RouteArgs& a, const int32_t* ids,
   for (int64_t base = begin; base < end; base += 32) {
     const int64_t f = base + lane;
     const bool in = f < end;
-    const int id = in ? ids[f] : -1;
+    const int raw = in ? ids[f] : -1;
+    const int id = raw - a.id_base;
     const bool ok = in && id >= 0 && id < a.E;
     const uint32_t okmask = __ballot_sync(0xffffffffu, ok);
     if (ok) {
@@ -79,7 +80,7 @@ __device__ __forceinline__ int warp_rank(const RouteArgs& a, const int32_t* ids,
     } else if (in) {
       a.gather[f] = -1;
       a.row_pos[f] = -1;
-      ++invalid;
+      if (raw < 0 || raw >= a.E_all) ++invalid;   // outside every expert; in-range ids outside E are skipped silently
     }
     __syncwarp();
   }
@@ -214,7 +215,7 @@ __global__ void __launch_bounds__(1024, 1) route_small_kernel(const RouteArgs a)
   __syncthreads();
   const int64_t per = (a.P + NHW - 1) / NHW;
   const int64_t b = min(a.P, (int64_t)warp * per), en = min(a.P, b + per);
-  if (warp < NHW) warp_histogram(s_ids, b, en, E, hist + warp * E);
+  if (warp < NHW) warp_histogram(s_ids, b, en, E, hist + warp * E, a.id_base);
   __syncthreads();
   for (int e = tid; e < E; e += 1024) {
     int run = 0;
@@ -258,7 +259,7 @@ __global__ void __launch_bounds__(256) route_hist_kernel(const RouteArgs a) {
   __syncthreads();
   const int64_t cb = (int64_t)blockIdx.x * a.chunk;
   const int64_t wb = cb + (int64_t)warp * (a.chunk / 8);
-  warp_histogram(a.ids, min(wb, a.P), min(wb + a.chunk / 8, a.P), E, hist + warp * E);
+  warp_histogram(a.ids, min(wb, a.P), min(wb + a.chunk / 8, a.P), E, hist + warp * E, a.id_base);
   __syncthreads();
   for (int e = tid; e < E; e += 256) {
     int s = 0;
@@ -309,7 +310,7 @@ __global__ void __launch_bounds__(256) route_rank_kernel(const RouteArgs a) {
   const int64_t cb = (int64_t)blockIdx.x * a.chunk;
   const int64_t wb = cb + (int64_t)warp * (a.chunk / 8);
   const int64_t b = min(wb, a.P), en = min(wb + a.chunk / 8, a.P);
-  warp_histogram(a.ids, b, en, E, hist + warp * E);
+  warp_histogram(a.ids, b, en, E, hist + warp * E, a.id_base);
   __syncthreads();
   for (int e = tid; e < E; e += 256) {
     int run = s_offs[e] + a.blockhist[(size_t)blockIdx.x * E + e];
@@ -408,16 +409,142 @@ __global__ void __launch_bounds__(256) init_move_kernel(const InitMoveArgs a) {
   }
 }
 
-// Histogram output (formula 3, count or inclusive cumsum), the scatter form of
-// expanded_row_idx (formula 2), and the zero fill of unfilled drop/pad slots.
+// Row-driven move ("npu_moe_init_routing_v2", formula 5 in scatter form:
+// expandedX[i] = quantResult[scatterRowIdx[i] // K]), for every option: one
+// warp per sorted position i of a routed pair; the row goes to position i
+// (dropless, i < the Active limit) or to slot e*C + rank (drop/pad).
+//   quant -1: bf16 copy; with a [T] scale the row's scale is its token's
+//   quant  0: q = rint(x*scale + offset) in fp32, saturated to [-128, 127]
+//   quant  1: xs = x * smooth row (of the pair's expert, or the one shared
+//             row, or 1); s = row_max|xs| / 127; q = rint(xs / s), +-127
+__global__ void __launch_bounds__(256) init_rows_kernel(const InitRowsArgs a) {
+  pdl_wait();
+  pdl_launch_dependents();
+  const int lane = threadIdx.x & 31;
+  const int64_t w0 = ((int64_t)blockIdx.x * 256 + threadIdx.x) >> 5, nw = ((int64_t)gridDim.x * 256) >> 5;
+  const int64_t avail = a.hdr[HDR_NVALID];
+  const int64_t nmove = (!a.drop_pad && a.active_num > 0 && a.active_num < avail) ? a.active_num : avail;
+  const int nvec = a.H / 8;   // 8 bf16 per 16-byte vector
+  for (int64_t i = w0; i < nmove; i += nw) {
+    const int f = a.sorted_row[i];
+    const int e = a.ids[f] - a.id_base;
+    int64_t dest = i;
+    if (a.drop_pad) {
+      const int r = (int)(i - (a.cumsum[e] - a.count[e]));
+      if (r >= a.C) continue;
+      dest = (int64_t)e * a.C + r;
+    }
+    const int64_t t = f / a.k;
+    const uint4* xv = reinterpret_cast<const uint4*>(a.x + t * a.H);
+    if (a.quant_mode == -1) {
+      uint4* dv = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.expanded_x) + dest * a.H);
+      for (int v = lane; v < nvec; v += 32) dv[v] = __ldg(xv + v);
+      if (lane == 0 && a.scale && a.expanded_scale) a.expanded_scale[dest] = __ldg(a.scale + t);
+      continue;
+    }
+    int8_t* drow = static_cast<int8_t*>(a.expanded_x) + dest * a.H;
+    if (a.quant_mode == 0) {
+      const float sc = __ldg(a.scale), of = __ldg(a.offset);
+      for (int v = lane; v < nvec; v += 32) {
+        const uint4 u = __ldg(xv + v);
+        const uint32_t wd[4] = {u.x, u.y, u.z, u.w};
+        uint32_t q[2] = {0u, 0u};
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const uint32_t bits = (j & 1) ? (wd[j >> 1] >> 16) : (wd[j >> 1] & 0xFFFFu);
+          float y = rintf(__fadd_rn(__fmul_rn(bf16_bits_to_f32(bits), sc), of));
+          y = fminf(fmaxf(y, -128.0f), 127.0f);
+          q[j >> 2] |= ((uint32_t)(int)y & 0xFFu) << (8 * (j & 3));
+        }
+        *reinterpret_cast<uint2*>(drow + v * 8) = make_uint2(q[0], q[1]);
+      }
+      continue;
+    }
+    const float* sm = (a.scale && a.scale_rows > 0) ? a.scale + (a.scale_rows == 1 ? 0 : (int64_t)e) * a.H : nullptr;
+    float amax = 0.0f;
+    for (int v = lane; v < nvec; v += 32) {
+      const uint4 u = __ldg(xv + v);
+      const uint32_t wd[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const uint32_t bits = (j & 1) ? (wd[j >> 1] >> 16) : (wd[j >> 1] & 0xFFFFu);
+        float x = bf16_bits_to_f32(bits);
+        if (sm) x = __fmul_rn(x, __ldg(sm + v * 8 + j));
+        amax = fmaxf(amax, fabsf(x));
+      }
+    }
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+    const float s = __fdiv_rn(amax, 127.0f);
+    for (int v = lane; v < nvec; v += 32) {
+      const uint4 u = __ldg(xv + v);
+      const uint32_t wd[4] = {u.x, u.y, u.z, u.w};
+      uint32_t q[2] = {0u, 0u};
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const uint32_t bits = (j & 1) ? (wd[j >> 1] >> 16) : (wd[j >> 1] & 0xFFFFu);
+        float x = bf16_bits_to_f32(bits);
+        if (sm) x = __fmul_rn(x, __ldg(sm + v * 8 + j));
+        int qi = 0;
+        if (s != 0.0f) qi = (int)fminf(fmaxf(rintf(__fdiv_rn(x, s)), -127.0f), 127.0f);
+        q[j >> 2] |= ((uint32_t)qi & 0xFFu) << (8 * (j & 3));
+      }
+      *reinterpret_cast<uint2*>(drow + v * 8) = make_uint2(q[0], q[1]);
+    }
+    if (lane == 0 && a.expanded_scale) a.expanded_scale[dest] = s;
+  }
+}
+
+// Histogram output (formula 3: inclusive cumsum or count over the routed
+// experts, or key_value rows), expanded_row_idx in scatter form (formula 2)
+// or -- after a row-driven move -- in gather form, availableIdxNum (formula
+// 6), and the zero fill of unfilled drop/pad slots.
 __global__ void __launch_bounds__(256) init_finish_kernel(const InitFinishArgs a) {
   pdl_wait();
   pdl_launch_dependents();
   const int64_t gtid = (int64_t)blockIdx.x * 256 + threadIdx.x;
   const int64_t nthr = (int64_t)gridDim.x * 256;
-  for (int64_t e = gtid; e < a.E; e += nthr) a.tokens_out[e] = a.tokens_num_type == 1 ? a.count[e] : a.cumsum[e];
-  if (a.row_idx_type == 1)
+  const int64_t avail = a.hdr[HDR_NVALID];
+  if (a.tokens_num_type == 2) {
+    // key_value: (expert id, count) of the routed experts with a non-zero count, in expert order, then zeros
+    if (blockIdx.x == 0) {
+      __shared__ int s_n;
+      if (threadIdx.x == 0) {
+        int n = 0;
+        for (int e = 0; e < a.E; ++e)
+          if (a.count[e] > 0) {
+            a.tokens_out[2 * n] = a.id_base + e;
+            a.tokens_out[2 * n + 1] = a.count[e];
+            ++n;
+          }
+        s_n = n;
+      }
+      __syncthreads();
+      for (int64_t j = 2 * (int64_t)s_n + threadIdx.x; j < 2 * (int64_t)a.E_all; j += 256) a.tokens_out[j] = 0;
+    }
+  } else {
+    for (int64_t e = gtid; e < a.E; e += nthr) a.tokens_out[e] = a.tokens_num_type == 1 ? a.count[e] : a.cumsum[e];
+  }
+  if (gtid == 0 && a.available_out) *a.available_out = (int32_t)avail;
+  if (a.row_idx_type == 1) {
     for (int64_t i = gtid; i < a.P; i += nthr) a.expanded_row_idx[i] = a.sorted_row[i];
+  } else if (a.gather_idx) {
+    const int64_t nmove = (!a.drop_pad && a.active_num > 0 && a.active_num < avail) ? a.active_num : avail;
+    for (int64_t f = gtid; f < a.P; f += nthr) {
+      const int g = a.gather[f];
+      int d = -1;
+      if (g >= 0) {
+        if (!a.drop_pad) {
+          d = g < nmove ? g : -1;
+        } else {
+          const int e = a.ids[f] - a.id_base;
+          const int r = g - (a.cumsum[e] - a.count[e]);
+          d = r < a.C ? e * a.C + r : -1;
+        }
+      }
+      a.expanded_row_idx[f] = d;
+    }
+  }
   if (a.drop_pad) {
     const int lane = threadIdx.x & 31;
     const int64_t gw = gtid >> 5, nw = nthr >> 5;
@@ -456,6 +583,14 @@ cudaError_t launch_init_move(const InitMoveArgs& a, cudaStream_t st) {
   void* kargs[] = {&args};
   const unsigned blocks = (unsigned)((a.T + 7) / 8);
   return launch_with_pdl((const void*)init_move_kernel, dim3(blocks ? blocks : 1), dim3(256), 0, st, kargs);
+}
+
+cudaError_t launch_init_rows(const InitRowsArgs& a, int64_t P, cudaStream_t st, int num_sms) {
+  InitRowsArgs args = a;
+  void* kargs[] = {&args};
+  const int64_t want = (P + 7) / 8;
+  const unsigned blocks = (unsigned)(want < (int64_t)num_sms * 8 ? want : (int64_t)num_sms * 8);
+  return launch_with_pdl((const void*)init_rows_kernel, dim3(blocks ? blocks : 1), dim3(256), 0, st, kargs);
 }
 
 cudaError_t launch_init_finish(const InitFinishArgs& a, cudaStream_t st, int num_sms) {

@@ -117,12 +117,9 @@ extern "C" moe_status_t moe_init_routing_static(const moe_shape_t* shape, int64_
   if (!x || !expert_ids || !opts || !expanded_x || !expanded_row_idx || !tokens_cumsum_or_count || num_rows < 1)
     return MOE_ERR_INVALID_ARG;
   if (num_rows > kStaticMaxPairs / shape->top_k) return MOE_ERR_WORKSPACE_TOO_SMALL;  // beyond the static scratch
-  if (opts->drop_pad != 0 && opts->drop_pad != 1) return MOE_ERR_INVALID_ARG;
-  if (opts->drop_pad && opts->expert_capacity < 1) return MOE_ERR_INVALID_ARG;
-  if (opts->row_idx_type != 0 && opts->row_idx_type != 1) return MOE_ERR_INVALID_ARG;
-  if (opts->tokens_num_type == 2 || opts->quant_mode == 0) return MOE_ERR_UNSUPPORTED;
-  if (opts->tokens_num_type != 0 && opts->tokens_num_type != 1) return MOE_ERR_INVALID_ARG;
-  if (opts->quant_mode != -1 && opts->quant_mode != 1) return MOE_ERR_INVALID_ARG;
+  int32_t base = 0, range = 0;
+  const moe_status_t ost = init_routing_check(shape, opts, &base, &range);
+  if (ost != MOE_OK) return ost;
   if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(expanded_x)) % 16 != 0)
     return MOE_ERR_INVALID_ARG;
 
@@ -156,43 +153,8 @@ extern "C" moe_status_t moe_init_routing_static(const moe_shape_t* shape, int64_
   ra.blockhist = reinterpret_cast<int32_t*>(w + L.blockhist);
   ra.chunk = kRouteChunk;
   ra.nblk = (int32_t)((ra.P + kRouteChunk - 1) / kRouteChunk);
-  int nl = 0;
-  if (launch_routing(ra, stream, &nl) != cudaSuccess) return MOE_ERR_CUDA;
-
-  InitMoveArgs ma{};
-  ma.x = static_cast<const uint16_t*>(x);
-  ma.ids = expert_ids;
-  ma.gather = ra.gather;
-  ma.offs = ra.offs;
-  ma.T = num_rows;
-  ma.k = k;
-  ma.E = E;
-  ma.H = shape->hidden;
-  ma.drop_pad = opts->drop_pad;
-  ma.C = opts->expert_capacity;
-  ma.quant_mode = opts->quant_mode;
-  ma.row_idx_type = opts->row_idx_type;
-  ma.expanded_x = expanded_x;
-  ma.expanded_scale = opts->quant_mode == 1 ? expanded_scale : nullptr;
-  ma.expanded_row_idx = expanded_row_idx;
-  if (launch_init_move(ma, stream) != cudaSuccess) return MOE_ERR_CUDA;
-
-  InitFinishArgs fa{};
-  fa.count = ra.count;
-  fa.cumsum = ra.cumsum;
-  fa.sorted_row = ra.sorted_row;
-  fa.P = ra.P;
-  fa.E = E;
-  fa.H = shape->hidden;
-  fa.C = opts->expert_capacity;
-  fa.drop_pad = opts->drop_pad;
-  fa.row_idx_type = opts->row_idx_type;
-  fa.tokens_num_type = opts->tokens_num_type;
-  fa.esize = opts->quant_mode == 1 ? 1 : 2;
-  fa.expanded_x = expanded_x;
-  fa.expanded_scale = ma.expanded_scale;
-  fa.expanded_row_idx = expanded_row_idx;
-  fa.tokens_out = tokens_cumsum_or_count;
-  if (launch_init_finish(fa, stream, sms) != cudaSuccess) return MOE_ERR_CUDA;
+  if (init_routing_enqueue(ra, base, range, shape, num_rows, x, expert_ids, opts, expanded_x, expanded_row_idx,
+                           tokens_cumsum_or_count, expanded_scale, sms, stream) != cudaSuccess)
+    return MOE_ERR_CUDA;
   return MOE_OK;
 }

@@ -83,10 +83,17 @@ def test_null_and_bad_args_rejected_without_device(L):
     st = L.moe_prepare_workspace(ctypes.byref(shp), None, 0, 16, None)
     assert st == 1
     p = ctypes.c_void_p(256)
-    for opts, want in ((api.moe_routing_opts_t(0, 0, 0, 2, 1), 2),     # key_value histogram
-                       (api.moe_routing_opts_t(0, 0, 0, 0, 0), 2),     # static int8
-                       (api.moe_routing_opts_t(1, 0, 0, 0, 1), 1),     # drop_pad without capacity
-                       (api.moe_routing_opts_t(0, 0, 3, 0, 1), 1)):    # bad row_idx_type
+    O = api.moe_routing_opts_t
+    for opts, want in ((O(0, 0, 0, 3, 1), 1),                          # no such histogram mode
+                       (O(0, 0, 0, 0, 0), 1),                          # static int8 without scale / offset
+                       (O(0, 0, 0, 0, 2), 1),                          # no such quant mode
+                       (O(1, 0, 0, 0, 1), 1),                          # drop_pad without capacity
+                       (O(0, 0, 3, 0, 1), 1),                          # bad row_idx_type
+                       (O(0, 0, 0, 0, 1, 5, 5), 1),                    # empty expert range
+                       (O(0, 0, 0, 0, 1, 4, 33), 1),                   # range past E
+                       (O(1, 8, 0, 0, 1, 4, 20), 1),                   # drop/pad needs every expert
+                       (O(0, 0, 0, 0, 1, 0, 0, 0, 256, 3), 1),         # smooth scale rows neither 1 nor the range
+                       (O(0, 0, 0, 2, 1, 4, 20), 3)):                  # valid options, workspace too small
         st = L.moe_init_routing(ctypes.byref(shp), 16, p, p, ctypes.byref(opts), p, p, p, None, p, 1 << 20, None)
         assert st == want
     assert L.moe_test_mma_fp4(p, p, p, p, 200, 256, p, p, None) == 1

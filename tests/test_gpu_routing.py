@@ -94,3 +94,125 @@ def test_routing_zero_rows_and_duplicates():
     ids[7] = [3, 3, 3, 3]          # duplicates within a row: still a stable sort by flat index
     _check(x, ids, E)
     _check(x, ids, E, drop_pad=1, C=3)
+
+
+# ------------------------------------------------- the op's remaining options
+# active_expert_range, active_num, key_value histogram, static int8, smooth
+# scale, carried token scale ("npu_moe_init_routing_v2", formulas 1-6).
+
+def _run_ex(x, ids, E, kw, static=False):
+    T, H = x.shape
+    k = ids.shape[1]
+    shp = api.shape(H, 128, E, k)
+    qm = kw.get("quant_mode", 1)
+    lo, hi = kw.get("expert_start", 0), kw.get("expert_end", 0) or E
+    R = hi - lo
+    rows = R * kw["expert_capacity"] if kw.get("drop_pad") else T * k
+    ex = torch.full((rows, H), 0x55, dtype=torch.int8, device="cuda") if qm != -1 else \
+        torch.full((rows, H), 0x5555, dtype=torch.int16, device="cuda")
+    ridx = torch.full((T * k,), -7, dtype=torch.int32, device="cuda")
+    ntok = 2 * E if kw.get("tokens_num_type") == 2 else R
+    tok = torch.full((ntok,), -9, dtype=torch.int32, device="cuda")
+    scale_out = torch.full((rows,), -1.0, dtype=torch.float32, device="cuda")
+    avail = torch.full((1,), -3, dtype=torch.int32, device="cuda")
+    sc = None if kw.get("scale") is None else dev(np.asarray(kw["scale"], np.float32))
+    of = None if kw.get("offset") is None else dev(np.asarray(kw["offset"], np.float32))
+    srows = sc.shape[0] if (sc is not None and qm == 1) else 0
+    opts = api.routing_opts(drop_pad=kw.get("drop_pad", 0), expert_capacity=kw.get("expert_capacity", 0),
+                            row_idx_type=kw.get("row_idx_type", 0), tokens_num_type=kw.get("tokens_num_type", 0),
+                            quant_mode=qm, expert_start=lo, expert_end=kw.get("expert_end", 0),
+                            active_num=kw.get("active_num", 0), scale=sc, scale_rows=srows, offset=of,
+                            available_out=avail)
+    xd, idd = dev(x, torch.bfloat16), dev(ids)
+    if static:
+        api.moe_init_routing_static(shp, T, xd, idd, opts, ex, ridx, tok, scale_out)
+        torch.cuda.synchronize()
+        st = None
+    else:
+        ws = torch.empty(api.moe_workspace_size(shp, T), dtype=torch.uint8, device="cuda")
+        api.moe_prepare_workspace(shp, ws, T)
+        api.moe_init_routing(shp, T, xd, idd, opts, ex, ridx, tok, scale_out, ws)
+        st = api.moe_read_status(ws)
+    return ex.cpu().numpy(), ridx.cpu().numpy(), tok.cpu().numpy(), scale_out.cpu().numpy(), int(avail.item()), st
+
+
+def _check_ex(x, ids, E, static=False, **kw):
+    ex, ridx, tok, sc, avail, st = _run_ex(x, ids, E, kw, static)
+    okw = {k: v for k, v in kw.items() if k not in ("expert_end",)}
+    if kw.get("expert_end"):
+        okw["expert_end"] = kw["expert_end"]
+    rex, rridx, rtok, rsc, ravail = oracle.init_routing_ex(x, ids, E, **okw)
+    assert avail == ravail
+    np.testing.assert_array_equal(ridx, rridx)
+    np.testing.assert_array_equal(tok.reshape(rtok.shape), rtok)
+    if kw.get("drop_pad"):
+        moved = rex.shape[0]
+    else:
+        an = kw.get("active_num", 0)
+        moved = min(an, ravail) if an > 0 else ravail
+    np.testing.assert_array_equal(ex[:moved].view(rex.dtype), rex[:moved])
+    if rsc is not None:
+        np.testing.assert_array_equal(sc[:moved], rsc[:moved])
+    return st
+
+
+def test_expert_range_on_the_routing_workload():
+    x = gen.draw_x(0, 4096, 3584)
+    ids = gen.draw_ids_uniform(0, 4096, 896, 16)
+    st = _check_ex(x, ids, 896, expert_start=100, expert_end=612)
+    assert st == (0, 0)          # ids outside the range are not errors
+
+
+@pytest.mark.parametrize("T,E,k,lo,hi", [(300, 64, 8, 5, 40), (1000, 128, 16, 0, 17), (3, 896, 16, 800, 896)])
+def test_expert_range_scatter_count_unquantized(T, E, k, lo, hi):
+    x = gen.draw_x(T, T, 512)
+    ids = gen.draw_ids_zipf(T, T, E, k)
+    _check_ex(x, ids, E, expert_start=lo, expert_end=hi, row_idx_type=1, tokens_num_type=1, quant_mode=-1)
+    _check_ex(x, ids, E, expert_start=lo, expert_end=hi, quant_mode=1)
+
+
+@pytest.mark.parametrize("lo,hi", [(0, 0), (300, 700)])
+def test_key_value_histogram(lo, hi):
+    x = gen.draw_x(7, 257, 512)
+    ids = gen.draw_ids_zipf(7, 257, 896, 16)
+    _check_ex(x, ids, 896, expert_start=lo, expert_end=hi, tokens_num_type=2)
+
+
+@pytest.mark.parametrize("row_idx_type", [0, 1])
+def test_active_num(row_idx_type):
+    x = gen.draw_x(8, 1000, 512)
+    ids = gen.draw_ids_uniform(8, 1000, 128, 16)
+    _check_ex(x, ids, 128, active_num=5000, row_idx_type=row_idx_type)
+    _check_ex(x, ids, 128, active_num=5000, expert_start=10, expert_end=90, quant_mode=-1)
+
+
+def test_static_int8():
+    x = gen.draw_x(9, 64, 512)
+    ids = gen.draw_ids_uniform(9, 64, 32, 4)
+    _check_ex(x, ids, 32, quant_mode=0, scale=[0.37], offset=[-1.5])
+    _check_ex(x, ids, 32, quant_mode=0, scale=[40.0], offset=[3.0], drop_pad=1, expert_capacity=6)
+
+
+def test_dynamic_int8_with_smooth_scale():
+    T, E, k, lo, hi = 200, 64, 8, 8, 40
+    x = gen.draw_x(10, T, 512)
+    ids = gen.draw_ids_zipf(10, T, E, k)
+    rs = np.random.default_rng(10)
+    shared = rs.uniform(0.2, 3.0, (1, 512)).astype(np.float32)
+    per_expert = rs.uniform(0.2, 3.0, (hi - lo, 512)).astype(np.float32)
+    _check_ex(x, ids, E, scale=shared)
+    _check_ex(x, ids, E, expert_start=lo, expert_end=hi, scale=per_expert)
+
+
+def test_unquantized_rows_carry_the_token_scale():
+    x = gen.draw_x(11, 40, 512)
+    ids = gen.draw_ids_uniform(11, 40, 32, 4)
+    s = np.arange(1, 41, dtype=np.float32) * 0.5
+    _check_ex(x, ids, 32, quant_mode=-1, scale=s)
+
+
+def test_options_through_the_workspace_free_entry_point():
+    x = gen.draw_x(12, 500, 512)
+    ids = gen.draw_ids_zipf(12, 500, 128, 16)
+    _check_ex(x, ids, 128, static=True, expert_start=20, expert_end=100, tokens_num_type=2)
+    _check_ex(x, ids, 128, static=True, quant_mode=0, scale=[2.0], offset=[0.25], active_num=3000)
