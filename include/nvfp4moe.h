@@ -107,6 +107,24 @@ moe_status_t moe_forward(const moe_shape_t* shape, int64_t num_tokens, const voi
                          const float* dA_dW2, const float* situ_beta, const float* situ_linear_beta, void* ws,
                          size_t ws_bytes, void* out, cudaStream_t stream);
 
+/* The forward over a contiguous slice of the experts, as one expert-parallel
+ * rank runs it ("npu_moe_init_routing_v2": active_expert_range, the
+ * EP-local routing of a rank's experts).  shape.num_experts is the slice
+ * size; w13/sf13/w2/sf2 and dX_dW13/qA/dA_dW2/situ_* hold the slice's
+ * experts, expert_begin .. expert_begin + num_experts - 1 (prepared with that
+ * shape).  expert_ids are global: pairs routed outside the slice contribute
+ * nothing here and are not errors (negative ids are still skipped and
+ * flagged).  out [T, H] bf16 = the rank's partial output, the route-weighted
+ * sum over its own experts only (zero for tokens with no pair on the rank);
+ * summing the ranks' partial outputs is the caller's collective.  Everything
+ * else is as in moe_forward; the workspace is prepared for shape. */
+moe_status_t moe_forward_local_experts(const moe_shape_t* shape, int32_t expert_begin, int64_t num_tokens,
+                                       const void* x, const int32_t* expert_ids, const void* route_weights,
+                                       const uint8_t* w13, const uint8_t* sf13, const uint8_t* w2, const uint8_t* sf2,
+                                       const float* qX, const float* dX_dW13, const float* qA, const float* dA_dW2,
+                                       const float* situ_beta, const float* situ_linear_beta, void* ws,
+                                       size_t ws_bytes, void* out, cudaStream_t stream);
+
 /* Options of moe_init_routing (torch_npu "npu_moe_init_routing_v2",
  * parameter list: drop_pad_mode, expert_capacity, row_idx_type,
  * expert_tokens_num_type, quant_mode, active_expert_range, active_num,

@@ -24,7 +24,7 @@ STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
 DEVSTAT_INVALID_EXPERT, DEVSTAT_TIMEOUT, DEVSTAT_BAD_TILE = 1, 2, 4
 
 EXPORTED = ["moe_workspace_size", "moe_prepared_weight_bytes", "moe_prepare_weights", "moe_prepare_workspace",
-            "moe_forward", "moe_init_routing", "moe_init_routing_static", "moe_read_status", "moe_status_string", "moe_test_codec_sweep",
+            "moe_forward", "moe_forward_local_experts", "moe_init_routing", "moe_init_routing_static", "moe_read_status", "moe_status_string", "moe_test_codec_sweep",
             "moe_test_quantize_rows", "moe_test_situ_requant", "moe_test_requant_lanes", "moe_test_mma_fp4",
             "moe_workspace_layout", "moe_forward_launch_count", "moe_profile_start", "moe_profile_stop"]
 
@@ -75,6 +75,7 @@ def lib():
         "moe_prepare_weights": [S] + [P] * 8 + [P],
         "moe_prepare_workspace": [S, P, sz, i64, P],
         "moe_forward": [S, i64] + [P] * 13 + [P, sz, P, P],
+        "moe_forward_local_experts": [S, i32, i64] + [P] * 13 + [P, sz, P, P],
         "moe_init_routing": [S, i64, P, P, ctypes.POINTER(moe_routing_opts_t), P, P, P, P, P, sz, P],
         "moe_init_routing_static": [S, i64, P, P, ctypes.POINTER(moe_routing_opts_t), P, P, P, P, P],
         "moe_read_status": [P, P, P],
@@ -153,6 +154,15 @@ def moe_forward(shp, num_tokens, x, expert_ids, route_weights, w13, sf13, w2, sf
     _check(lib().moe_forward(ctypes.byref(shp), num_tokens, _p(x), _p(expert_ids), _p(route_weights), _p(w13),
                              _p(sf13), _p(w2), _p(sf2), _p(qX), _p(dX_dW13), _p(qA), _p(dA_dW2), _p(situ_beta),
                              _p(situ_linear_beta), _p(ws), _nbytes(ws), _p(out), _stream(stream)), "moe_forward")
+
+
+def moe_forward_local_experts(shp, expert_begin: int, num_tokens: int, x, expert_ids, route_weights, w13, sf13, w2,
+                              sf2, qX, dX_dW13, qA, dA_dW2, situ_beta, situ_linear_beta, ws, out, stream=None):
+    _check(lib().moe_forward_local_experts(ctypes.byref(shp), expert_begin, num_tokens, _p(x), _p(expert_ids),
+                                           _p(route_weights), _p(w13), _p(sf13), _p(w2), _p(sf2), _p(qX),
+                                           _p(dX_dW13), _p(qA), _p(dA_dW2), _p(situ_beta), _p(situ_linear_beta),
+                                           _p(ws), _nbytes(ws), _p(out), _stream(stream)),
+           "moe_forward_local_experts")
 
 
 def routing_opts(drop_pad=0, expert_capacity=0, row_idx_type=0, tokens_num_type=0, quant_mode=1, expert_start=0,

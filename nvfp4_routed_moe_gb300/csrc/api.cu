@@ -1,6 +1,7 @@
 // api.cu -- the C ABI: host validation, workspace planning, tensor maps and
 // the launch sequence of the forward and of the standalone init-routing.
 #include <algorithm>
+#include <cstdint>
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
@@ -385,93 +386,13 @@ cudaError_t init_routing_enqueue(RouteArgs ra, int32_t base, int32_t range, cons
   return launch_init_finish(fa, st, sms);
 }
 
-}  // namespace moe
-
-using namespace moe;
-
-extern "C" {
-
-const char* moe_status_string(moe_status_t st) {
-  switch (st) {
-    case MOE_OK: return "MOE_OK";
-    case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG";
-    case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED";
-    case MOE_ERR_WORKSPACE_TOO_SMALL: return "MOE_ERR_WORKSPACE_TOO_SMALL";
-    case MOE_ERR_NOT_PREPARED: return "MOE_ERR_NOT_PREPARED";
-    case MOE_ERR_CUDA: return "MOE_ERR_CUDA";
-    case MOE_ERR_DEVICE_STATUS: return "MOE_ERR_DEVICE_STATUS";
-  }
-  return "MOE_ERR_UNKNOWN";
-}
-
-moe_status_t moe_workspace_size(const moe_shape_t* shape, int64_t max_tokens, size_t* bytes) {
-  moe_status_t st = shape_supported(shape);
-  if (st != MOE_OK) return st;
-  if (!bytes || max_tokens < 1) return MOE_ERR_INVALID_ARG;
-  if (max_tokens * shape->top_k >= ((int64_t)1 << 31) - (int64_t)kTileRows * kMaxExperts)
-    return MOE_ERR_UNSUPPORTED;
-  *bytes = make_layout(to_shape(shape), max_tokens).total;
-  return MOE_OK;
-}
-
-moe_status_t moe_prepared_weight_bytes(const moe_shape_t* shape, size_t* w13_bytes, size_t* sf13_bytes,
-                                       size_t* w2_bytes, size_t* sf2_bytes) {
-  moe_status_t st = shape_supported(shape);
-  if (st != MOE_OK) return st;
-  if (!w13_bytes || !sf13_bytes || !w2_bytes || !sf2_bytes) return MOE_ERR_INVALID_ARG;
-  const size_t E = shape->num_experts, H = shape->hidden, I = shape->inter;
-  *w13_bytes = E * 2 * I * (H / 2);
-  *sf13_bytes = E * 2 * I * (H / 16);
-  *w2_bytes = E * H * (I / 2);
-  *sf2_bytes = E * H * (I / 16);
-  return MOE_OK;
-}
-
-moe_status_t moe_prepare_weights(const moe_shape_t* shape, const uint8_t* w13, const uint8_t* sf13,
-                                 const uint8_t* w2, const uint8_t* sf2, uint8_t* w13_out, uint8_t* sf13_out,
-                                 uint8_t* w2_out, uint8_t* sf2_out, cudaStream_t stream) {
-  moe_status_t st = shape_supported(shape);
-  if (st != MOE_OK) return st;
-  if (!w13 || !sf13 || !w2 || !sf2 || !w13_out || !sf13_out || !w2_out || !sf2_out) return MOE_ERR_INVALID_ARG;
-  if (!aligned(w13, 16) || !aligned(w2, 16) || !aligned(w13_out, 256) || !aligned(w2_out, 256) ||
-      !aligned(sf13_out, 16) || !aligned(sf2_out, 16))
-    return MOE_ERR_INVALID_ARG;
-  int sms = 0;
-  MOE_CUDA(device_ready(&sms));
-  PrepArgs a{w13, sf13, w2, sf2, w13_out, sf13_out, w2_out, sf2_out, shape->hidden, shape->inter,
-             shape->num_experts};
-  MOE_CUDA(launch_prep(a, stream, sms));
-  return MOE_OK;
-}
-
-moe_status_t moe_prepare_workspace(const moe_shape_t* shape, void* ws, size_t ws_bytes, int64_t num_tokens,
-                                   cudaStream_t stream) {
-  moe_status_t st = shape_supported(shape);
-  if (st != MOE_OK) return st;
-  if (!ws || num_tokens < 1 || !aligned(ws, 256)) return MOE_ERR_INVALID_ARG;
-  const Shape s = to_shape(shape);
-  const int64_t cap = capacity_tokens(s, ws_bytes);
-  if (cap < num_tokens) return MOE_ERR_WORKSPACE_TOO_SMALL;
-  const WsLayout L = make_layout(s, cap);
-  int sms = 0;
-  MOE_CUDA(device_ready(&sms));
-  uint8_t* w = static_cast<uint8_t*>(ws);
-  MOE_CUDA(cudaMemsetAsync(w + L.header, 0, HDR_WORDS * 4, stream));
-  fill_f32_kernel<<<4, 256, 0, stream>>>(reinterpret_cast<float*>(w + L.beta_def), s.E, 4.0f);
-  fill_f32_kernel<<<4, 256, 0, stream>>>(reinterpret_cast<float*>(w + L.lam_def), s.E, 25.0f);
-  MOE_CUDA(cudaGetLastError());
-  if (!is_prepared(ws, ws_bytes, num_tokens, s)) {
-    std::lock_guard<std::mutex> lock(g_mu);
-    g_prepared.push_back(PreparedEntry{ws, ws_bytes, num_tokens, s});
-  }
-  return MOE_OK;
-}
-
-moe_status_t moe_forward(const moe_shape_t* shape, int64_t num_tokens, const void* x, const int32_t* expert_ids,
-                         const void* route_weights, const uint8_t* w13, const uint8_t* sf13, const uint8_t* w2,
-                         const uint8_t* sf2, const float* qX, const float* dX_dW13, const float* qA,
-                         const float* dA_dW2, const float* situ_beta, const float* situ_linear_beta, void* ws,
-                         size_t ws_bytes, void* out, cudaStream_t stream) {
+static moe_status_t forward_impl(const moe_shape_t* shape, int32_t expert_begin, int32_t id_limit,
+                                 int64_t num_tokens, const void* x, const int32_t* expert_ids,
+                                 const void* route_weights, const uint8_t* w13, const uint8_t* sf13,
+                                 const uint8_t* w2, const uint8_t* sf2, const float* qX, const float* dX_dW13,
+                                 const float* qA, const float* dA_dW2, const float* situ_beta,
+                                 const float* situ_linear_beta, void* ws, size_t ws_bytes, void* out,
+                                 cudaStream_t stream) {
   moe_status_t st = shape_supported(shape);
   if (st != MOE_OK) return st;
   if (!x || !expert_ids || !route_weights || !w13 || !sf13 || !w2 || !sf2 || !qX || !dX_dW13 || !qA || !dA_dW2 ||
@@ -513,6 +434,8 @@ moe_status_t moe_forward(const moe_shape_t* shape, int64_t num_tokens, const voi
   // 1. routing
   prof_mark(0, stream);
   RouteArgs ra = route_args(s, L, w, expert_ids, T);
+  ra.id_base = expert_begin;
+  ra.E_all = id_limit;
   int nl = 0;
   MOE_CUDA(launch_routing(ra, stream, &nl));
 
@@ -601,6 +524,111 @@ moe_status_t moe_forward(const moe_shape_t* shape, int64_t num_tokens, const voi
 
   prof_end_call(stream);
   return MOE_OK;
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+const char* moe_status_string(moe_status_t st) {
+  switch (st) {
+    case MOE_OK: return "MOE_OK";
+    case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG";
+    case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED";
+    case MOE_ERR_WORKSPACE_TOO_SMALL: return "MOE_ERR_WORKSPACE_TOO_SMALL";
+    case MOE_ERR_NOT_PREPARED: return "MOE_ERR_NOT_PREPARED";
+    case MOE_ERR_CUDA: return "MOE_ERR_CUDA";
+    case MOE_ERR_DEVICE_STATUS: return "MOE_ERR_DEVICE_STATUS";
+  }
+  return "MOE_ERR_UNKNOWN";
+}
+
+moe_status_t moe_workspace_size(const moe_shape_t* shape, int64_t max_tokens, size_t* bytes) {
+  moe_status_t st = shape_supported(shape);
+  if (st != MOE_OK) return st;
+  if (!bytes || max_tokens < 1) return MOE_ERR_INVALID_ARG;
+  if (max_tokens * shape->top_k >= ((int64_t)1 << 31) - (int64_t)kTileRows * kMaxExperts)
+    return MOE_ERR_UNSUPPORTED;
+  *bytes = make_layout(to_shape(shape), max_tokens).total;
+  return MOE_OK;
+}
+
+moe_status_t moe_prepared_weight_bytes(const moe_shape_t* shape, size_t* w13_bytes, size_t* sf13_bytes,
+                                       size_t* w2_bytes, size_t* sf2_bytes) {
+  moe_status_t st = shape_supported(shape);
+  if (st != MOE_OK) return st;
+  if (!w13_bytes || !sf13_bytes || !w2_bytes || !sf2_bytes) return MOE_ERR_INVALID_ARG;
+  const size_t E = shape->num_experts, H = shape->hidden, I = shape->inter;
+  *w13_bytes = E * 2 * I * (H / 2);
+  *sf13_bytes = E * 2 * I * (H / 16);
+  *w2_bytes = E * H * (I / 2);
+  *sf2_bytes = E * H * (I / 16);
+  return MOE_OK;
+}
+
+moe_status_t moe_prepare_weights(const moe_shape_t* shape, const uint8_t* w13, const uint8_t* sf13,
+                                 const uint8_t* w2, const uint8_t* sf2, uint8_t* w13_out, uint8_t* sf13_out,
+                                 uint8_t* w2_out, uint8_t* sf2_out, cudaStream_t stream) {
+  moe_status_t st = shape_supported(shape);
+  if (st != MOE_OK) return st;
+  if (!w13 || !sf13 || !w2 || !sf2 || !w13_out || !sf13_out || !w2_out || !sf2_out) return MOE_ERR_INVALID_ARG;
+  if (!aligned(w13, 16) || !aligned(w2, 16) || !aligned(w13_out, 256) || !aligned(w2_out, 256) ||
+      !aligned(sf13_out, 16) || !aligned(sf2_out, 16))
+    return MOE_ERR_INVALID_ARG;
+  int sms = 0;
+  MOE_CUDA(device_ready(&sms));
+  PrepArgs a{w13, sf13, w2, sf2, w13_out, sf13_out, w2_out, sf2_out, shape->hidden, shape->inter,
+             shape->num_experts};
+  MOE_CUDA(launch_prep(a, stream, sms));
+  return MOE_OK;
+}
+
+moe_status_t moe_prepare_workspace(const moe_shape_t* shape, void* ws, size_t ws_bytes, int64_t num_tokens,
+                                   cudaStream_t stream) {
+  moe_status_t st = shape_supported(shape);
+  if (st != MOE_OK) return st;
+  if (!ws || num_tokens < 1 || !aligned(ws, 256)) return MOE_ERR_INVALID_ARG;
+  const Shape s = to_shape(shape);
+  const int64_t cap = capacity_tokens(s, ws_bytes);
+  if (cap < num_tokens) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  const WsLayout L = make_layout(s, cap);
+  int sms = 0;
+  MOE_CUDA(device_ready(&sms));
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  MOE_CUDA(cudaMemsetAsync(w + L.header, 0, HDR_WORDS * 4, stream));
+  fill_f32_kernel<<<4, 256, 0, stream>>>(reinterpret_cast<float*>(w + L.beta_def), s.E, 4.0f);
+  fill_f32_kernel<<<4, 256, 0, stream>>>(reinterpret_cast<float*>(w + L.lam_def), s.E, 25.0f);
+  MOE_CUDA(cudaGetLastError());
+  if (!is_prepared(ws, ws_bytes, num_tokens, s)) {
+    std::lock_guard<std::mutex> lock(g_mu);
+    g_prepared.push_back(PreparedEntry{ws, ws_bytes, num_tokens, s});
+  }
+  return MOE_OK;
+}
+
+moe_status_t moe_forward(const moe_shape_t* shape, int64_t num_tokens, const void* x, const int32_t* expert_ids,
+                         const void* route_weights, const uint8_t* w13, const uint8_t* sf13, const uint8_t* w2,
+                         const uint8_t* sf2, const float* qX, const float* dX_dW13, const float* qA,
+                         const float* dA_dW2, const float* situ_beta, const float* situ_linear_beta, void* ws,
+                         size_t ws_bytes, void* out, cudaStream_t stream) {
+  if (!shape) return MOE_ERR_INVALID_ARG;
+  return forward_impl(shape, 0, shape->num_experts, num_tokens, x, expert_ids, route_weights, w13, sf13, w2, sf2, qX,
+                      dX_dW13, qA, dA_dW2, situ_beta, situ_linear_beta, ws, ws_bytes, out, stream);
+}
+
+moe_status_t moe_forward_local_experts(const moe_shape_t* shape, int32_t expert_begin, int64_t num_tokens,
+                                       const void* x, const int32_t* expert_ids, const void* route_weights,
+                                       const uint8_t* w13, const uint8_t* sf13, const uint8_t* w2, const uint8_t* sf2,
+                                       const float* qX, const float* dX_dW13, const float* qA, const float* dA_dW2,
+                                       const float* situ_beta, const float* situ_linear_beta, void* ws,
+                                       size_t ws_bytes, void* out, cudaStream_t stream) {
+  if (!shape || expert_begin < 0 || (int64_t)expert_begin + shape->num_experts > (int64_t)INT32_MAX)
+    return MOE_ERR_INVALID_ARG;
+  // negative ids are flagged; ids past the slice belong to other ranks
+  return forward_impl(shape, expert_begin, INT32_MAX, num_tokens, x, expert_ids, route_weights, w13, sf13, w2, sf2,
+                      qX, dX_dW13, qA, dA_dW2, situ_beta, situ_linear_beta, ws, ws_bytes, out, stream);
 }
 
 moe_status_t moe_init_routing(const moe_shape_t* shape, int64_t num_rows, const void* x, const int32_t* expert_ids,

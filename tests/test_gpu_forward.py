@@ -281,3 +281,53 @@ def test_full_shape_sampled_tokens(full_model, T, routing, big):
     counts = np.bincount(inp.expert_ids.ravel(), minlength=inp.E)
     lay = ws_view(m, ws)
     np.testing.assert_array_equal(ws_i32(ws, lay.count, inp.E), counts)
+
+
+# ------------------------------------------------------------- expert slices
+# The forward of one expert-parallel rank ("npu_moe_init_routing_v2",
+# active_expert_range): the rank holds experts [begin, begin + E_local) and
+# returns the route-weighted sum over them only.  The oracle is the same
+# forward with the ids shifted by -begin (ids outside [0, E_local) are not
+# routed) and the slice's weights and scales.
+
+def _slice(inp, begin, n):
+    s = gen.MoEInputs(inp.H, inp.I, n, inp.k, inp.T, inp.x, inp.expert_ids - begin, inp.route_weights, inp.qX)
+    s.w13, s.sf13, s.w2, s.sf2 = (a[begin:begin + n] for a in (inp.w13, inp.sf13, inp.w2, inp.sf2))
+    s.dXdW13, s.qA, s.dAdW2 = (a[begin:begin + n] for a in (inp.dXdW13, inp.qA, inp.dAdW2))
+    return s
+
+
+def _local_forward(inp_slice, begin, global_ids):
+    m = Model(inp_slice)
+    T = inp_slice.T
+    ws = m.workspace(T)
+    api.moe_prepare_workspace(m.shape, ws, T)
+    out = torch.empty((T, inp_slice.H), dtype=torch.bfloat16, device="cuda")
+    api.moe_forward_local_experts(m.shape, begin, T, dev(inp_slice.x, torch.bfloat16), dev(global_ids),
+                                  dev(inp_slice.route_weights, torch.bfloat16), m.w13, m.sf13, m.w2, m.sf2,
+                                  dev(np.array([inp_slice.qX], np.float32)), m.dXdW13, m.qA, m.dAdW2, None, None,
+                                  ws, out)
+    torch.cuda.synchronize()
+    return out, ws
+
+
+@pytest.mark.parametrize("begin,n", [(0, 16), (16, 16), (5, 11)])
+def test_local_expert_slice_tiny(begin, n):
+    inp = cases.prepare_tiny(0, T=40)
+    sl = _slice(inp, begin, n)
+    out, ws = _local_forward(sl, begin, inp.expert_ids)
+    assert api.moe_read_status(ws) == (0, 0)       # pairs of other ranks are not errors
+    assert_close(out_bits(out), cases.run_oracle(sl), f"slice {begin}+{n}")
+
+
+def test_local_expert_slices_sum_to_the_full_forward():
+    inp = gen.full(21, T=16, routing="uniform", weights=True)
+    full = cases.run_oracle(inp)
+    total = np.zeros((inp.T, inp.H), np.float64)
+    for begin in (0, 448):
+        sl = _slice(inp, begin, 448)
+        out, _ = _local_forward(sl, begin, inp.expert_ids)
+        part = out_bits(out)
+        assert_close(part, cases.run_oracle(sl), f"slice {begin}")
+        total += gen.bf16_bits_to_f32(part)
+    assert_close(gen.f32_to_bf16_bits(total.astype(np.float32)), full, "sum of slices")
