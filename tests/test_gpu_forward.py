@@ -263,6 +263,26 @@ def test_full_shape_decode_all_tokens(full_model, T):
     assert_close(out_bits(out), ref, f"decode T={T}")
 
 
+@pytest.mark.parametrize("T", [16, 2048])
+def test_full_shape_per_expert_situ_parameters(full_model, T):
+    """Non-default per-expert gate and linear smoothing ("Cake SiTU backend":
+    situ_beta / situ_linear_beta, float32 [896]) at full shape: every token
+    at decode size, sampled tokens at T=2048."""
+    minp, m = full_model
+    inp = _full_case(minp, T, "uniform", seed=40 + T)
+    rs = np.random.default_rng(T)
+    beta = rs.uniform(1.0, 8.0, inp.E).astype(np.float32)
+    lam = rs.uniform(2.0, 60.0, inp.E).astype(np.float32)
+    out, ws = m.forward_inputs(inp, beta=dev(beta), lam=dev(lam))
+    torch.cuda.synchronize()
+    assert api.moe_read_status(ws) == (0, 0)
+    toks = np.arange(T) if T <= 16 else np.unique(np.concatenate([[0, T - 1], rs.choice(T, 14, replace=False)]))
+    ref = cases.run_oracle(inp, tokens=toks, beta=beta, lam=lam)
+    assert_close(out_bits(out)[toks], ref, f"situ params T={T}")
+    default = cases.run_oracle(inp, tokens=toks[:4])
+    assert not np.array_equal(ref[:4], default)      # the parameters do change the result
+
+
 @pytest.mark.parametrize("T,routing,big", [(512, "uniform", 0.0), (4096, "zipf", 0.0), (16384, "uniform", 0.01)])
 def test_full_shape_sampled_tokens(full_model, T, routing, big):
     minp, m = full_model
