@@ -111,6 +111,20 @@ def traffic_from_profile(kernel, workload):
     return None
 
 
+def job_throughput(ms_local: float, tokens_per_rank: int, steps: int, world: int, device: str = "cuda"):
+    """Whole-job throughput of a replicated run: every rank times its own
+    steps; the job's time is the slowest rank's (all-reduce MAX when
+    world > 1) and the job processed world * tokens_per_rank * steps tokens.
+    Returns (max_ms, tokens/s)."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms_local], dtype=torch.float64, device=device)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    ms = float(t.item())
+    return ms, world * tokens_per_rank * steps / (ms / 1e3)
+
+
 class ClockSampler:
     """nvidia-smi clock samples every 200 ms in a background process."""
 
@@ -317,12 +331,8 @@ def main():
         stage_ms, ncalls = api.moe_profile_stop()
         stage = {k: v / max(ncalls, 1) for k, v in stage_ms.items()}
     clk = clocks.stop()
-    ms_t = torch.tensor([ms], dtype=torch.float64, device="cuda")
-    if world > 1:
-        dist.all_reduce(ms_t, op=dist.ReduceOp.MAX)
-    ms = float(ms_t.item())
+    ms, value = job_throughput(ms, T, args.steps, world)
     ms_per_step = ms / args.steps
-    value = world * T * args.steps / (ms / 1e3)
     launches = api.moe_forward_launch_count(shp, T) * args.steps
 
     # ------------------------------------------------------------ end to end
@@ -351,10 +361,7 @@ def main():
         out_h.copy_(out, non_blocking=True)
     e1.record()
     torch.cuda.synchronize()
-    e2e_ms = torch.tensor([e0.elapsed_time(e1)], dtype=torch.float64, device="cuda")
-    if world > 1:
-        dist.all_reduce(e2e_ms, op=dist.ReduceOp.MAX)
-    e2e_val = world * T * e2e_steps / (float(e2e_ms.item()) / 1e3)
+    _, e2e_val = job_throughput(e0.elapsed_time(e1), T, e2e_steps, world)
     h2d = x_h.numel() * 2 + ids_h.numel() * 4 + rw_h.numel() * 2
     d2h = out_h.numel() * 2
     assert torch.equal(out_h.view(torch.int16), out.cpu().view(torch.int16))
