@@ -60,8 +60,10 @@ moe_status_t moe_test_mma_fp4(const uint8_t* a, const uint8_t* sfa_atoms, const 
 /* Byte offsets of the internal workspace regions of a workspace of ws_bytes
  * (its carve-up depends only on the shape and its size), for inspection of
  * intermediates in tests (host out struct).  Routing arrays are int32;
- * xq/aq are packed codes of padded expanded rows ([rows, H/2] / [rows, I/2]);
- * sfx/sfa are their block scales in the 128x4 atom layout; row_pos maps a
+ * xq holds the packed X codes once per token ([tokens, H/2]; FC1 gathers them
+ * per tile row), aq the packed A codes of the padded expanded rows
+ * ([rows, I/2]); sfx/sfa are the block scales of the padded expanded rows
+ * (X and A) in the 128x4 atom layout; row_pos maps a
  * flat pair t*k+j to its padded row; acc [tokens, H] fp32 is the FC2
  * combine accumulator (route-weighted sums before the BF16 rounding). */
 typedef struct {

@@ -33,7 +33,7 @@ cudaError_t launch_situ_requant(const float* z, int64_t rows, int I, float qA, f
 cudaError_t launch_requant_lanes(const float* act, int64_t rows, int I, float qA, uint8_t* packed, uint8_t* sf,
                                  cudaStream_t st);
 cudaError_t gemm_set_attributes();
-cudaError_t launch_fc1(const CUtensorMap& w13, const RowMaps& xq, const Fc1Args& a, int pair, int grid,
+cudaError_t launch_fc1(const CUtensorMap& w13, const Fc1Args& a, int pair, int grid,
                        cudaStream_t st);
 cudaError_t launch_fc2(const CUtensorMap& w2, const RowMaps& aq, const Fc2Args& a, int grid, cudaStream_t st);
 cudaError_t launch_mma_check(const CUtensorMap& a, const CUtensorMap& b, const uint8_t* sfa, const uint8_t* sfb,
@@ -413,15 +413,13 @@ static moe_status_t forward_impl(const moe_shape_t* shape, int32_t expert_begin,
   const int NIT = s.I / 64, NKB = s.H / kFc1KBlock, NMT = s.H / 128, NKB2 = s.I / kFc2KBlock;
 
   CUtensorMap tm_w13, tm_w2;
-  RowMaps tm_xq, tm_aq;
+  RowMaps tm_aq;
   {
     const uint64_t d[3] = {128, 128, (uint64_t)s.E * NIT * NKB};
     const uint64_t str[2] = {128, 16384};
     const uint32_t box[3] = {128, 128, 1};
     if (!make_map(&tm_w13, w13, 3, d, str, box, CU_TENSOR_MAP_SWIZZLE_128B)) return MOE_ERR_CUDA;
   }
-  if (!make_row_maps(&tm_xq, w + L.xq, (uint64_t)s.H / 2, (uint64_t)L.PpadMax, 128, CU_TENSOR_MAP_SWIZZLE_128B))
-    return MOE_ERR_CUDA;
   {
     const uint64_t d[3] = {64, 128, (uint64_t)s.E * NMT * NKB2};
     const uint64_t str[2] = {64, 8192};
@@ -439,7 +437,7 @@ static moe_status_t forward_impl(const moe_shape_t* shape, int32_t expert_begin,
   int nl = 0;
   MOE_CUDA(launch_routing(ra, stream, &nl));
 
-  // 2. quantize X into the padded expanded rows
+  // 2. quantize X (token-major codes; block scales into the padded rows' atoms)
   QuantXArgs qa{};
   qa.x = static_cast<const uint16_t*>(x);
   qa.row_pos = ra.row_pos;
@@ -475,6 +473,10 @@ static moe_status_t forward_impl(const moe_shape_t* shape, int32_t expert_begin,
   const int64_t tt = tt_bound(P, s.E);
   Fc1Args f1{};
   f1.sf13p = sf13;
+  f1.xq = w + L.xq;
+  f1.prow_pair = ra.prow_pair;
+  f1.k = s.k;
+  f1.num_pairs = P;
   f1.sfx = w + L.sfx;
   f1.tt_list = ra.tt_list;
   f1.hdr = ra.hdr;
@@ -493,7 +495,7 @@ static moe_status_t forward_impl(const moe_shape_t* shape, int32_t expert_begin,
   const int pair = fc1_pair(s, T);
   const int grid1 = (int)std::min<int64_t>(sms, tt * (s.I / 64 / pair));
   prof_mark(2, stream);
-  MOE_CUDA(launch_fc1(tm_w13, tm_xq, f1, pair, grid1, stream));
+  MOE_CUDA(launch_fc1(tm_w13, f1, pair, grid1, stream));
 
   // 4. FC2 with the route-weighted combine into the fp32 accumulator
   Fc2Args f2{};

@@ -44,7 +44,7 @@ cudaError_t launch_with_pdl(const void* fn, dim3 grid, dim3 block, size_t smem, 
 
 constexpr uint32_t kTmemCols = 512;
 
-// FC1 stage: X [128 tokens x 128 B] | W [PAIR tiles of 128 interleaved
+// FC1 stage: X [128 tokens x 128 B, gathered] | W [PAIR tiles of 128 interleaved
 // gate/up rows x 128 B] | X scale atoms | W scale atoms (4 of 512 B per tile).
 // PAIR = 2 shares the X tile and its atoms between two W13 tiles (single-
 // buffered accumulators); PAIR = 1 keeps double-buffered accumulators and a
@@ -62,11 +62,12 @@ static_assert(Fc1Cfg<1>::kBufs * 128 + Fc1Cfg<1>::kStages * Fc1Cfg<1>::kSfCols <
                   Fc1Cfg<2>::kBufs * 256 + Fc1Cfg<2>::kStages * Fc1Cfg<2>::kSfCols <= 512,
               "FC1 TMEM plan");
 constexpr int kFc1EpiWarps = 16;
-// FC1 warps: 2 TMA producer, 3 MMA issuer and TMEM owner, 4.. epilogue (0 and
-// 1 idle).  TMEM lane quarter q is read by warps w with w % 4 == q, which share
-// a scheduler; tiles fill the low quarters first, so the two issuing warps sit
-// on the schedulers of quarters 2 and 3.
+// FC1 warps: 0 and 1 gather X rows, 2 TMA producer, 3 MMA issuer and TMEM
+// owner, 4.. epilogue.  TMEM lane quarter q is read by warps w with
+// w % 4 == q, which share a scheduler; tiles fill the low quarters first, so
+// the two issuing warps sit on the schedulers of quarters 2 and 3.
 constexpr int kFc1Producer = 2, kFc1Mma = 3, kFc1Epi0 = 4;
+constexpr int kFc1Gather = 32 * kFc1Producer;   // gather threads (warps 0 and 1)
 constexpr int kFc1Threads = 32 * (kFc1Epi0 + kFc1EpiWarps);
 // FC2 shared memory: barriers (1 KB) | two activation slots (a token tile's
 // A codes [I/128 k-blocks][128 rows x 64 B] + its I/64 scale atoms) | ring of
@@ -132,10 +133,10 @@ __device__ __forceinline__ uint8_t* aligned_smem(uint8_t* raw) {
 __device__ __forceinline__ uint64_t sf_desc(const uint8_t* p) { return smem_desc(smem_u32(p), 0, 128, kLayoutNone); }
 
 template <int STAGES, int EPI_WARPS>
-__device__ void gemm_setup(Barriers* bars, int warp, int tmem_warp) {
+__device__ void gemm_setup(Barriers* bars, int warp, int tmem_warp, uint32_t full_arrivals = 1) {
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&bars->full[s], 1);
+      mbar_init(&bars->full[s], full_arrivals);
       mbar_init(&bars->empty[s], 1);
     }
     for (int b = 0; b < kMaxAccSlots; ++b) {
@@ -239,20 +240,16 @@ __device__ __forceinline__ uint32_t quant16_even(const uint32_t (&lo)[16], const
 // ================================================================== FC1
 template <int PAIR>
 __global__ void __launch_bounds__(kFc1Threads, 1)
-    fc1_kernel(const __grid_constant__ CUtensorMap tm_w13, const __grid_constant__ RowMaps tm_xq,
-               const Fc1Args p) {
+    fc1_kernel(const __grid_constant__ CUtensorMap tm_w13, const Fc1Args p) {
   using C = Fc1Cfg<PAIR>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = aligned_smem(smem_raw);
   Barriers* bars = reinterpret_cast<Barriers*>(smem + C::kStages * C::kStage);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int NIT = p.I / 64, NP = NIT / PAIR, NKB = p.H / kFc1KBlock;
-  if (warp == kFc1Producer && lane == 0) {
-    tma_prefetch_desc(&tm_w13);
-    tma_prefetch_desc(&tm_xq.m16);
-    tma_prefetch_desc(&tm_xq.m128);
-  }
-  gemm_setup<C::kStages, kFc1EpiWarps>(bars, warp, kFc1Mma);
+  if (warp == kFc1Producer && lane == 0) tma_prefetch_desc(&tm_w13);
+  // a stage is full once the producer's copies and every gather thread's rows have landed
+  gemm_setup<C::kStages, kFc1EpiWarps>(bars, warp, kFc1Mma, 1u + kFc1Gather);
   const uint32_t tmem = bars->tmem_base;
   pdl_wait();
   pdl_launch_dependents();
@@ -260,7 +257,59 @@ __global__ void __launch_bounds__(kFc1Threads, 1)
   const int4* tiles = reinterpret_cast<const int4*>(p.tt_list);
 
   if (warp < kFc1Producer) {
-    // idle
+    // -------------------------------------------------------------- gather
+    // The tile's X rows come from the token-major codes: row r of the tile is
+    // routed pair prow_pair[row0 + r], i.e. token pair / k.  Eight lanes copy
+    // one row's 128-byte k-block slice as 16-byte chunks (chunk c to position
+    // c ^ (r % 8) of the 128B-swizzled row), so one warp instruction moves four
+    // whole lines; thread (warp w, lane l) takes rows 8i + 4w + l/8, i < 16.
+    // Rows past the tile's fill are not copied (their outputs are discarded).
+    const int c = lane & 7, rsub = (warp << 2) + (lane >> 3);
+    const uint32_t dst0 = (uint32_t)(rsub * 128 + ((c ^ rsub) << 4));
+    const size_t H2 = (size_t)p.H / 2;
+    // The next unit's pair indices are loaded a unit ahead and only turned
+    // into token rows when that unit starts, so their latency stays hidden.
+    auto pairs = [&](const int4& t, int (&f)[16]) {
+      const bool ok = tile_ok(t, p.E, p.max_rows);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const int r = 8 * i + rsub;
+        f[i] = (ok && r < t.z) ? __ldg(p.prow_pair + t.y + r) : -1;
+      }
+    };
+    uint32_t stage = 0, phase = 0;
+    bool ok = true;
+    int4 nxt = next_tile(tiles, blockIdx.x, num_units, NP);
+    int4 nxt2 = next_tile(tiles, blockIdx.x + gridDim.x, num_units, NP);
+    int f_nxt[16];
+    pairs(nxt, f_nxt);
+    for (int unit = blockIdx.x; unit < num_units && ok; unit += gridDim.x) {
+      const int4 tl = nxt;
+      int tok[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) tok[i] = (f_nxt[i] >= 0 && f_nxt[i] < p.num_pairs) ? f_nxt[i] / p.k : -1;
+      nxt = nxt2;
+      nxt2 = next_tile(tiles, unit + 2 * gridDim.x, num_units, NP);
+      pairs(nxt, f_nxt);                                      // in flight while this unit streams
+      if (!tile_ok(tl, p.E, p.max_rows)) continue;
+      for (int kb = 0; kb < NKB; ++kb) {
+        if (!wait_or_abort(&bars->empty[stage], phase ^ 1u, bars, p.status)) {
+          ok = false;
+          break;
+        }
+        uint8_t* xs = smem + stage * C::kStage + C::kX + dst0;
+        const uint8_t* src = p.xq + (size_t)kb * 128 + c * 16;
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          if (tok[i] >= 0) cp_async16(xs + i * 1024, src + (size_t)tok[i] * H2);
+        cp_async_mbar_arrive(&bars->full[stage]);
+        if (++stage == C::kStages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+    cp_async_wait_all();   // every issued copy has landed before the CTA may exit
   } else if (warp == kFc1Producer) {
     if (lane == 0) {
       // ---------------------------------------------------------- producer
@@ -275,10 +324,9 @@ __global__ void __launch_bounds__(kFc1Threads, 1)
           set_status(p.status, DEVSTAT_BAD_TILE);
           continue;
         }
-        const int e = tl.x, row0 = tl.y, rows = tl.z;
+        const int e = tl.x, row0 = tl.y;
         const int w0 = (e * NIT + PAIR * (unit % NP)) * NKB;   // first W13 tile; the next is NKB later
-        const int nch = (rows + kTokChunk - 1) / kTokChunk;
-        const uint32_t tx = (uint32_t)nch * 2048u + (uint32_t)PAIR * 16384u + (1u + PAIR) * 2048u;
+        const uint32_t tx = (uint32_t)PAIR * 16384u + (1u + PAIR) * 2048u;
         for (int kb = 0; kb < NKB; ++kb) {
           if (!wait_or_abort(&bars->empty[stage], phase ^ 1u, bars, p.status)) {
             ok = false;
@@ -288,7 +336,6 @@ __global__ void __launch_bounds__(kFc1Threads, 1)
           mbar_arrive_expect_tx(&bars->full[stage], tx);
           armed |= 1u << stage;
           last_phase = (last_phase & ~(1u << stage)) | (phase << stage);
-          load_rows(st + C::kX, tm_xq, kb * 128, row0, nch, 2048u, &bars->full[stage]);
           bulk_g2s(st + C::kSX, p.sfx + ((size_t)(row0 >> 7) * (p.H / 64) + (size_t)kb * 4) * 512u, 2048u,
                    &bars->full[stage]);
 #pragma unroll
@@ -334,6 +381,7 @@ __global__ void __launch_bounds__(kFc1Threads, 1)
               if (!wait_or_abort(&bars->tmem_empty[buf * PAIR + j], par, bars, p.status)) ok = false;
             if (!ok) break;
           }
+          fence_proxy_async_shared();   // the gathered X rows (cp.async) before the MMA reads them
           tc_fence_after();
           const uint8_t* st = smem + stage * C::kStage;
           const uint32_t sfc = tmem + 256 + stage * C::kSfCols;
@@ -773,12 +821,10 @@ cudaError_t gemm_set_attributes() {
                               (int)kMmaCheckSmem);
 }
 
-cudaError_t launch_fc1(const CUtensorMap& w13, const RowMaps& xq, const Fc1Args& a, int pair, int grid,
-                       cudaStream_t st) {
+cudaError_t launch_fc1(const CUtensorMap& w13, const Fc1Args& a, int pair, int grid, cudaStream_t st) {
   CUtensorMap m0 = w13;
-  RowMaps m1 = xq;
   Fc1Args args = a;
-  void* kargs[] = {&m0, &m1, &args};
+  void* kargs[] = {&m0, &args};
   if (pair == 2)
     return launch_with_pdl((const void*)fc1_kernel<2>, dim3(grid), dim3(kFc1Threads), Fc1Cfg<2>::kSmem, st, kargs);
   return launch_with_pdl((const void*)fc1_kernel<1>, dim3(grid), dim3(kFc1Threads), Fc1Cfg<1>::kSmem, st, kargs);

@@ -83,7 +83,7 @@ inline WsLayout make_layout(const Shape& s, int64_t max_tokens) {
   L.prow_pair = take((size_t)L.PpadMax * 4);
   L.tt_list = take((size_t)L.TTmax * 16);
   L.blockhist = take((size_t)L.nblkMax * s.E * 4);
-  L.xq = take((size_t)L.PpadMax * (s.H / 2));
+  L.xq = take((size_t)max_tokens * (s.H / 2));
   L.sfx = take((size_t)(L.PpadMax / kTileRows) * (s.H / 64) * 512);
   L.sft = take((size_t)max_tokens * (s.H / 16));
   L.aq = take((size_t)L.PpadMax * (s.I / 2));
@@ -121,6 +121,8 @@ struct RouteArgs {
 
 struct Fc1Args {
   const uint8_t* sf13p;
+  const uint8_t* xq;        // [T, H/2] token-major X codes, gathered per tile row
+  const int32_t* prow_pair; // [Ppad] flat pair of each padded row (-1: padding)
   const uint8_t* sfx;
   const int32_t* tt_list;
   const int32_t* hdr;
@@ -131,9 +133,10 @@ struct Fc1Args {
   uint8_t* aq;
   uint8_t* sfa;
   int32_t* status;
-  int32_t H, I, E;
+  int32_t H, I, E, k;
   int32_t max_tiles;      // capacity of the tile list
   int64_t max_rows;       // padded rows of the workspace
+  int64_t num_pairs;      // T * k of this call
 };
 
 struct Fc2Args {
@@ -207,7 +210,7 @@ struct QuantXArgs {
   float* wrow;              // [Ppad] out: route weight of each padded row (fp32)
   float* acc;               // [T, H] out: zeroed
   const float* qX;          // [1]
-  uint8_t* xq;              // [Ppad, H/2]
+  uint8_t* xq;              // [T, H/2] token-major codes
   uint8_t* sfx;             // atom layout, H/16 chunks per row (written here when sft is null)
   uint8_t* sft;             // [T, H/16] token-major block scales, or null
   int64_t T;

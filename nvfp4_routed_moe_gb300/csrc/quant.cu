@@ -12,10 +12,12 @@ cudaError_t launch_with_pdl(const void* fn, dim3 grid, dim3 block, size_t smem, 
 
 // ------------------------------------------------------------ X quantization
 // Each lane quantizes one 16-element group of a token ("Cake SiTU backend":
-// group-16 NVFP4 input quantization with qX) once, and writes the codes and
-// block scales to the padded expanded row
-// of every pair the token is routed to ("npu_moe_init_routing_v2", formula 5,
-// gather form: expandedX[gatherRowIdx[i]] = quantResult[i // k]).  It also
+// group-16 NVFP4 input quantization with qX) once and writes the codes once,
+// to the token's row of the token-major codes; FC1 gathers them per tile row
+// ("npu_moe_init_routing_v2", formula 5, gather form: expandedX[gatherRowIdx[i]]
+// = quantResult[i // k], carried out as the GEMM's operand load).  The block
+// scales go to the padded expanded row of every pair the token is routed to,
+// in the atom layout the MMA's scale copies take.  It also
 // stores each pair's route weight (fp32) at the pair's padded row for FC2,
 // and zeroes the token's fp32 combine accumulator row, into which FC2 adds
 // the token's route-weighted expert outputs.  Block scales go straight into
@@ -63,11 +65,12 @@ __global__ void __launch_bounds__(256) quant_x_kernel(const QuantXArgs a) {
   word |= __shfl_xor_sync(0xffffffffu, word, 1);
   word |= __shfl_xor_sync(0xffffffffu, word, 2);
   if (a.sft && valid && (lane & 3) == 0) *reinterpret_cast<uint32_t*>(a.sft + t * G + g) = word;
+  if (valid) *reinterpret_cast<uint2*>(a.xq + (size_t)t * (H / 2) + g * 8) = packed;
+  if (a.sft) return;
   for (int j = 0; j < a.k; ++j) {
     const int row = __shfl_sync(0xffffffffu, rp, j);
     if (row < 0 || row >= a.max_rows || !valid) continue;
-    *reinterpret_cast<uint2*>(a.xq + (size_t)row * (H / 2) + g * 8) = packed;
-    if (!a.sft && (lane & 3) == 0) *reinterpret_cast<uint32_t*>(a.sfx + atom_offset(row, g, KC)) = word;
+    if ((lane & 3) == 0) *reinterpret_cast<uint32_t*>(a.sfx + atom_offset(row, g, KC)) = word;
   }
 }
 

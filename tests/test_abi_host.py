@@ -94,7 +94,7 @@ def test_null_and_bad_args_rejected_without_device(L):
                        (O(1, 8, 0, 0, 1, 4, 20), 1),                   # drop/pad needs every expert
                        (O(0, 0, 0, 0, 1, 0, 0, 0, 256, 3), 1),         # smooth scale rows neither 1 nor the range
                        (O(0, 0, 0, 2, 1, 4, 20), 3)):                  # valid options, workspace too small
-        st = L.moe_init_routing(ctypes.byref(shp), 16, p, p, ctypes.byref(opts), p, p, p, None, p, 1 << 20, None)
+        st = L.moe_init_routing(ctypes.byref(shp), 16, p, p, ctypes.byref(opts), p, p, p, None, p, 1 << 18, None)
         assert st == want
     assert L.moe_test_mma_fp4(p, p, p, p, 200, 256, p, p, None) == 1
     assert L.moe_test_codec_sweep(0xFFFFFFF0, 100, None, None, None, None) == 1

@@ -52,14 +52,14 @@ def test_tiny_intermediates(tiny):
     pstart = np.concatenate([[0], np.cumsum((r["count"] + 127) // 128 * 128)])[:-1]
     rank = r["gather"] - (r["cumsum"] - r["count"])[inp.expert_ids.ravel()]
     np.testing.assert_array_equal(row_pos, pstart[inp.expert_ids.ravel()] + rank)
-    # quantized X rows, bit-exact (oracle quantizes each token with qX)
+    # quantized X, bit-exact (oracle quantizes each token with qX): the codes
+    # once per token, the block scales in the atoms of every routed row
     xq_ref, xsf_ref = oracle.nvfp4_quant_rows(gen.bf16_bits_to_f32(inp.x), q=inp.qX)
     npad = int(row_pos.max()) + 1
-    xq = ws_u8(ws, lay.xq, npad * (H // 2)).reshape(npad, H // 2)
+    np.testing.assert_array_equal(ws_u8(ws, lay.xq, T * (H // 2)).reshape(T, H // 2), xq_ref)
     sfx = ws_u8(ws, lay.sfx, ((npad + 127) // 128) * (H // 64) * 512)
     for f in range(P):
         t, p = f // k, row_pos[f]
-        np.testing.assert_array_equal(xq[p], xq_ref[t])
         got_sf = [sfx[oracle.scale_atom_offset(p, c, H // 16)] for c in range(H // 16)]
         np.testing.assert_array_equal(got_sf, xsf_ref[t])
     # quantized A codes: equal except where FC1 sums round differently near a boundary
@@ -81,7 +81,7 @@ def test_two_pass_scale_layout_bit_exact():
     then laid out in atoms by a second pass.  On sampled tiles (and the last,
     partly filled one) the atoms equal the oracle's scales of each row's token
     scattered through the oracle's atom layout, zero on rows past the tile's
-    fill, and the packed codes equal the oracle's."""
+    fill, and the token-major packed codes equal the oracle's."""
     base = cases.prepare_tiny(3)
     inp = gen.tiny(3, 16400)          # weights and per-expert scales of the 16-token case
     for name in ("w13", "sf13", "w2", "sf2", "dXdW13", "qA", "dAdW2"):
@@ -105,8 +105,7 @@ def test_two_pass_scale_layout_bit_exact():
         exp_rows[:rows] = xsf_ref[toks]
         got = ws_u8(ws, lay.sfx + tile * atom_bytes, atom_bytes)
         np.testing.assert_array_equal(got, oracle.to_atom_layout(exp_rows))
-        xq = ws_u8(ws, lay.xq + tile * 128 * (H // 2), rows * (H // 2)).reshape(rows, H // 2)
-        np.testing.assert_array_equal(xq, xq_ref[toks])
+    np.testing.assert_array_equal(ws_u8(ws, lay.xq, T * (H // 2)).reshape(T, H // 2), xq_ref)
     toks = np.arange(0, T, 97)
     assert_close(out_bits(out)[toks], cases.run_oracle(inp, tokens=toks), "two-pass scales")
 
