@@ -21,7 +21,7 @@ cudaError_t launch_init_move(const InitMoveArgs& a, cudaStream_t st);
 cudaError_t launch_init_finish(const InitFinishArgs& a, cudaStream_t st, int num_sms);
 cudaError_t launch_init_rows(const InitRowsArgs& a, int64_t P, cudaStream_t st, int num_sms);
 cudaError_t launch_quant_x(const QuantXArgs& a, cudaStream_t st);
-cudaError_t launch_sf_atoms(const SfAtomArgs& a, int64_t max_words, int num_sms, cudaStream_t st);
+cudaError_t launch_sf_atoms(const SfAtomArgs& a, int64_t max_tiles, int num_sms, cudaStream_t st);
 cudaError_t launch_finalize(const float* acc, uint16_t* out, int64_t T, int H, int num_sms, cudaStream_t st);
 cudaError_t launch_prep(const PrepArgs& a, cudaStream_t st, int num_sms);
 cudaError_t launch_codec_sweep(uint32_t start, int64_t n, uint8_t* lo, uint8_t* hi, uint8_t* e4, cudaStream_t st,
@@ -465,8 +465,8 @@ static moe_status_t forward_impl(const moe_shape_t* shape, int32_t expert_begin,
     sa.num_pairs = P;
     sa.H = s.H;
     sa.k = s.k;
-    sa.max_tiles = (int32_t)L.TTmax;
-    MOE_CUDA(launch_sf_atoms(sa, tt_bound(P, s.E) * (s.H / 64) * 128, sms, stream));
+    sa.max_tiles = (int32_t)std::min<int64_t>(L.TTmax, L.PpadMax / kTileRows);   // atoms exist for the padded rows
+    MOE_CUDA(launch_sf_atoms(sa, tt_bound(P, s.E), sms, stream));
   }
 
   // 3. FC1 + SiTU + requant

@@ -75,29 +75,41 @@ __global__ void __launch_bounds__(256) quant_x_kernel(const QuantXArgs a) {
 }
 
 // ------------------------------------------------------------ scale atoms
-// One thread per 4-byte word of the atom layout ("Nvfp4 Tensor", block-scale
-// atom: byte (row%32)*16 + ((row%128)/32)*4 + chunk%4 of atom (row/128,
-// chunk/4)): the word holds the scales of chunks 4c..4c+3 of padded row
-// tile*128 + 32j + l, copied from that row's token in the token-major scales;
-// rows past a tile's fill are zero.
+// One warp per 128-row tile ("Nvfp4 Tensor", block-scale atom: the scale of
+// padded row r, 16-element group g sits at byte (r%32)*16 + ((r%128)/32)*4 +
+// g%4 of atom (r/128, g/4)): lane l owns rows l, l+32, l+64, l+96 of the
+// tile.  Per step it loads 16 scale bytes (groups 16m..16m+15) of each of
+// its four rows' tokens from the token-major scales and writes the 16-byte
+// chunk l of atoms 4m..4m+3, word c of a chunk from row l + 32c, so a warp
+// store covers one whole 512-byte atom.  Rows past a tile's fill are zero.
 __global__ void __launch_bounds__(256) sf_atoms_kernel(const SfAtomArgs a) {
   pdl_wait();
   pdl_launch_dependents();
   const int ntiles = min(a.hdr[HDR_NUM_TT], a.max_tiles);
-  const int NA4 = a.H / 64, G = a.H / 16;
-  const int64_t words = (int64_t)(ntiles > 0 ? ntiles : 0) * NA4 * 128;
+  const int lane = threadIdx.x & 31, NA4 = a.H / 64, G = a.H / 16, NM = a.H / 256;
   const int4* tiles = reinterpret_cast<const int4*>(a.tt_list);
-  for (int64_t w = (int64_t)blockIdx.x * 256 + threadIdx.x; w < words; w += (int64_t)gridDim.x * 256) {
-    const int64_t tile = w / (NA4 * 128);
-    const int rem = (int)(w - tile * NA4 * 128);
-    const int atom = rem >> 7, wi = rem & 127;
-    const int rr = (wi & 3) * 32 + (wi >> 2);    // row within the tile
-    uint32_t v = 0;
-    if (rr < __ldg(&tiles[tile].z)) {
-      const int f = __ldg(a.prow_pair + tile * kTileRows + rr);
-      if (f >= 0 && f < a.num_pairs) v = __ldg(reinterpret_cast<const uint32_t*>(a.sft + (int64_t)(f / a.k) * G) + atom);
+  uint4* atoms = reinterpret_cast<uint4*>(a.sfx);
+  const int64_t nwarps = (int64_t)gridDim.x * 8;
+  for (int64_t tile = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5); tile < ntiles; tile += nwarps) {
+    const int rows = __ldg(&tiles[tile].z);
+    const uint4* src[4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const int r = lane + 32 * c;
+      const int f = r < rows ? __ldg(a.prow_pair + tile * kTileRows + r) : -1;
+      src[c] = (f >= 0 && f < a.num_pairs) ? reinterpret_cast<const uint4*>(a.sft + (int64_t)(f / a.k) * G) : nullptr;
     }
-    a.sfx[w] = v;
+    uint4* dst = atoms + tile * NA4 * 32 + lane;
+#pragma unroll 2
+    for (int m = 0; m < NM; ++m) {
+      uint4 v[4];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) v[c] = src[c] ? __ldg(src[c] + m) : make_uint4(0u, 0u, 0u, 0u);
+      dst[(4 * m + 0) * 32] = make_uint4(v[0].x, v[1].x, v[2].x, v[3].x);
+      dst[(4 * m + 1) * 32] = make_uint4(v[0].y, v[1].y, v[2].y, v[3].y);
+      dst[(4 * m + 2) * 32] = make_uint4(v[0].z, v[1].z, v[2].z, v[3].z);
+      dst[(4 * m + 3) * 32] = make_uint4(v[0].w, v[1].w, v[2].w, v[3].w);
+    }
   }
 }
 
@@ -266,10 +278,10 @@ cudaError_t launch_quant_x(const QuantXArgs& a, cudaStream_t st) {
   return launch_with_pdl((const void*)quant_x_kernel, dim3(blocks), dim3(256), 0, st, kargs);
 }
 
-cudaError_t launch_sf_atoms(const SfAtomArgs& a, int64_t max_words, int num_sms, cudaStream_t st) {
+cudaError_t launch_sf_atoms(const SfAtomArgs& a, int64_t max_tiles, int num_sms, cudaStream_t st) {
   SfAtomArgs args = a;
   void* kargs[] = {&args};
-  const int64_t want = (max_words + 255) / 256;
+  const int64_t want = (max_tiles + 7) / 8;   // a warp per tile
   const unsigned blocks = (unsigned)(want < (int64_t)num_sms * 8 ? want : (int64_t)num_sms * 8);
   return launch_with_pdl((const void*)sf_atoms_kernel, dim3(blocks ? blocks : 1), dim3(256), 0, st, kargs);
 }
