@@ -1,7 +1,7 @@
 """ctypes binding of libnvfp4moe.so -- argument marshalling only.
 
 Every function has the name of the C entry point it calls (see
-include/nvfp4moe.h and include/nvfp4moe_testing.h).  Tensor arguments are
+include/nvfp4moe.h, include/nvfp4moe_stream.h and include/nvfp4moe_testing.h).  Tensor arguments are
 torch tensors already on the GPU; the binding passes their data pointers,
 byte sizes and the current CUDA stream, and raises :class:`MoeError` on a
 non-OK status.  No computation happens here, and there is no fallback: if the
@@ -22,11 +22,16 @@ MOE_OK = 0
 STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_WORKSPACE_TOO_SMALL",
                 4: "MOE_ERR_NOT_PREPARED", 5: "MOE_ERR_CUDA", 6: "MOE_ERR_DEVICE_STATUS"}
 DEVSTAT_INVALID_EXPERT, DEVSTAT_TIMEOUT, DEVSTAT_BAD_TILE = 1, 2, 4
+DEVSTAT_STREAM_WAIT, DEVSTAT_STREAM_BOUNDS = 8, 16
+STREAM_ROUTE, STREAM_LAYOUT = 1, 2
+STREAM_PRODUCER_TIMEOUT = 1
 
 EXPORTED = ["moe_workspace_size", "moe_prepared_weight_bytes", "moe_prepare_weights", "moe_prepare_workspace",
             "moe_forward", "moe_forward_local_experts", "moe_init_routing", "moe_init_routing_static", "moe_read_status", "moe_status_string", "moe_test_codec_sweep",
             "moe_test_quantize_rows", "moe_test_situ_requant", "moe_test_requant_lanes", "moe_test_mma_fp4",
-            "moe_workspace_layout", "moe_forward_launch_count", "moe_profile_start", "moe_profile_stop"]
+            "moe_workspace_layout", "moe_forward_launch_count", "moe_profile_start", "moe_profile_stop",
+            "moe_stream_ring_size", "moe_stream_ring_init", "moe_stream_begin", "moe_stream_publish",
+            "moe_stream_forward", "moe_stream_read_status"]
 
 
 class MoeError(RuntimeError):
@@ -54,6 +59,10 @@ class moe_ws_layout_t(ctypes.Structure):
                  "acc", "total")]
 
 
+class moe_stream_ring_t(ctypes.Structure):
+    _fields_ = [("num_slots", ctypes.c_int32), ("tokens_per_slot", ctypes.c_int32)]
+
+
 def shape(hidden: int, inter: int, num_experts: int, top_k: int) -> moe_shape_t:
     return moe_shape_t(hidden, inter, num_experts, top_k)
 
@@ -69,6 +78,7 @@ def lib():
     P, i32, i64, u32, f32, sz = (ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_uint32, ctypes.c_float,
                                  ctypes.c_size_t)
     S = ctypes.POINTER(moe_shape_t)
+    R = ctypes.POINTER(moe_stream_ring_t)
     sig = {
         "moe_workspace_size": [S, i64, ctypes.POINTER(sz)],
         "moe_prepared_weight_bytes": [S] + [ctypes.POINTER(sz)] * 4,
@@ -88,6 +98,12 @@ def lib():
         "moe_forward_launch_count": [S, i64, ctypes.POINTER(i32)],
         "moe_profile_start": [i32],
         "moe_profile_stop": [ctypes.POINTER(ctypes.c_float), ctypes.POINTER(i32)],
+        "moe_stream_ring_size": [S, R, ctypes.POINTER(sz)],
+        "moe_stream_ring_init": [S, R, P, sz, P],
+        "moe_stream_begin": [S, R, P, sz, P],
+        "moe_stream_publish": [S, R, P, sz, i64, i64, i32, i32, P, P, P, u32, P],
+        "moe_stream_forward": [S, R, P, sz, i64] + [P] * 10 + [P, sz, P, i64, u32, P],
+        "moe_stream_read_status": [P, P, P],
     }
     for name, args in sig.items():
         fn = getattr(L, name)
@@ -249,3 +265,44 @@ def moe_profile_stop():
     calls = ctypes.c_int32()
     _check(lib().moe_profile_stop(ms, ctypes.byref(calls)), "moe_profile_stop")
     return dict(zip(STAGES, [float(v) for v in ms])), calls.value
+
+
+# ------------------------------------------------------------ streaming front end
+def moe_stream_ring_size(shp, ring_cfg: moe_stream_ring_t) -> int:
+    out = ctypes.c_size_t()
+    _check(lib().moe_stream_ring_size(ctypes.byref(shp), ctypes.byref(ring_cfg), ctypes.byref(out)),
+           "moe_stream_ring_size")
+    return out.value
+
+
+def moe_stream_ring_init(shp, ring_cfg: moe_stream_ring_t, ring, stream=None):
+    _check(lib().moe_stream_ring_init(ctypes.byref(shp), ctypes.byref(ring_cfg), _p(ring), _nbytes(ring),
+                                      _stream(stream)), "moe_stream_ring_init")
+
+
+def moe_stream_begin(shp, ring_cfg: moe_stream_ring_t, ring, stream=None):
+    _check(lib().moe_stream_begin(ctypes.byref(shp), ctypes.byref(ring_cfg), _p(ring), _nbytes(ring),
+                                  _stream(stream)), "moe_stream_begin")
+
+
+def moe_stream_publish(shp, ring_cfg: moe_stream_ring_t, ring, chunk: int, token_base: int, n: int, parts: int,
+                       x=None, expert_ids=None, route_weights=None, wait_us: int = 0, stream=None):
+    _check(lib().moe_stream_publish(ctypes.byref(shp), ctypes.byref(ring_cfg), _p(ring), _nbytes(ring), chunk,
+                                    token_base, n, parts, _p(x), _p(expert_ids), _p(route_weights), wait_us,
+                                    _stream(stream)), "moe_stream_publish")
+
+
+def moe_stream_forward(shp, ring_cfg: moe_stream_ring_t, ring, chunk: int, w13, sf13, w2, sf2, qX, dX_dW13, qA,
+                       dA_dW2, situ_beta, situ_linear_beta, ws, out, wait_us: int = 0, stream=None):
+    _check(lib().moe_stream_forward(ctypes.byref(shp), ctypes.byref(ring_cfg), _p(ring), _nbytes(ring), chunk,
+                                    _p(w13), _p(sf13), _p(w2), _p(sf2), _p(qX), _p(dX_dW13), _p(qA), _p(dA_dW2),
+                                    _p(situ_beta), _p(situ_linear_beta), _p(ws), _nbytes(ws), _p(out),
+                                    out.shape[0], wait_us, _stream(stream)), "moe_stream_forward")
+
+
+def moe_stream_read_status(ring, stream=None) -> int:
+    """Returns the ring status word (STREAM_* bits) and clears it (synchronizes)."""
+    h = ctypes.c_int32()
+    _check(lib().moe_stream_read_status(_p(ring), ctypes.cast(ctypes.byref(h), ctypes.c_void_p), _stream(stream)),
+           "moe_stream_read_status")
+    return int(h.value)

@@ -8,6 +8,7 @@
 #include <vector>
 
 #include "nvfp4moe.h"
+#include "nvfp4moe_stream.h"
 #include "nvfp4moe_testing.h"
 #include "plan.h"
 #include "ptx.cuh"
@@ -392,7 +393,9 @@ static moe_status_t forward_impl(const moe_shape_t* shape, int32_t expert_begin,
                                  const uint8_t* w2, const uint8_t* sf2, const float* qX, const float* dX_dW13,
                                  const float* qA, const float* dA_dW2, const float* situ_beta,
                                  const float* situ_linear_beta, void* ws, size_t ws_bytes, void* out,
-                                 cudaStream_t stream) {
+                                 cudaStream_t stream, int64_t stream_out_rows = -1) {
+  // stream_out_rows >= 0: a streamed chunk; the finalize writes the chunk's
+  // rows (count and base from the workspace header) into out [stream_out_rows, H]
   moe_status_t st = shape_supported(shape);
   if (st != MOE_OK) return st;
   if (!x || !expert_ids || !route_weights || !w13 || !sf13 || !w2 || !sf2 || !qX || !dX_dW13 || !qA || !dA_dW2 ||
@@ -522,7 +525,12 @@ static moe_status_t forward_impl(const moe_shape_t* shape, int32_t expert_begin,
 
   // 5. BF16 finalize
   prof_mark(4, stream);
-  MOE_CUDA(launch_finalize(reinterpret_cast<const float*>(w + L.acc), static_cast<uint16_t*>(out), T, s.H, sms, stream));
+  if (stream_out_rows >= 0)
+    MOE_CUDA(launch_finalize_rows(reinterpret_cast<const float*>(w + L.acc), static_cast<uint16_t*>(out),
+                                  stream_out_rows, s.H, ra.hdr, T, sms, stream));
+  else
+    MOE_CUDA(launch_finalize(reinterpret_cast<const float*>(w + L.acc), static_cast<uint16_t*>(out), T, s.H, sms,
+                             stream));
 
   prof_end_call(stream);
   return MOE_OK;
@@ -656,6 +664,145 @@ moe_status_t moe_init_routing(const moe_shape_t* shape, int64_t num_rows, const 
   RouteArgs ra = route_args(s, L, static_cast<uint8_t*>(ws), expert_ids, num_rows);
   MOE_CUDA(init_routing_enqueue(ra, base, range, shape, num_rows, x, expert_ids, opts, expanded_x, expanded_row_idx,
                                 tokens_cumsum_or_count, expanded_scale, sms, stream));
+  return MOE_OK;
+}
+
+// ------------------------------------------------------------ streaming
+static moe_status_t ring_check(const moe_shape_t* shape, const moe_stream_ring_t* cfg, const void* ring,
+                               size_t ring_bytes, RingLayout* R) {
+  moe_status_t st = shape_supported(shape);
+  if (st != MOE_OK) return st;
+  if (!cfg || cfg->num_slots < 1 || cfg->num_slots > 64 || cfg->tokens_per_slot < 1) return MOE_ERR_INVALID_ARG;
+  if ((int64_t)cfg->tokens_per_slot * shape->top_k >= ((int64_t)1 << 31)) return MOE_ERR_UNSUPPORTED;
+  *R = make_ring_layout(to_shape(shape), cfg->num_slots, cfg->tokens_per_slot);
+  if (ring) {
+    if (!aligned(ring, 256)) return MOE_ERR_INVALID_ARG;
+    if (ring_bytes < R->total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  }
+  return MOE_OK;
+}
+
+static StreamArgs stream_args(const RingLayout& R, void* ring, int64_t chunk, uint32_t wait_us) {
+  uint8_t* b = static_cast<uint8_t*>(ring);
+  StreamArgs r{};
+  r.hdr = reinterpret_cast<RingHeader*>(b + R.header);
+  r.meta = reinterpret_cast<SlotMeta*>(b + R.meta);
+  r.S = R.S;
+  r.chunk = chunk;
+  r.wait_ns = (uint64_t)(wait_us ? wait_us : 1000000u) * 1000u;
+  return r;
+}
+
+static bool chunk_ok(int64_t chunk) { return chunk >= 0 && chunk < ((int64_t)1 << 32) - 1; }
+
+moe_status_t moe_stream_ring_size(const moe_shape_t* shape, const moe_stream_ring_t* ring_cfg, size_t* bytes) {
+  if (!bytes) return MOE_ERR_INVALID_ARG;
+  RingLayout R;
+  moe_status_t st = ring_check(shape, ring_cfg, nullptr, 0, &R);
+  if (st != MOE_OK) return st;
+  *bytes = R.total;
+  return MOE_OK;
+}
+
+moe_status_t moe_stream_ring_init(const moe_shape_t* shape, const moe_stream_ring_t* ring_cfg, void* ring,
+                                  size_t ring_bytes, cudaStream_t stream) {
+  if (!ring) return MOE_ERR_INVALID_ARG;
+  RingLayout R;
+  moe_status_t st = ring_check(shape, ring_cfg, ring, ring_bytes, &R);
+  if (st != MOE_OK) return st;
+  MOE_CUDA(cudaMemsetAsync(ring, 0, R.total, stream));
+  return MOE_OK;
+}
+
+moe_status_t moe_stream_begin(const moe_shape_t* shape, const moe_stream_ring_t* ring_cfg, void* ring,
+                              size_t ring_bytes, cudaStream_t stream) {
+  if (!ring) return MOE_ERR_INVALID_ARG;
+  RingLayout R;
+  moe_status_t st = ring_check(shape, ring_cfg, ring, ring_bytes, &R);
+  if (st != MOE_OK) return st;
+  int sms = 0;
+  MOE_CUDA(device_ready(&sms));
+  MOE_CUDA(launch_stream_begin(stream_args(R, ring, 0, 0), stream));
+  return MOE_OK;
+}
+
+moe_status_t moe_stream_publish(const moe_shape_t* shape, const moe_stream_ring_t* ring_cfg, void* ring,
+                                size_t ring_bytes, int64_t chunk, int64_t token_base, int32_t n, int32_t parts,
+                                const void* x, const int32_t* expert_ids, const void* route_weights, uint32_t wait_us,
+                                cudaStream_t stream) {
+  if (!ring || !chunk_ok(chunk) || token_base < 0 || n < 0 || parts < 1 || parts > 3) return MOE_ERR_INVALID_ARG;
+  RingLayout R;
+  moe_status_t st = ring_check(shape, ring_cfg, ring, ring_bytes, &R);
+  if (st != MOE_OK) return st;
+  if (n > R.C) return MOE_ERR_INVALID_ARG;
+  if ((parts & MOE_STREAM_LAYOUT) && n > 0 && (!x || !aligned(x, 16))) return MOE_ERR_INVALID_ARG;
+  if ((parts & MOE_STREAM_ROUTE) && n > 0 && (!expert_ids || !route_weights)) return MOE_ERR_INVALID_ARG;
+  int sms = 0;
+  MOE_CUDA(device_ready(&sms));
+  uint8_t* b = static_cast<uint8_t*>(ring);
+  const int64_t slot = chunk % R.S;
+  PublishArgs a{};
+  a.r = stream_args(R, ring, chunk, wait_us);
+  a.token_base = token_base;
+  a.C = R.C;
+  a.n = n;
+  a.H = shape->hidden;
+  a.k = shape->top_k;
+  a.E = shape->num_experts;
+  a.parts = parts;
+  a.x = static_cast<const uint16_t*>(x);
+  a.ids = expert_ids;
+  a.w = static_cast<const uint16_t*>(route_weights);
+  a.slot_x = reinterpret_cast<uint16_t*>(b + R.x) + slot * R.C * a.H;
+  a.slot_ids = reinterpret_cast<int32_t*>(b + R.ids) + slot * R.C * a.k;
+  a.slot_w = reinterpret_cast<uint16_t*>(b + R.w) + slot * R.C * a.k;
+  MOE_CUDA(launch_stream_publish(a, sms, stream));
+  return MOE_OK;
+}
+
+moe_status_t moe_stream_forward(const moe_shape_t* shape, const moe_stream_ring_t* ring_cfg, void* ring,
+                                size_t ring_bytes, int64_t chunk, const uint8_t* w13, const uint8_t* sf13,
+                                const uint8_t* w2, const uint8_t* sf2, const float* qX, const float* dX_dW13,
+                                const float* qA, const float* dA_dW2, const float* situ_beta,
+                                const float* situ_linear_beta, void* ws, size_t ws_bytes, void* out,
+                                int64_t out_rows, uint32_t wait_us, cudaStream_t stream) {
+  if (!ring || !chunk_ok(chunk) || !out || out_rows < 1 || !ws) return MOE_ERR_INVALID_ARG;
+  RingLayout R;
+  moe_status_t st = ring_check(shape, ring_cfg, ring, ring_bytes, &R);
+  if (st != MOE_OK) return st;
+  if (!aligned(ws, 256)) return MOE_ERR_INVALID_ARG;
+  const Shape s = to_shape(shape);
+  const int64_t cap = capacity_tokens(s, ws_bytes);
+  if (cap < R.C) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  if (!is_prepared(ws, ws_bytes, R.C, s)) return MOE_ERR_NOT_PREPARED;
+  if (!w13 || !sf13 || !w2 || !sf2 || !qX || !dX_dW13 || !qA || !dA_dW2) return MOE_ERR_INVALID_ARG;
+  int sms = 0;
+  MOE_CUDA(device_ready(&sms));
+  uint8_t* b = static_cast<uint8_t*>(ring);
+  const int64_t slot = chunk % R.S;
+  const StreamArgs r = stream_args(R, ring, chunk, wait_us);
+  int32_t* ws_hdr = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(ws) + make_layout(s, cap).header);
+  MOE_CUDA(launch_stream_gate(r, R.C, ws_hdr, stream));
+  // the slot's C tokens; rows past the chunk's count carry the id E, which the
+  // routing skips without flagging it (ids above E are still flagged)
+  st = forward_impl(shape, 0, shape->num_experts + 1, R.C, reinterpret_cast<uint16_t*>(b + R.x) + slot * R.C * s.H,
+                    reinterpret_cast<int32_t*>(b + R.ids) + slot * R.C * s.k,
+                    reinterpret_cast<uint16_t*>(b + R.w) + slot * R.C * s.k, w13, sf13, w2, sf2, qX, dX_dW13, qA,
+                    dA_dW2, situ_beta, situ_linear_beta, ws, ws_bytes, out, stream, out_rows);
+  if (st != MOE_OK) return st;
+  MOE_CUDA(launch_stream_release(r, ws_hdr, stream));
+  return MOE_OK;
+}
+
+moe_status_t moe_stream_read_status(const void* ring, int32_t* host_status, cudaStream_t stream) {
+  if (!ring || !host_status) return MOE_ERR_INVALID_ARG;
+  int32_t* d = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(const_cast<void*>(ring)) + offsetof(RingHeader, status));
+  int32_t h = 0;
+  MOE_CUDA(cudaMemcpyAsync(&h, d, sizeof(h), cudaMemcpyDeviceToHost, stream));
+  MOE_CUDA(cudaStreamSynchronize(stream));
+  MOE_CUDA(cudaMemsetAsync(d, 0, sizeof(h), stream));
+  MOE_CUDA(cudaStreamSynchronize(stream));
+  *host_status = h;
   return MOE_OK;
 }
 

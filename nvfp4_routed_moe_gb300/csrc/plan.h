@@ -30,6 +30,9 @@ enum : int {
   HDR_DONE = 4,        // last-arriver ticket of the multi-CTA routing
   HDR_NVALID = 5,      // routed pairs this call
   HDR_MAXROWS = 6,     // largest number of pairs routed to one expert this call
+  HDR_STREAM_OK = 7,   // streamed chunk: 1 once its generations were seen published
+  HDR_STREAM_N = 8,    // streamed chunk: valid tokens
+  HDR_STREAM_BASE = 10,  // streamed chunk: first logical token (int64, words 10-11)
   HDR_WORDS = 64,
 };
 
@@ -234,6 +237,77 @@ struct PrepArgs {
   uint8_t *w13o, *sf13o, *w2o, *sf2o;
   int32_t H, I, E;
 };
+
+// ---------------------------------------------------------------- streaming
+// Ring of a chunk-ready stream: header | slot metadata | x | ids | weights.
+struct RingHeader {
+  uint64_t epoch;        // incremented by every moe_stream_begin
+  int32_t status;        // MOE_STREAM_* bits
+  int32_t pad[61];
+};
+static_assert(sizeof(RingHeader) == 256, "ring header");
+
+struct SlotMeta {
+  uint64_t route_gen, layout_gen, consumed_gen;
+  int64_t token_base;
+  int32_t n;
+  int32_t done[2];       // CTAs of the publish in flight that have finished copying (ROUTE[+LAYOUT], LAYOUT)
+  int32_t fail[2];       // ... and whether one of them gave up waiting for the slot
+  int32_t pad[3];
+};
+static_assert(sizeof(SlotMeta) == 64, "slot metadata");
+
+struct RingLayout {
+  int32_t S;
+  int64_t C;
+  size_t header, meta, x, ids, w, total;
+};
+
+inline RingLayout make_ring_layout(const Shape& s, int32_t S, int64_t C) {
+  RingLayout R{};
+  R.S = S;
+  R.C = C;
+  size_t o = 0;
+  R.header = o;
+  o += sizeof(RingHeader);
+  R.meta = o;
+  o = align_up(o + (size_t)S * sizeof(SlotMeta), 256);
+  R.x = o;
+  o = align_up(o + (size_t)S * C * s.H * 2, 256);
+  R.ids = o;
+  o = align_up(o + (size_t)S * C * s.k * 4, 256);
+  R.w = o;
+  o = align_up(o + (size_t)S * C * s.k * 2, 256);
+  R.total = o;
+  return R;
+}
+
+struct StreamArgs {
+  RingHeader* hdr;
+  SlotMeta* meta;
+  int32_t S;
+  int64_t chunk;         // chunk index of this invocation; slot chunk % S
+  uint64_t wait_ns;
+};
+
+struct PublishArgs {
+  StreamArgs r;
+  int64_t token_base, C;
+  int32_t n, H, k, E, parts;
+  const uint16_t* x;     // [n, H]
+  const int32_t* ids;    // [n, k]
+  const uint16_t* w;     // [n, k]
+  uint16_t* slot_x;      // [C, H]
+  int32_t* slot_ids;     // [C, k]
+  uint16_t* slot_w;      // [C, k]
+};
+
+cudaError_t launch_stream_begin(const StreamArgs& r, cudaStream_t st);
+cudaError_t launch_stream_publish(const PublishArgs& a, int num_sms, cudaStream_t st);
+cudaError_t launch_stream_gate(const StreamArgs& r, int64_t C, int32_t* ws_hdr, cudaStream_t st);
+cudaError_t launch_stream_release(const StreamArgs& r, const int32_t* ws_hdr, cudaStream_t st);
+cudaError_t launch_finalize_rows(const float* acc, uint16_t* out, int64_t out_rows, int H, int32_t* ws_hdr,
+                                 int64_t C, int num_sms, cudaStream_t st);
 
 // Init-routing shared by moe_init_routing and moe_init_routing_static: the
 // host check of the options (fills the routed expert range) and the

@@ -14,6 +14,8 @@ enum : int32_t {
   DEVSTAT_INVALID_EXPERT = 1,   // an expert id outside [0, E) was seen and skipped
   DEVSTAT_TIMEOUT = 2,          // a bounded wait gave up
   DEVSTAT_BAD_TILE = 4,         // a tile descriptor failed its bounds check
+  DEVSTAT_STREAM_WAIT = 8,      // a streamed chunk's generations were not published in time
+  DEVSTAT_STREAM_BOUNDS = 16,   // a streamed chunk's output rows fell outside the output
 };
 
 __device__ __forceinline__ void set_status(int32_t* status, int32_t code) {
