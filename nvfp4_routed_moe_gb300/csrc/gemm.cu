@@ -357,12 +357,12 @@ __global__ void __launch_bounds__(kFc1Threads, 1)
     if (lane == 0) {
       // --------------------------------------------------------------- MMA
       // TMEM: accumulator buffer b holds the unit's PAIR blocks at columns
-      // (b*PAIR + j)*128; the scale atoms of stage s at 256 + kSfCols*s (X, then
-      // each W tile: 16 columns each).
+      // (b*PAIR + j)*128; the scale atoms of stage s at 256 + kSfCols*s: X's
+      // four (K-steps 0..3), then per K-step the PAIR W tiles' atoms.
       uint32_t stage = 0, phase = 0;
       int local = 0;
       bool ok = true;
-      const uint32_t idesc = idesc_mxf4nvf4(128, 128);
+      const uint32_t idesc = idesc_mxf4nvf4(128, 128 * PAIR);
       int4 nxt = next_tile(tiles, blockIdx.x, num_units, NP);
       for (int unit = blockIdx.x; unit < num_units && ok; unit += gridDim.x) {
         const int4 tl = nxt;
@@ -390,17 +390,18 @@ __global__ void __launch_bounds__(kFc1Threads, 1)
             tmem_cp_32x128b_x4(sfc + a * 4, sf_desc(st + C::kSX + a * 512));
 #pragma unroll
             for (int j = 0; j < PAIR; ++j)
-              tmem_cp_32x128b_x4(sfc + 16 * (1 + j) + a * 4, sf_desc(st + C::kSW + j * 2048 + a * 512));
+              tmem_cp_32x128b_x4(sfc + 16 + (a * PAIR + j) * 4, sf_desc(st + C::kSW + j * 2048 + a * 512));
           }
+          // M = tokens (X tile), N = the PAIR W13 tiles as one operand of
+          // PAIR*128 rows (contiguous in shared memory, their accumulators
+          // contiguous in TMEM, their scale atoms side by side per K-step):
+          // one long MMA per K-step, during which the tensor pipe also works
+          // off the scale copies.
 #pragma unroll
-          for (int ks = 0; ks < 4; ++ks) {   // M = tokens (X tile), N = W13 rows
+          for (int ks = 0; ks < 4; ++ks) {
             const uint64_t xd = smem_desc(smem_u32(st + C::kX) + ks * 32, 16, 1024, kLayoutSW128);
-            const uint32_t acc = (kb | ks) ? 1u : 0u;
-#pragma unroll
-            for (int j = 0; j < PAIR; ++j) {
-              const uint64_t wd = smem_desc(smem_u32(st + C::kW + j * 16384) + ks * 32, 16, 1024, kLayoutSW128);
-              mma_mxf4nvf4(dcol + j * 128, xd, wd, idesc, sfc + ks * 4, sfc + 16 * (1 + j) + ks * 4, acc);
-            }
+            const uint64_t wd = smem_desc(smem_u32(st + C::kW) + ks * 32, 16, 1024, kLayoutSW128);
+            mma_mxf4nvf4(dcol, xd, wd, idesc, sfc + ks * 4, sfc + 16 + ks * 4 * PAIR, (kb | ks) ? 1u : 0u);
           }
           tc_commit(&bars->empty[stage]);
           if (++stage == C::kStages) {
