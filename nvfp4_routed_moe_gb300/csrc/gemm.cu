@@ -92,6 +92,7 @@ struct Barriers {
   uint64_t drain;
   uint32_t tmem_base;
   volatile int32_t abort_flag;
+  int32_t fc2_g;         // FC2: output tiles per work unit, chosen by thread 0 during setup
 };
 static_assert(sizeof(Barriers) <= 1024, "barrier block");
 
@@ -203,12 +204,11 @@ __device__ __forceinline__ int4 fc2_next_tile(const int4* tiles, int unit, int n
 // hand-over.  Small batches get long units (few tiles, overhead dominates);
 // large batches short ones.
 __device__ __forceinline__ int fc2_group(int ntiles, int NMT, int npu, int grid) {
-  int best = 1;
-  int64_t best_cost = -1;
+  int best = 1, best_cost = -1;
   for (int G = 1; G <= npu; ++G) {
     if (npu % G) continue;
-    const int64_t units = (int64_t)ntiles * (NMT / G);
-    const int64_t cost = (units + grid - 1) / grid * (G + 2);
+    const int units = ntiles * (NMT / G);
+    const int cost = (units + grid - 1) / grid * (G + 2);
     if (best_cost < 0 || cost < best_cost) {
       best_cost = cost;
       best = G;
@@ -503,12 +503,18 @@ __global__ void __launch_bounds__(kFc2Threads, 1)
     tma_prefetch_desc(&tm_aq.m16);
     tma_prefetch_desc(&tm_aq.m128);
   }
+  if (threadIdx.x == 0) {
+    // The tile count comes from the routing kernel, which completed before
+    // FC1 started, so it is read before waiting for FC1; one thread picks the
+    // group size and the setup barrier shares it.
+    bars->fc2_g = fc2_group(clamp_tiles(__ldcg(p.hdr + HDR_NUM_TT), p.max_tiles), NMT, npu, gridDim.x);
+  }
   gemm_setup<kMaxStages, kFc2EpiWarps>(bars, warp, 1);
   const uint32_t tmem = bars->tmem_base;
   pdl_wait();
   pdl_launch_dependents();
   const int ntiles = clamp_tiles(p.hdr[HDR_NUM_TT], p.max_tiles);
-  const int G = fc2_group(ntiles, NMT, npu, gridDim.x);
+  const int G = bars->fc2_g;
   const int num_units = ntiles * (NMT / G);
   // Accumulator slots: the 256 accumulator columns split into slots as wide as
   // the widest token tile of this call, at least 32 columns (8 slots when
