@@ -142,7 +142,11 @@ class MoEInputs:
 
 def tiny(seed: int = 0, T: int = 16) -> MoEInputs:
     """The tiny case; weights come back as fp32 (the consumer quantizes)."""
-    H, I, E, k = TINY["H"], TINY["I"], TINY["E"], TINY["k"]
+    return small(seed, T, **TINY)
+
+
+def small(seed: int, T: int, H: int, I: int, E: int, k: int) -> MoEInputs:
+    """A small case of any shape, drawn like the tiny one (fp32 weights)."""
     x = draw_x(seed, T, H)
     ids = draw_ids_uniform(seed, T, E, k)
     rw = draw_route_weights(seed, T, k)

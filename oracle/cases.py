@@ -32,7 +32,16 @@ def quantize_expert_weights(w_f32: np.ndarray):
 
 
 def prepare_tiny(seed: int = 0, T: int = 16) -> gen.MoEInputs:
-    inp = gen.tiny(seed, T)
+    return prepare(gen.tiny(seed, T))
+
+
+def prepare_small(seed: int, T: int, H: int, I: int, E: int, k: int) -> gen.MoEInputs:
+    """A small case of another shape, prepared like the tiny one."""
+    return prepare(gen.small(seed, T, H, I, E, k))
+
+
+def prepare(inp: gen.MoEInputs) -> gen.MoEInputs:
+    T = inp.T
     inp.w13, inp.sf13, dW13 = quantize_expert_weights(inp.w13_f32)
     inp.w2, inp.sf2, dW2 = quantize_expert_weights(inp.w2_f32)
     dX = np.float32(np.float32(1.0) / inp.qX)
