@@ -14,8 +14,9 @@ path); rank 0 prints one JSON line.
 
 Also measured: per-stage times from timing events recorded between the
 stages inside the timed steps (the dominant kernel's roofline uses them),
-an end-to-end pass with pinned host buffers (copies inside the timed
-region), SM clocks during the timed region, a decode/prefill sweep (L2
+an end-to-end pass through moe_forward with pinned host buffers (every
+step's input copy and output read-back inside the timed region, pipelined on
+copy-in / compute / copy-out streams with double buffers), SM clocks during the timed region, a decode/prefill sweep (L2
 flushed between steps), and the CPU oracle on a bounded sample of the same
 workload (rank 0, one GPU only).
 
@@ -336,35 +337,61 @@ def main():
     launches = api.moe_forward_launch_count(shp, T) * args.steps
 
     # ------------------------------------------------------------ end to end
+    # Every step copies its inputs from pinned host memory and reads its
+    # output back, pipelined as a server would run it: step n's input copy
+    # (copy-in stream) and step n-1's output copy (copy-out stream) overlap
+    # step n's forward (compute stream); inputs and outputs are double-
+    # buffered and events order every hand-over.
     x_h = batch["x"].cpu().pin_memory()
     ids_h = batch["ids"].cpu().pin_memory()
     rw_h = batch["rw"].cpu().pin_memory()
-    out_h = torch.empty((T, H), dtype=torch.bfloat16).pin_memory()
-    xb, idb, rwb = torch.empty_like(batch["x"]), torch.empty_like(batch["ids"]), torch.empty_like(batch["rw"])
-    ebatch = dict(batch, x=xb, ids=idb, rw=rwb)
+    outs_h = [torch.empty((T, H), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    ins = [dict(batch, x=torch.empty_like(batch["x"]), ids=torch.empty_like(batch["ids"]),
+                rw=torch.empty_like(batch["rw"])) for _ in range(2)]
+    outs = [torch.empty_like(out) for _ in range(2)]
+    s_in, s_cmp, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    ev = lambda: torch.cuda.Event()
+    in_ready, in_free = [ev(), ev()], [ev(), ev()]
+    out_ready, out_free = [ev(), ev()], [ev(), ev()]
     e2e_steps = min(args.steps, 200)
-    for _ in range(2):
-        xb.copy_(x_h, non_blocking=True)
-        idb.copy_(ids_h, non_blocking=True)
-        rwb.copy_(rw_h, non_blocking=True)
-        forward(ebatch, ws, out)
-        out_h.copy_(out, non_blocking=True)
+
+    def e2e_step(n):
+        b = n % 2
+        with torch.cuda.stream(s_in):
+            if n >= 2:
+                s_in.wait_event(in_free[b])
+            ins[b]["x"].copy_(x_h, non_blocking=True)
+            ins[b]["ids"].copy_(ids_h, non_blocking=True)
+            ins[b]["rw"].copy_(rw_h, non_blocking=True)
+            in_ready[b].record(s_in)
+        s_cmp.wait_event(in_ready[b])
+        if n >= 2:
+            s_cmp.wait_event(out_free[b])
+        forward(ins[b], ws, outs[b], stream=s_cmp)
+        in_free[b].record(s_cmp)
+        out_ready[b].record(s_cmp)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(out_ready[b])
+            outs_h[b].copy_(outs[b], non_blocking=True)
+            out_free[b].record(s_out)
+
+    torch.cuda.synchronize()
+    for n in range(2):
+        e2e_step(n)
     barrier()
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for _ in range(e2e_steps):
-        xb.copy_(x_h, non_blocking=True)
-        idb.copy_(ids_h, non_blocking=True)
-        rwb.copy_(rw_h, non_blocking=True)
-        forward(ebatch, ws, out)
-        out_h.copy_(out, non_blocking=True)
-    e1.record()
+    e0.record(s_in)
+    for n in range(e2e_steps):
+        e2e_step(n)
+    s_in.wait_stream(s_out)
+    e1.record(s_in)
     torch.cuda.synchronize()
     _, e2e_val = job_throughput(e0.elapsed_time(e1), T, e2e_steps, world)
     h2d = x_h.numel() * 2 + ids_h.numel() * 4 + rw_h.numel() * 2
-    d2h = out_h.numel() * 2
-    assert torch.equal(out_h.view(torch.int16), out.cpu().view(torch.int16))
+    d2h = outs_h[0].numel() * 2
+    last = (e2e_steps - 1) % 2
+    assert torch.equal(outs_h[last].view(torch.int16), outs[last].cpu().view(torch.int16))
 
     # ------------------------------------------------------------ roofline
     peak, peak_src = peaks()
@@ -440,7 +467,7 @@ def main():
                 "roofline": roof, "roofline_kernels": roof_all, "forward_roofline": fwd_roof, "stages_ms": stage,
                 "cpu_baseline": cpu,
                 "e2e": {"value": e2e_val, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                        "steps": e2e_steps},
+                        "steps": e2e_steps, "pipeline": "copy-in, compute and copy-out streams, double-buffered"},
                 "gpu_launches": launches, "clocks": clk, "sweep": sweep}
         print(json.dumps(line), flush=True)
     if world > 1:
