@@ -69,6 +69,43 @@ def peaks():
         return 6800.0, "fallback"
 
 
+def init_routing_sweep(shp, flush, dev):
+    """moe_init_routing alone on 4096 rows (k=16, E=896, H=3584, uniform distinct
+    ids, dynamic int8): dropless with gather indices and cumsum, and drop/pad
+    with capacity 96.  Achieved GB/s over the algorithmic bytes (x read, ids
+    read, expanded rows, scales and indices written)."""
+    import torch
+    from nvfp4_routed_moe_gb300 import api
+    rows, H, k, E = 4096, shp.hidden, shp.top_k, shp.num_experts
+    b = gen.full(200, T=rows, routing="uniform", weights=False, E=E)
+    x = dev(b.x, torch.bfloat16)
+    ids = dev(b.expert_ids)
+    ws = torch.empty(api.moe_workspace_size(shp, rows), dtype=torch.uint8, device="cuda")
+    api.moe_prepare_workspace(shp, ws, rows)
+    res = {}
+    for name, C in (("dropless", 0), ("drop_pad_C96", 96)):
+        n_out = E * C if C else rows * k
+        ex = torch.empty((n_out, H), dtype=torch.int8, device="cuda")
+        idx = torch.empty(rows * k, dtype=torch.int32, device="cuda")
+        tok = torch.empty(E, dtype=torch.int32, device="cuda")
+        sc = torch.empty(n_out, dtype=torch.float32, device="cuda")
+        opts = api.routing_opts(drop_pad=1 if C else 0, expert_capacity=C, quant_mode=1)
+        call = lambda: api.moe_init_routing(shp, rows, x, ids, opts, ex, idx, tok, sc, ws)
+        for _ in range(3):
+            call()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(20)]
+        for a, c in evs:
+            flush.fill_(1)
+            a.record()
+            call()
+            c.record()
+        torch.cuda.synchronize()
+        t_ms = statistics.median([a.elapsed_time(c) for a, c in evs])
+        byt = rows * H * 2 + rows * k * 4 + n_out * H + n_out * 4 + rows * k * 4 + E * 4
+        res[name] = {"rows": rows, "ms": round(t_ms, 4), "bytes": byt, "gb_per_s": byt / (t_ms * 1e-3) / 1e9}
+    return res
+
+
 def step_bytes(T, n_active):
     """Algorithmic bytes of one forward: weights and block scales of the
     active experts, x read and out written (bf16), ids and route weights."""
@@ -418,8 +455,9 @@ def main():
         sweep = {}
         flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
         for name, T_s, routing in (("decode1", 1, "uniform"), ("decode8", 8, "uniform"), ("decode16", 16, "uniform"),
-                                   ("T128", 128, "uniform"), ("T1024", 1024, "uniform"),
-                                   ("prefill", 4096, "zipf")):
+                                   ("T32", 32, "uniform"), ("T128", 128, "uniform"), ("T512", 512, "uniform"),
+                                   ("T1024", 1024, "uniform"), ("T2048", 2048, "uniform"), ("prefill", 4096, "zipf"),
+                                   ("T8192", 8192, "uniform")):
             b = make_batch(gen.full(100 + T_s, T=T_s, routing=routing, weights=False, E=E))
             ws_s = torch.empty(api.moe_workspace_size(shp, T_s), dtype=torch.uint8, device="cuda")
             api.moe_prepare_workspace(shp, ws_s, T_s)
@@ -435,6 +473,20 @@ def main():
                 c.record()
             torch.cuda.synchronize()
             t_ms = statistics.median([a.elapsed_time(c) for a, c in evs])
+            # the same forward captured once in a CUDA graph and replayed
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                forward(b, ws_s, out_s)
+            for _ in range(3):
+                g.replay()
+            for a, c in evs:
+                flush.fill_(1)
+                a.record()
+                g.replay()
+                c.record()
+            torch.cuda.synchronize()
+            t_graph = statistics.median([a.elapsed_time(c) for a, c in evs])
+            del g
             api.moe_profile_start(n_s)           # stage breakdown in a separate pass
             for _ in range(n_s):
                 flush.fill_(1)
@@ -442,10 +494,12 @@ def main():
             torch.cuda.synchronize()
             st_ms, nc = api.moe_profile_stop()
             byt = step_bytes(T_s, b["n_active"])
-            sweep[name] = {"T": T_s, "ms": round(t_ms, 4), "tokens_per_s": T_s / (t_ms * 1e-3),
+            sweep[name] = {"T": T_s, "ms": round(t_ms, 4), "ms_graph": round(t_graph, 4),
+                           "tokens_per_s": T_s / (t_ms * 1e-3),
                            "hbm_frac": byt / (t_ms * 1e-3) / 1e9 / peak, "n_active": b["n_active"],
                            "fc1_ms": round(st_ms["fc1"] / nc, 4), "fc2_ms": round(st_ms["fc2"] / nc, 4),
                            "fc1_hbm_frac": fc1_bytes(T_s, b["n_active"]) / (st_ms["fc1"] / nc * 1e-3) / 1e9 / peak}
+        sweep["init_routing"] = init_routing_sweep(shp, flush, dev)
         del flush
 
     cpu = None

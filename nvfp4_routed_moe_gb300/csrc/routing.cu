@@ -35,21 +35,35 @@ __device__ __forceinline__ uint32_t lanemask_lt() {
   return m;
 }
 
+// The ids of a warp's run are loaded kIdBatch steps of 32 at a time, all in
+// flight together, and then processed step by step in order.
+constexpr int kIdBatch = 8;
+
 // Pass 1: per-warp histogram of ids[begin, end) into hist_w[E] (shared).
 __device__ __forceinline__ void warp_histogram(const int32_t* ids, int64_t begin, int64_t end, int E,
                                                int* hist_w, int id_base) {
   const int lane = threadIdx.x & 31;
-  for (int64_t base = begin; base < end; base += 32) {
-    const int64_t f = base + lane;
-    const bool in = f < end;
-    const int id = in ? ids[f] - id_base : -1;
-    const bool ok = in && id >= 0 && id < E;
-    const uint32_t okmask = __ballot_sync(0xffffffffu, ok);
-    if (ok) {
-      const uint32_t peers = __match_any_sync(okmask, id);
-      if (lane == __ffs(peers) - 1) hist_w[id] += __popc(peers);
+  for (int64_t base0 = begin; base0 < end; base0 += 32 * kIdBatch) {
+    int raw[kIdBatch];
+#pragma unroll
+    for (int j = 0; j < kIdBatch; ++j) {
+      const int64_t f = base0 + j * 32 + lane;
+      raw[j] = f < end ? ids[f] : 0;   // generic load: ids may be in shared memory
     }
-    __syncwarp();
+#pragma unroll
+    for (int j = 0; j < kIdBatch; ++j) {
+      if (base0 + j * 32 >= end) break;   // warp-uniform: the run is done
+      const int64_t f = base0 + j * 32 + lane;
+      const bool in = f < end;
+      const int id = raw[j] - id_base;
+      const bool ok = in && id >= 0 && id < E;
+      const uint32_t okmask = __ballot_sync(0xffffffffu, ok);
+      if (ok) {
+        const uint32_t peers = __match_any_sync(okmask, id);
+        if (lane == __ffs(peers) - 1) hist_w[id] += __popc(peers);
+      }
+      __syncwarp();
+    }
   }
 }
 
@@ -59,10 +73,19 @@ __device__ __forceinline__ int warp_rank(const RouteArgs& a, const int32_t* ids,
                                          int* base_w, const int* s_offs, const int* s_poffs) {
   const int lane = threadIdx.x & 31;
   int invalid = 0;
-  for (int64_t base = begin; base < end; base += 32) {
-    const int64_t f = base + lane;
+  for (int64_t base0 = begin; base0 < end; base0 += 32 * kIdBatch) {
+   int rawb[kIdBatch];
+#pragma unroll
+   for (int j = 0; j < kIdBatch; ++j) {
+     const int64_t f = base0 + j * 32 + lane;
+     rawb[j] = f < end ? ids[f] : -1;   // generic load: ids may be in shared memory
+   }
+#pragma unroll
+   for (int j = 0; j < kIdBatch; ++j) {
+    if (base0 + j * 32 >= end) break;   // warp-uniform: the run is done
+    const int64_t f = base0 + j * 32 + lane;
     const bool in = f < end;
-    const int raw = in ? ids[f] : -1;
+    const int raw = in ? rawb[j] : -1;
     const int id = raw - a.id_base;
     const bool ok = in && id >= 0 && id < a.E;
     const uint32_t okmask = __ballot_sync(0xffffffffu, ok);
@@ -83,6 +106,7 @@ __device__ __forceinline__ int warp_rank(const RouteArgs& a, const int32_t* ids,
       if (raw < 0 || raw >= a.E_all) ++invalid;   // outside every expert; in-range ids outside E are skipped silently
     }
     __syncwarp();
+   }
   }
   return invalid;
 }
@@ -272,19 +296,31 @@ __global__ void __launch_bounds__(256) route_hist_kernel(const RouteArgs a) {
   __syncthreads();
   if (!s_last) return;
   __threadfence();
-  for (int e = tid; e < E; e += 256) {
-    int run = 0;
-    for (int blk0 = 0; blk0 < a.nblk; blk0 += 8) {   // 8 loads in flight per thread
-      int c[8];
+  // Each thread scans the block counts of its experts, two experts and 32
+  // blocks at a time: 64 independent loads in flight per step.
+  for (int e0 = tid; e0 < E; e0 += 512) {
+    const int e1 = e0 + 256;
+    int run0 = 0, run1 = 0;
+    for (int blk0 = 0; blk0 < a.nblk; blk0 += 32) {
+      int c0[32], c1[32];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) c[j] = blk0 + j < a.nblk ? __ldcg(&a.blockhist[(size_t)(blk0 + j) * E + e]) : 0;
+      for (int j = 0; j < 32; ++j) {
+        const bool inb = blk0 + j < a.nblk;
+        c0[j] = inb ? __ldcg(&a.blockhist[(size_t)(blk0 + j) * E + e0]) : 0;
+        c1[j] = inb && e1 < E ? __ldcg(&a.blockhist[(size_t)(blk0 + j) * E + e1]) : 0;
+      }
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        if (blk0 + j < a.nblk) a.blockhist[(size_t)(blk0 + j) * E + e] = run;
-        run += c[j];
+      for (int j = 0; j < 32; ++j) {
+        if (blk0 + j < a.nblk) {
+          a.blockhist[(size_t)(blk0 + j) * E + e0] = run0;
+          if (e1 < E) a.blockhist[(size_t)(blk0 + j) * E + e1] = run1;
+        }
+        run0 += c0[j];
+        run1 += c1[j];
       }
     }
-    s_cnt[e] = run;
+    s_cnt[e0] = run0;
+    if (e1 < E) s_cnt[e1] = run1;
   }
   __syncthreads();
   scan_experts<256>(a, s_cnt, s_offs, s_poffs, s_tmp);
