@@ -2,20 +2,22 @@
 //
 // FC1 ("Cake SiTU backend": FC1 over gate and up, SiTU, intermediate NVFP4
 // requantization): the MMA takes the routed tokens of one expert tile on its
-// M side (128 rows; a decode-sized group fills only the first rows, which
-// costs the tensor pipe no more than a narrow N would) and a prepared W13
-// tile on its N side: 128 rows holding 64 intermediate features with gate and
-// up rows interleaved (row 2i = gate of feature i, row 2i+1 = up).  A work
-// unit is one token tile and two such W13 tiles (128 features): per k-block of
-// 256 FP4 elements the X tile and its scale atoms serve both, so a k-block
-// costs 12 scale-atom copies to TMEM for 8 MMAs instead of 16, and 54 KB of
-// loads for two [128 x 128] products instead of 72.  The two accumulators
-// (256 TMEM columns) are single-buffered; the epilogue releases each as soon
-// as it has read it.  In the epilogue a thread owns one token row: it reads
-// 16 features' gate/up pairs,
-// forms z = acc * dX*dW13[e] and a = SiTU(z_g, z_u), and quantizes the 16
-// values with qA[e] in registers into the token's padded row of A (codes and
-// atom-layout scale) -- no cross-lane traffic.
+// M side (128 rows, gathered per row from the token-major quantized X; a
+// decode-sized group fills only the first rows, which costs the tensor pipe
+// no more than a narrow N would) and prepared W13 tiles on its N side: 128
+// rows holding 64 intermediate features with gate and up rows interleaved
+// (row 2i = gate of feature i, row 2i+1 = up).  A work unit is one token tile
+// and two such W13 tiles (128 features), which form one 256-row operand: per
+// k-block of 256 FP4 elements one N = 256 MMA per K-step, and the X tile and
+// its scale atoms serve both tiles (12 scale-atom copies to TMEM instead of
+// 16, 54 KB of loads for a [128 x 256] product instead of 72).  The
+// accumulators (256 TMEM columns) are single-buffered; the epilogue releases
+// them as soon as it has read them.  In the epilogue a thread owns one token
+// row: it reads 16 features' gate/up pairs, forms z = acc * dX*dW13[e] and
+// a = SiTU(z_g, z_u), and quantizes the 16 values with qA[e] in registers
+// into the token's padded row of A (codes and atom-layout scale) -- no
+// cross-lane traffic.  Below 17 tokens a unit is one W13 tile (N = 128), for
+// more units to spread over the SMs.
 //
 // FC2 ("Cake SiTU backend": FC2, BF16 weighted finalization): weights on the
 // MMA's M side (128 output features), tokens on N (16..128).  A work unit is
@@ -30,9 +32,10 @@
 // T x H/nq fp32, stay resident in L2 while they are summed; the per-pair FC2
 // rows never reach memory.  The finalize kernel rounds the sums to BF16.
 //
-// Warp roles: warp 0 issues TMA, warp 1 owns TMEM and issues MMAs, the
-// remaining warps drain TMEM (each 32-lane quarter by several warps taking
-// alternate 16-column chunks).  Persistent CTAs stride over the work units;
+// Warp roles (FC2; FC1's are listed with its constants): warp 0 issues TMA,
+// warp 1 owns TMEM and issues MMAs, the remaining warps drain TMEM (each
+// 32-lane quarter by several warps taking alternate 16-column chunks).  In
+// FC1 warps 0 and 1 gather the X rows.  Persistent CTAs stride over the work units;
 // the stage ring and the barrier phases carry across units.  Every wait is
 // bounded.
 #include "nvfp4.cuh"

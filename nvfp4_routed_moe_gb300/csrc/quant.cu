@@ -1,6 +1,7 @@
-// quant.cu -- activation quantization with token gather, the BF16 finalize,
-// weight preparation into the kernel layout, and the test kernels that expose
-// the device quantizer and codecs.
+// quant.cu -- activation quantization (token-major codes, block scales laid
+// out for the padded expanded rows), the BF16 finalize, weight preparation
+// into the kernel layout, and the test kernels that expose the device
+// quantizer and codecs.
 #include <cuda_bf16.h>
 
 #include "nvfp4.cuh"
