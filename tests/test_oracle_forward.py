@@ -117,6 +117,29 @@ def test_token_permutation_equivariance(tiny):
     np.testing.assert_array_equal(out2, out[perm])
 
 
+def test_route_weights_enter_linearly(tiny):
+    """The combine is linear in the route weights: doubling every weight
+    doubles every output exactly (a power-of-two scale commutes with the fp64
+    sum and the one BF16 rounding), and splitting the weights w = w1 + w2
+    (both exact in BF16) gives out(w1) + out(w2) up to the BF16 roundings."""
+    inp = cases.prepare_tiny(0)
+    w = gen.bf16_bits_to_f32(inp.route_weights).astype(np.float64)
+    out = gen.bf16_bits_to_f32(cases.run_oracle(inp)).astype(np.float64)
+    inp.route_weights = gen.f32_to_bf16_bits((2.0 * w).astype(np.float32))
+    out2 = gen.bf16_bits_to_f32(cases.run_oracle(inp)).astype(np.float64)
+    np.testing.assert_array_equal(out2, 2.0 * out)
+    w1 = gen.bf16_bits_to_f32(gen.f32_to_bf16_bits((0.75 * w).astype(np.float32))).astype(np.float64)
+    w2 = w - w1
+    assert np.array_equal(gen.bf16_bits_to_f32(gen.f32_to_bf16_bits(w2.astype(np.float32))), w2)
+    parts = []
+    for wp in (w1, w2):
+        inp.route_weights = gen.f32_to_bf16_bits(wp.astype(np.float32))
+        parts.append(gen.bf16_bits_to_f32(cases.run_oracle(inp)).astype(np.float64))
+    # each output carries at most half a BF16 ulp of rounding (relative 2^-9)
+    bound = 2.0 ** -8 * (np.abs(out) + np.abs(parts[0]) + np.abs(parts[1])) + 1e-30
+    assert (np.abs(parts[0] + parts[1] - out) <= bound).all()
+
+
 def test_exact_arithmetic_case():
     """Power-of-two scales and small codes: every sum is exact, so the whole
     forward is computable by hand (here: in fp64 with exact integers)."""
