@@ -302,6 +302,38 @@ def test_full_shape_sampled_tokens(full_model, T, routing, big):
     np.testing.assert_array_equal(ws_i32(ws, lay.count, inp.E), counts)
 
 
+def test_full_shape_streamed_chunks(full_model):
+    """The chunk-ready streaming front end at full shape: T = 4096 published
+    as four 1024-token chunks through a two-slot ring, each routed on its own;
+    sampled tokens match the oracle and the whole output matches the batch
+    forward within the tolerance."""
+    minp, m = full_model
+    T, C = 4096, 1024
+    inp = _full_case(minp, T, "uniform", seed=3)
+    x, ids, rw = dev(inp.x, torch.bfloat16), dev(inp.expert_ids), dev(inp.route_weights, torch.bfloat16)
+    qX = dev(np.array([inp.qX], np.float32))
+    cfg = api.moe_stream_ring_t(2, C)
+    ring = torch.empty(api.moe_stream_ring_size(m.shape, cfg), dtype=torch.uint8, device="cuda")
+    api.moe_stream_ring_init(m.shape, cfg, ring)
+    ws = m.workspace(C)
+    api.moe_prepare_workspace(m.shape, ws, C)
+    out = torch.empty((T, inp.H), dtype=torch.bfloat16, device="cuda")
+    api.moe_stream_begin(m.shape, cfg, ring)
+    for c in range(T // C):
+        sl = slice(c * C, (c + 1) * C)
+        api.moe_stream_publish(m.shape, cfg, ring, c, c * C, C, api.STREAM_ROUTE | api.STREAM_LAYOUT, x[sl], ids[sl],
+                               rw[sl])
+        api.moe_stream_forward(m.shape, cfg, ring, c, m.w13, m.sf13, m.w2, m.sf2, qX, m.dXdW13, m.qA, m.dAdW2,
+                               None, None, ws, out)
+    torch.cuda.synchronize()
+    assert api.moe_read_status(ws) == (0, 0)
+    assert api.moe_stream_read_status(ring) == 0
+    sample = np.unique(np.concatenate([[0, C - 1, C, T - 1], np.random.default_rng(9).choice(T, 12, replace=False)]))
+    assert_close(out_bits(out)[sample], cases.run_oracle(inp, tokens=sample), "streamed full shape")
+    batch, _ = m.forward(x, ids, rw, qX=qX)
+    assert_close(out_bits(out), out_bits(batch), "streamed vs batch, full shape")
+
+
 # ------------------------------------------------------------- expert slices
 # The forward of one expert-parallel rank ("npu_moe_init_routing_v2",
 # active_expert_range): the rank holds experts [begin, begin + E_local) and
