@@ -101,15 +101,25 @@ __global__ void __launch_bounds__(256) sf_atoms_kernel(const SfAtomArgs a) {
       src[c] = (f >= 0 && f < a.num_pairs) ? reinterpret_cast<const uint4*>(a.sft + (int64_t)(f / a.k) * G) : nullptr;
     }
     uint4* dst = atoms + tile * NA4 * 32 + lane;
-#pragma unroll 2
-    for (int m = 0; m < NM; ++m) {
-      uint4 v[4];
+    // seven 256-column steps (28 gathered 16-byte loads per lane) in flight
+    // before their atoms are written
+    constexpr int kB = 7;
+    for (int m0 = 0; m0 < NM; m0 += kB) {
+      uint4 v[kB][4];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) v[c] = src[c] ? __ldg(src[c] + m) : make_uint4(0u, 0u, 0u, 0u);
-      dst[(4 * m + 0) * 32] = make_uint4(v[0].x, v[1].x, v[2].x, v[3].x);
-      dst[(4 * m + 1) * 32] = make_uint4(v[0].y, v[1].y, v[2].y, v[3].y);
-      dst[(4 * m + 2) * 32] = make_uint4(v[0].z, v[1].z, v[2].z, v[3].z);
-      dst[(4 * m + 3) * 32] = make_uint4(v[0].w, v[1].w, v[2].w, v[3].w);
+      for (int i = 0; i < kB; ++i)
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          v[i][c] = (m0 + i < NM && src[c]) ? __ldg(src[c] + m0 + i) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+      for (int i = 0; i < kB; ++i) {
+        if (m0 + i >= NM) break;
+        uint4* d = dst + 4 * (m0 + i) * 32;
+        d[0] = make_uint4(v[i][0].x, v[i][1].x, v[i][2].x, v[i][3].x);
+        d[32] = make_uint4(v[i][0].y, v[i][1].y, v[i][2].y, v[i][3].y);
+        d[64] = make_uint4(v[i][0].z, v[i][1].z, v[i][2].z, v[i][3].z);
+        d[96] = make_uint4(v[i][0].w, v[i][1].w, v[i][2].w, v[i][3].w);
+      }
     }
   }
 }

@@ -40,6 +40,8 @@ __device__ __forceinline__ uint32_t lanemask_lt() {
 constexpr int kIdBatch = 8;
 
 // Pass 1: per-warp histogram of ids[begin, end) into hist_w[E] (shared).
+// Counts do not depend on order, so each lane adds its own pair with a
+// shared-memory atomic.
 __device__ __forceinline__ void warp_histogram(const int32_t* ids, int64_t begin, int64_t end, int E,
                                                int* hist_w, int id_base) {
   const int lane = threadIdx.x & 31;
@@ -48,21 +50,12 @@ __device__ __forceinline__ void warp_histogram(const int32_t* ids, int64_t begin
 #pragma unroll
     for (int j = 0; j < kIdBatch; ++j) {
       const int64_t f = base0 + j * 32 + lane;
-      raw[j] = f < end ? ids[f] : 0;   // generic load: ids may be in shared memory
+      raw[j] = f < end ? ids[f] : id_base - 1;   // generic load: ids may be in shared memory
     }
 #pragma unroll
     for (int j = 0; j < kIdBatch; ++j) {
-      if (base0 + j * 32 >= end) break;   // warp-uniform: the run is done
-      const int64_t f = base0 + j * 32 + lane;
-      const bool in = f < end;
       const int id = raw[j] - id_base;
-      const bool ok = in && id >= 0 && id < E;
-      const uint32_t okmask = __ballot_sync(0xffffffffu, ok);
-      if (ok) {
-        const uint32_t peers = __match_any_sync(okmask, id);
-        if (lane == __ffs(peers) - 1) hist_w[id] += __popc(peers);
-      }
-      __syncwarp();
+      if (id >= 0 && id < E) atomicAdd(hist_w + id, 1);
     }
   }
 }
@@ -296,31 +289,34 @@ __global__ void __launch_bounds__(256) route_hist_kernel(const RouteArgs a) {
   __syncthreads();
   if (!s_last) return;
   __threadfence();
-  // Each thread scans the block counts of its experts, two experts and 32
-  // blocks at a time: 64 independent loads in flight per step.
-  for (int e0 = tid; e0 < E; e0 += 512) {
-    const int e1 = e0 + 256;
-    int run0 = 0, run1 = 0;
+  // Each thread scans the block counts of experts tid + 256 j (j < 4; E <=
+  // 1024 here), 32 blocks at a time: 128 independent loads in flight per step.
+  {
+    int run[4] = {0, 0, 0, 0};
     for (int blk0 = 0; blk0 < a.nblk; blk0 += 32) {
-      int c0[32], c1[32];
+      int c[4][32];
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
         const bool inb = blk0 + j < a.nblk;
-        c0[j] = inb ? __ldcg(&a.blockhist[(size_t)(blk0 + j) * E + e0]) : 0;
-        c1[j] = inb && e1 < E ? __ldcg(&a.blockhist[(size_t)(blk0 + j) * E + e1]) : 0;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int e = tid + 256 * q;
+          c[q][j] = inb && e < E ? __ldcg(&a.blockhist[(size_t)(blk0 + j) * E + e]) : 0;
+        }
       }
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
-        if (blk0 + j < a.nblk) {
-          a.blockhist[(size_t)(blk0 + j) * E + e0] = run0;
-          if (e1 < E) a.blockhist[(size_t)(blk0 + j) * E + e1] = run1;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int e = tid + 256 * q;
+          if (blk0 + j < a.nblk && e < E) a.blockhist[(size_t)(blk0 + j) * E + e] = run[q];
+          run[q] += c[q][j];
         }
-        run0 += c0[j];
-        run1 += c1[j];
       }
     }
-    s_cnt[e0] = run0;
-    if (e1 < E) s_cnt[e1] = run1;
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      if (tid + 256 * q < E) s_cnt[tid + 256 * q] = run[q];
   }
   __syncthreads();
   scan_experts<256>(a, s_cnt, s_offs, s_poffs, s_tmp);
