@@ -464,6 +464,8 @@ static moe_status_t forward_impl(const moe_shape_t* shape, int32_t expert_begin,
     sa.prow_pair = ra.prow_pair;
     sa.tt_list = ra.tt_list;
     sa.hdr = ra.hdr;
+    sa.route_w = qa.route_w;
+    sa.wrow = qa.wrow;
     sa.sfx = reinterpret_cast<uint32_t*>(w + L.sfx);
     sa.num_pairs = P;
     sa.H = s.H;

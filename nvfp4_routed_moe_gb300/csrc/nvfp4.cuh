@@ -74,11 +74,31 @@ __device__ __forceinline__ float tanh_dev(float y) {
   return copysignf(t, y);
 }
 
+// e^x by Cody-Waite range reduction (W. J. Cody and W. Waite, "Software
+// Manual for the Elementary Functions", 1980): x log2(e) = n + f with n an
+// integer and f in [-1/2, 1/2] computed with log2(e) split into two fp32
+// parts, so the error of f no longer grows with |x|; e^x = 2^f 2^n, 2^f from
+// the hardware base-2 exponential and 2^n from exponent bits.  Relative error
+// a few 1e-7 (the hardware exponential's) over the whole fp32 range; +inf
+// above about 88.7, 0 below about -87.3 (flushed), NaN for NaN.
+__device__ __forceinline__ float exp_cw(float x) {
+  constexpr float kLog2eHi = 1.44269502162933349609375f;   // fp32 nearest to log2(e)
+  constexpr float kLog2eLo = 1.92596298909109e-08f;        // log2(e) - kLog2eHi
+  const float t = fminf(fmaxf(x * kLog2eHi, -126.0f), 128.0f);
+  const float n = rintf(t);
+  const float f = fmaf(x, kLog2eHi, -n) + x * kLog2eLo;
+  float p;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(p) : "f"(f));
+  return p * __int_as_float(((int)n + 127) << 23);
+}
+
 // SiTU ("Cake SiTU backend": default (4*tanh(g/4)*sigmoid(g))*(25*tanh(u/25)),
 // per-expert gate and linear smoothing parameters beta, lambda), with the
-// reciprocals 1/beta and 1/lambda supplied by the caller.
+// reciprocals 1/beta and 1/lambda supplied by the caller.  The sigmoid divides
+// approximately (2 ulp; exactly 0 once 1 + e^{-g} passes 2^126, where the
+// sigmoid is below 1e-38).
 __device__ __forceinline__ float situ_f32(float g, float u, float beta, float inv_beta, float lam, float inv_lam) {
-  const float sig = __frcp_rn(1.0f + expf(-g));
+  const float sig = __fdividef(1.0f, 1.0f + exp_cw(-g));
   const float gate = beta * tanh_dev(g * inv_beta) * sig;
   const float lin = lam * tanh_dev(u * inv_lam);
   return gate * lin;

@@ -210,7 +210,7 @@ struct QuantXArgs {
   const uint16_t* x;        // [T, H] bf16
   const int32_t* row_pos;   // [T*k] padded expanded row of each pair, -1 if not routed
   const uint16_t* route_w;  // [T*k] bf16 route weights
-  float* wrow;              // [Ppad] out: route weight of each padded row (fp32)
+  float* wrow;              // [Ppad] out: route weight of each padded row (fp32), when sft is null
   float* acc;               // [T, H] out: zeroed
   const float* qX;          // [1]
   uint8_t* xq;              // [T, H/2] token-major codes
@@ -227,6 +227,8 @@ struct SfAtomArgs {
   const int32_t* prow_pair; // [Ppad] flat pair of each padded row
   const int32_t* tt_list;   // int4 {expert, row0, rows, 0} per 128-row tile, in row order
   const int32_t* hdr;
+  const uint16_t* route_w;  // [T*k] bf16 route weights
+  float* wrow;              // [Ppad] out: route weight of each routed padded row (fp32)
   uint32_t* sfx;            // atom layout
   int64_t num_pairs;
   int32_t H, k, max_tiles;

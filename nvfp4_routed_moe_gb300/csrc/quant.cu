@@ -34,12 +34,17 @@ __global__ void __launch_bounds__(256) quant_x_kernel(const QuantXArgs a) {
   const int64_t w = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
   const int64_t t = w / S;
   const int sl = (int)(w - t * S);
-  pdl_wait();
+  // The token-major work (codes, token-major scales, the accumulator row)
+  // needs nothing from routing, so it does not wait for it: the routing
+  // kernel before this one starts only once the previous forward has
+  // completed, so nothing still reads the codes or the accumulator.  Only
+  // the row-position work below waits.  With token-major scales the route
+  // weights are placed by the scale-atom kernel, and one thread waits so
+  // that this kernel still completes after routing.
   pdl_launch_dependents();
+  if (a.sft && blockIdx.x == 0 && threadIdx.x == 0) pdl_wait();
   if (t >= a.T) return;
   const float q = __ldg(a.qX);
-  const int rp = (lane < a.k) ? a.row_pos[t * a.k + lane] : -1;
-  if (sl == 0 && rp >= 0 && rp < a.max_rows) a.wrow[rp] = bf16_bits_to_f32(a.route_w[t * a.k + lane]);
   // this slice's share of the token's accumulator row
   float4* accr = reinterpret_cast<float4*>(a.acc + t * H);
   for (int i = sl * 32 * 4 + lane; i < min(H / 4, (sl + 1) * 32 * 4); i += 32) accr[i] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -68,6 +73,9 @@ __global__ void __launch_bounds__(256) quant_x_kernel(const QuantXArgs a) {
   if (a.sft && valid && (lane & 3) == 0) *reinterpret_cast<uint32_t*>(a.sft + t * G + g) = word;
   if (valid) *reinterpret_cast<uint2*>(a.xq + (size_t)t * (H / 2) + g * 8) = packed;
   if (a.sft) return;
+  pdl_wait();   // routing's row positions
+  const int rp = (lane < a.k) ? a.row_pos[t * a.k + lane] : -1;
+  if (sl == 0 && rp >= 0 && rp < a.max_rows) a.wrow[rp] = bf16_bits_to_f32(a.route_w[t * a.k + lane]);
   for (int j = 0; j < a.k; ++j) {
     const int row = __shfl_sync(0xffffffffu, rp, j);
     if (row < 0 || row >= a.max_rows || !valid) continue;
@@ -98,7 +106,9 @@ __global__ void __launch_bounds__(256) sf_atoms_kernel(const SfAtomArgs a) {
     for (int c = 0; c < 4; ++c) {
       const int r = lane + 32 * c;
       const int f = r < rows ? __ldg(a.prow_pair + tile * kTileRows + r) : -1;
-      src[c] = (f >= 0 && f < a.num_pairs) ? reinterpret_cast<const uint4*>(a.sft + (int64_t)(f / a.k) * G) : nullptr;
+      const bool ok = f >= 0 && f < a.num_pairs;
+      src[c] = ok ? reinterpret_cast<const uint4*>(a.sft + (int64_t)(f / a.k) * G) : nullptr;
+      if (ok) a.wrow[tile * kTileRows + r] = bf16_bits_to_f32(__ldg(a.route_w + f));
     }
     uint4* dst = atoms + tile * NA4 * 32 + lane;
     // seven 256-column steps (28 gathered 16-byte loads per lane) in flight

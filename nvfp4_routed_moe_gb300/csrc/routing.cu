@@ -330,8 +330,11 @@ __global__ void __launch_bounds__(256) route_rank_kernel(const RouteArgs a) {
   int* s_offs = hist + 8 * E;     // [E]
   int* s_poffs = s_offs + E;      // [E]
   const int tid = threadIdx.x, warp = tid >> 5;
-  pdl_wait();
+  // The X quantization may start at once: this kernel itself starts only
+  // after the histogram kernel has waited for the previous forward, and
+  // the quantization reads nothing that routing writes before its own wait.
   pdl_launch_dependents();
+  pdl_wait();
   if (blockIdx.x == 0 && tid == 0) a.hdr[HDR_DONE] = 0;  // re-arm the ticket for the next call
   for (int i = tid; i < 8 * E; i += 256) hist[i] = 0;
   for (int e = tid; e < E; e += 256) {
