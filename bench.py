@@ -130,19 +130,32 @@ KERNEL_BYTES = {"fc1": (fc1_bytes, "n_active*1548288 + T*2016 + T*k*216"),
                 "fc2": (fc2_bytes, "n_active*774144 + T*k*216 + T*H*4")}
 
 
+# Sources compiled into the GEMM kernels (the file and everything it includes).
+GEMM_SOURCES = ("nvfp4_routed_moe_gb300/csrc/gemm.cu", "nvfp4_routed_moe_gb300/csrc/nvfp4.cuh",
+                "nvfp4_routed_moe_gb300/csrc/ptx.cuh", "nvfp4_routed_moe_gb300/csrc/plan.h",
+                "include/nvfp4moe.h")
+
+
+def gemm_sources_sha1():
+    """SHA-1 over the GEMM kernels' sources, in GEMM_SOURCES order."""
+    h = hashlib.sha1()
+    for rel in GEMM_SOURCES:
+        h.update(open(os.path.join(ROOT, rel), "rb").read())
+    return h.hexdigest()
+
+
 def traffic_from_profile(kernel, workload):
     """DRAM bytes per launch from the committed ncu summary of this kernel
-    and workload, used only while the kernel source is unchanged since the
+    and workload, used only while the kernel sources are unchanged since the
     capture."""
     path = os.path.join(ROOT, "profiles", f"{kernel}_kernel_{workload}.md")
     try:
         kv = {}
         for line in open(path).read().splitlines():
-            if line.startswith(("gemm_cu_sha1", "dram_bytes_per_launch")) and "=" in line:
+            if line.startswith(("gemm_sources_sha1", "dram_bytes_per_launch")) and "=" in line:
                 k, v = line.split("=", 1)
                 kv[k.strip()] = v.strip().strip("`")
-        sha = hashlib.sha1(open(os.path.join(ROOT, "nvfp4_routed_moe_gb300", "csrc", "gemm.cu"), "rb").read())
-        if kv.get("gemm_cu_sha1") == sha.hexdigest():
+        if kv.get("gemm_sources_sha1") == gemm_sources_sha1():
             return float(kv["dram_bytes_per_launch"])
     except Exception:
         pass
