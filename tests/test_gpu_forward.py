@@ -302,6 +302,30 @@ def test_full_shape_sampled_tokens(full_model, T, routing, big):
     np.testing.assert_array_equal(ws_i32(ws, lay.count, inp.E), counts)
 
 
+
+@pytest.mark.parametrize("T", [2048, 16384])
+def test_back_to_back_forwards_share_a_workspace(full_model, T):
+    """Two forwards with different inputs run back to back on one workspace,
+    with no synchronization between them: the second one quantizes X and
+    zeroes the accumulator rows ahead of its own routing, which must still
+    come after the first one's finalize.  Both outputs match the oracle on
+    sampled tokens (T=2048: block scales placed by the X quantizer; 16384:
+    by the scale-atom kernel)."""
+    minp, m = full_model
+    cases_ab = (_full_case(minp, T, "uniform", seed=70 + T), _full_case(minp, T, "zipf", seed=71 + T))
+    ws = m.workspace(T)
+    api.moe_prepare_workspace(m.shape, ws, T)
+    staged = [(dev(c.x, torch.bfloat16), dev(c.expert_ids), dev(c.route_weights, torch.bfloat16),
+               dev(np.array([c.qX], np.float32))) for c in cases_ab]
+    torch.cuda.synchronize()
+    outs = [m.forward(x, ids, rw, ws=ws, T=T, prepare=False, qX=qx)[0] for x, ids, rw, qx in staged]
+    torch.cuda.synchronize()
+    assert api.moe_read_status(ws) == (0, 0)
+    rs = np.random.default_rng(T)
+    sample = np.unique(np.concatenate([[0, T - 1], rs.choice(T, 10, replace=False)]))
+    for c, out, name in zip(cases_ab, outs, ("first", "second")):
+        assert_close(out_bits(out)[sample], cases.run_oracle(c, tokens=sample), f"back to back, {name}, T={T}")
+
 def test_full_shape_streamed_chunks(full_model):
     """The chunk-ready streaming front end at full shape: T = 4096 published
     as four 1024-token chunks through a two-slot ring, each routed on its own;
