@@ -61,7 +61,9 @@ __device__ __forceinline__ void warp_histogram(const int32_t* ids, int64_t begin
 }
 
 // Pass 2: hand out sorted slots.  base_w[e] holds the next slot of expert e
-// for this warp; offs/poffs are the expert's first dropless / padded row.
+// for this warp, counted from the expert's first row when kRelative (else
+// absolute); offs/poffs are the expert's first dropless / padded row.
+template <bool kRelative>
 __device__ __forceinline__ int warp_rank(const RouteArgs& a, const int32_t* ids, int64_t begin, int64_t end,
                                          int* base_w, const int* s_offs, const int* s_poffs) {
   const int lane = threadIdx.x & 31;
@@ -85,9 +87,10 @@ __device__ __forceinline__ int warp_rank(const RouteArgs& a, const int32_t* ids,
     if (ok) {
       const uint32_t peers = __match_any_sync(okmask, id);
       const int leader = __ffs(peers) - 1;
-      const int slot = base_w[id] + __popc(peers & lanemask_lt());
+      const int rank = base_w[id] + __popc(peers & lanemask_lt());   // within the expert (kRelative) or absolute
       __syncwarp(okmask);
       if (lane == leader) base_w[id] += __popc(peers);
+      const int slot = kRelative ? s_offs[id] + rank : rank;
       a.sorted_row[slot] = (int32_t)f;
       a.gather[f] = slot;
       const int prow = s_poffs[id] + (slot - s_offs[id]);
@@ -110,15 +113,18 @@ __device__ __forceinline__ int warp_rank(const RouteArgs& a, const int32_t* ids,
 template <int NT>
 __device__ void scan_experts(const RouteArgs& a, const int* cnt_s, int* s_offs, int* s_poffs, int* s_tmp) {
   constexpr int NWARP = NT / 32;
+  constexpr int PER = (kMaxExperts + NT - 1) / NT;   // experts per thread, at most
+  static_assert(PER <= 4, "E <= NT * 4");
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int E = a.E;
   const int per = (E + NT - 1) / NT;  // experts per thread (consecutive)
   const int e0 = tid * per;
-  int c[4] = {0, 0, 0, 0};
+  int c[PER];
   int v0 = 0, v1 = 0, v2 = 0;
-  for (int i = 0; i < per; ++i) {
+#pragma unroll
+  for (int i = 0; i < PER; ++i) {
     const int e = e0 + i;
-    const int n = (e < E) ? cnt_s[e] : 0;
+    const int n = (i < per && e < E) ? cnt_s[e] : 0;
     c[i] = n;
     v0 += n;
     v1 += (n + kTileRows - 1) / kTileRows * kTileRows;
@@ -142,7 +148,8 @@ __device__ void scan_experts(const RouteArgs& a, const int* cnt_s, int* s_offs, 
     s_tmp[warp * 3 + 2] = i2;
   }
   int mx = 0;   // largest expert group, for the GEMMs' accumulator sizing
-  for (int i = 0; i < per; ++i) mx = max(mx, c[i]);
+#pragma unroll
+  for (int i = 0; i < PER; ++i) mx = max(mx, c[i]);
   mx = __reduce_max_sync(0xffffffffu, mx);
   if (lane == 0) s_tmp[208 + warp] = mx;
   __syncthreads();
@@ -172,9 +179,10 @@ __device__ void scan_experts(const RouteArgs& a, const int* cnt_s, int* s_offs, 
   const int wb1 = warp ? s_tmp[96 + (warp - 1) * 3 + 1] : 0;
   const int wb2 = warp ? s_tmp[96 + (warp - 1) * 3 + 2] : 0;
   int o0 = wb0 + i0 - v0, o1 = wb1 + i1 - v1, o2 = wb2 + i2 - v2;  // exclusive
-  for (int i = 0; i < per; ++i) {
+#pragma unroll
+  for (int i = 0; i < PER; ++i) {
     const int e = e0 + i;
-    if (e < E) {
+    if (i < per && e < E) {
       const int n = c[i];
       const int nt = (n + kTileRows - 1) / kTileRows;
       s_offs[e] = o0;
@@ -244,10 +252,8 @@ __global__ void __launch_bounds__(1024, 1) route_small_kernel(const RouteArgs a)
     s_cnt[e] = run;
   }
   __syncthreads();
-  scan_experts<1024>(a, s_cnt, s_offs, s_poffs, s_tmp);
-  for (int i = tid; i < NHW * E; i += 1024) hist[i] += s_offs[i % E];
-  __syncthreads();
-  const int invalid = warp < NHW ? warp_rank(a, s_ids, b, en, hist + warp * E, s_offs, s_poffs) : 0;
+  scan_experts<1024>(a, s_cnt, s_offs, s_poffs, s_tmp);   // ends with a block barrier
+  const int invalid = warp < NHW ? warp_rank<true>(a, s_ids, b, en, hist + warp * E, s_offs, s_poffs) : 0;
   const int nvalid = s_tmp[200];
   for (int64_t i = nvalid + tid; i < a.P; i += 1024) a.sorted_row[i] = -1;
   if (invalid) {
@@ -356,7 +362,7 @@ __global__ void __launch_bounds__(256) route_rank_kernel(const RouteArgs a) {
     }
   }
   __syncthreads();
-  const int invalid = warp_rank(a, a.ids, b, en, hist + warp * E, s_offs, s_poffs);
+  const int invalid = warp_rank<false>(a, a.ids, b, en, hist + warp * E, s_offs, s_poffs);
   const int nvalid = a.offs[E];
   const int64_t t0 = max((int64_t)nvalid, cb), t1 = min(a.P, cb + a.chunk);
   for (int64_t i = t0 + tid; i < t1; i += 256) a.sorted_row[i] = -1;
