@@ -83,13 +83,20 @@ def init_routing_sweep(shp, flush, dev):
     ws = torch.empty(api.moe_workspace_size(shp, rows), dtype=torch.uint8, device="cuda")
     api.moe_prepare_workspace(shp, ws, rows)
     res = {}
-    for name, C in (("dropless", 0), ("drop_pad_C96", 96)):
-        n_out = E * C if C else rows * k
-        ex = torch.empty((n_out, H), dtype=torch.int8, device="cuda")
+    s_static = torch.tensor([0.5], dtype=torch.float32, device="cuda")
+    o_static = torch.tensor([1.0], dtype=torch.float32, device="cuda")
+    lo, hi = E // 8, 2 * E // 8   # one of eight expert-parallel ranks
+    in_range = int(((b.expert_ids >= lo) & (b.expert_ids < hi)).sum())
+    configs = (("dropless", 0, dict(quant_mode=1), rows * k),
+               ("drop_pad_C96", 96, dict(drop_pad=1, expert_capacity=96, quant_mode=1), E * 96),
+               ("static_int8", 0, dict(quant_mode=0, scale=s_static, offset=o_static), rows * k),
+               ("range_key_value", 0, dict(quant_mode=1, expert_start=lo, expert_end=hi, tokens_num_type=2), in_range))
+    for name, C, kw, n_out in configs:
+        ex = torch.empty((max(n_out, 1) if C else rows * k, H), dtype=torch.int8, device="cuda")
         idx = torch.empty(rows * k, dtype=torch.int32, device="cuda")
-        tok = torch.empty(E, dtype=torch.int32, device="cuda")
-        sc = torch.empty(n_out, dtype=torch.float32, device="cuda")
-        opts = api.routing_opts(drop_pad=1 if C else 0, expert_capacity=C, quant_mode=1)
+        tok = torch.empty(2 * E, dtype=torch.int32, device="cuda")
+        sc = torch.empty(ex.shape[0], dtype=torch.float32, device="cuda")
+        opts = api.routing_opts(**kw)
         call = lambda: api.moe_init_routing(shp, rows, x, ids, opts, ex, idx, tok, sc, ws)
         for _ in range(3):
             call()
@@ -102,7 +109,85 @@ def init_routing_sweep(shp, flush, dev):
         torch.cuda.synchronize()
         t_ms = statistics.median([a.elapsed_time(c) for a, c in evs])
         byt = rows * H * 2 + rows * k * 4 + n_out * H + n_out * 4 + rows * k * 4 + E * 4
-        res[name] = {"rows": rows, "ms": round(t_ms, 4), "bytes": byt, "gb_per_s": byt / (t_ms * 1e-3) / 1e9}
+        res[name] = {"rows": rows, "rows_out": n_out, "ms": round(t_ms, 4), "bytes": byt,
+                     "gb_per_s": byt / (t_ms * 1e-3) / 1e9}
+    return res
+
+
+def median_ms(call, flush, n=20):
+    """Median CUDA-event time of `call` over n runs, L2 flushed before each."""
+    import torch
+    for _ in range(3):
+        call()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    for a, c in evs:
+        flush.fill_(1)
+        a.record()
+        call()
+        c.record()
+    torch.cuda.synchronize()
+    return statistics.median([a.elapsed_time(c) for a, c in evs])
+
+
+def next_rows_sweep(shp, flush, dev, w, scales, winp, peak):
+    """The widened paths at T = 4096 (uniform ids), each beside the plain
+    forward of the same batch: the chunk-ready streaming front end (four
+    1024-token chunks through a two-slot ring, publish and forward on one
+    stream), one expert-parallel rank's slice (the first 112 of 896 experts,
+    its own prepared weights), and per-expert SiTU parameters."""
+    import torch
+    from nvfp4_routed_moe_gb300 import api
+    T, C, S = 4096, 1024, 2
+    b = gen.full(300, T=T, routing="uniform", weights=False, E=shp.num_experts)
+    x, ids, rw = dev(b.x, torch.bfloat16), dev(b.expert_ids), dev(b.route_weights, torch.bfloat16)
+    qx = dev(np.array([b.qX], np.float32))
+    out = torch.empty((T, shp.hidden), dtype=torch.bfloat16, device="cuda")
+    ws = torch.empty(api.moe_workspace_size(shp, T), dtype=torch.uint8, device="cuda")
+    api.moe_prepare_workspace(shp, ws, T)
+    plain = lambda: api.moe_forward(shp, T, x, ids, rw, *w, qx, *scales, None, None, ws, out)
+    t_plain = median_ms(plain, flush)
+    res = {"T": T, "plain_ms": round(t_plain, 4)}
+
+    cfg = api.moe_stream_ring_t(S, C)
+    ring = torch.empty(api.moe_stream_ring_size(shp, cfg), dtype=torch.uint8, device="cuda")
+    api.moe_stream_ring_init(shp, cfg, ring)
+    ws_c = torch.empty(api.moe_workspace_size(shp, C), dtype=torch.uint8, device="cuda")
+    api.moe_prepare_workspace(shp, ws_c, C)
+
+    def streamed():
+        api.moe_stream_begin(shp, cfg, ring)
+        for c, base in enumerate(range(0, T, C)):
+            api.moe_stream_publish(shp, cfg, ring, c, base, C, api.STREAM_ROUTE | api.STREAM_LAYOUT,
+                                   x[base:base + C], ids[base:base + C], rw[base:base + C])
+            api.moe_stream_forward(shp, cfg, ring, c, *w, qx, *scales, None, None, ws_c, out)
+    t_st = median_ms(streamed, flush)
+    assert api.moe_read_status(ws_c) == (0, 0) and api.moe_stream_read_status(ring) == 0
+    res["stream"] = {"chunk": C, "slots": S, "ms": round(t_st, 4), "tokens_per_s": T / (t_st * 1e-3),
+                     "vs_plain": t_plain / t_st}
+    del ring, ws_c
+
+    EL, lo = shp.num_experts // 8, 0
+    shp_l = api.shape(shp.hidden, shp.inter, EL, shp.top_k)
+    w_l = [torch.empty(n, dtype=torch.uint8, device="cuda") for n in api.moe_prepared_weight_bytes(shp_l)]
+    api.moe_prepare_weights(shp_l, dev(winp.w13[:EL]), dev(winp.sf13[:EL]), dev(winp.w2[:EL]), dev(winp.sf2[:EL]),
+                            *w_l)
+    sc_l = [dev(winp.dXdW13[:EL]), dev(winp.qA[:EL]), dev(winp.dAdW2[:EL])]
+    ws_l = torch.empty(api.moe_workspace_size(shp_l, T), dtype=torch.uint8, device="cuda")
+    api.moe_prepare_workspace(shp_l, ws_l, T)
+    local = lambda: api.moe_forward_local_experts(shp_l, lo, T, x, ids, rw, *w_l, qx, *sc_l, None, None, ws_l, out)
+    t_loc = median_ms(local, flush)
+    pairs = int(((b.expert_ids >= lo) & (b.expert_ids < lo + EL)).sum())
+    byt = EL * (FC1_BYTES_PER_EXPERT + FC2_BYTES_PER_EXPERT) + 2 * T * H * 2 + T * K * 6
+    res["local_experts"] = {"experts": EL, "pairs": pairs, "ms": round(t_loc, 4),
+                            "hbm_frac": byt / (t_loc * 1e-3) / 1e9 / peak}
+    del w_l, ws_l
+
+    rs = np.random.default_rng(4)
+    beta = dev(rs.uniform(1.0, 8.0, shp.num_experts).astype(np.float32))
+    lam = dev(rs.uniform(2.0, 60.0, shp.num_experts).astype(np.float32))
+    situ = lambda: api.moe_forward(shp, T, x, ids, rw, *w, qx, *scales, beta, lam, ws, out)
+    t_situ = median_ms(situ, flush)
+    res["situ_per_expert"] = {"ms": round(t_situ, 4), "vs_plain": t_plain / t_situ}
     return res
 
 
@@ -513,6 +598,7 @@ def main():
                            "fc1_ms": round(st_ms["fc1"] / nc, 4), "fc2_ms": round(st_ms["fc2"] / nc, 4),
                            "fc1_hbm_frac": fc1_bytes(T_s, b["n_active"]) / (st_ms["fc1"] / nc * 1e-3) / 1e9 / peak}
         sweep["init_routing"] = init_routing_sweep(shp, flush, dev)
+        sweep["next_rows"] = next_rows_sweep(shp, flush, dev, w, scales, winp, peak)
         del flush
 
     cpu = None

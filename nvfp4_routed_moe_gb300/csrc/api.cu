@@ -313,9 +313,11 @@ cudaError_t init_routing_enqueue(RouteArgs ra, int32_t base, int32_t range, cons
   cudaError_t err = launch_routing(ra, st, &nl);
   if (err != cudaSuccess) return err;
   // Token-driven move (each token quantized once, written to its pairs' rows)
-  // for the plain options; row-driven (scatter form) for the others.
-  const bool plain = base == 0 && range == shape->num_experts && o->active_num <= 0 && !o->scale &&
-                     o->quant_mode != 0;
+  // for every expert, no Active limit and a row that does not depend on the
+  // expert (static int8's scalar scale and offset, or no input scale);
+  // row-driven (scatter form) for the others.
+  const bool plain = base == 0 && range == shape->num_experts && o->active_num <= 0 &&
+                     (o->quant_mode == 0 || !o->scale);
   float* sc_out = (o->quant_mode == 1 || (o->quant_mode == -1 && o->scale)) ? expanded_scale : nullptr;
   if (plain) {
     InitMoveArgs ma{};
@@ -331,6 +333,8 @@ cudaError_t init_routing_enqueue(RouteArgs ra, int32_t base, int32_t range, cons
     ma.C = o->expert_capacity;
     ma.quant_mode = o->quant_mode;
     ma.row_idx_type = o->row_idx_type;
+    ma.scale = o->scale;
+    ma.offset = o->offset;
     ma.expanded_x = expanded_x;
     ma.expanded_scale = sc_out;
     ma.expanded_row_idx = expanded_row_idx;

@@ -166,6 +166,8 @@ struct InitMoveArgs {
   const int32_t* offs;        // [E] (ws)
   int64_t T;
   int32_t k, E, H, drop_pad, C, quant_mode, row_idx_type;
+  const float* scale;         // quant 0: [1]
+  const float* offset;        // quant 0: [1]
   void* expanded_x;
   float* expanded_scale;
   int32_t* expanded_row_idx;

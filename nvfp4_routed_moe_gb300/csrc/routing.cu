@@ -373,7 +373,8 @@ __global__ void __launch_bounds__(256) route_rank_kernel(const RouteArgs a) {
 }
 
 // -------------------------------------------------------- init-routing move
-// One warp per token: dynamic int8 quant of the row (formula 4) or a bf16
+// One warp per token: dynamic int8 quant of the row (formula 4), static int8
+// with the scalar scale and offset (formula 3), or a bf16
 // copy, written to each destination row of the token's pairs (formula 5).
 __global__ void __launch_bounds__(256) init_move_kernel(const InitMoveArgs a) {
   const int lane = threadIdx.x & 31;
@@ -438,6 +439,27 @@ __global__ void __launch_bounds__(256) init_move_kernel(const InitMoveArgs a) {
     for (int j = 0; j < a.k; ++j) {
       const int d = __shfl_sync(0xffffffffu, dest, j);
       if (d >= 0 && lane == 0 && a.expanded_scale) a.expanded_scale[d] = s;
+    }
+  } else if (a.quant_mode == 0) {
+    // static int8: q = rint(x*scale + offset) in fp32, saturated to [-128, 127]
+    const float sc = __ldg(a.scale), of = __ldg(a.offset);
+    for (int v = lane; v < nvec; v += 32) {
+      const uint4 u = __ldg(xv + v);
+      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+      uint32_t q[2] = {0u, 0u};
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const uint32_t bits = (i & 1) ? (w[i >> 1] >> 16) : (w[i >> 1] & 0xFFFFu);
+        float y = rintf(__fadd_rn(__fmul_rn(bf16_bits_to_f32(bits), sc), of));
+        y = fminf(fmaxf(y, -128.0f), 127.0f);
+        q[i >> 2] |= ((uint32_t)(int)y & 0xFFu) << (8 * (i & 3));
+      }
+      for (int j = 0; j < a.k; ++j) {
+        const int d = __shfl_sync(0xffffffffu, dest, j);
+        if (d >= 0)
+          *reinterpret_cast<uint2*>(static_cast<int8_t*>(a.expanded_x) + (int64_t)d * a.H + v * 8) =
+              make_uint2(q[0], q[1]);
+      }
     }
   } else {
     for (int v = lane; v < nvec; v += 32) {

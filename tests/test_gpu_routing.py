@@ -191,6 +191,10 @@ def test_static_int8():
     ids = gen.draw_ids_uniform(9, 64, 32, 4)
     _check_ex(x, ids, 32, quant_mode=0, scale=[0.37], offset=[-1.5])
     _check_ex(x, ids, 32, quant_mode=0, scale=[40.0], offset=[3.0], drop_pad=1, expert_capacity=6)
+    _check_ex(x, ids, 32, quant_mode=0, scale=[0.37], offset=[-1.5], row_idx_type=1)
+    xb = gen.draw_x(10, 2048, 512)      # 8192 pairs: the multi-block routing path
+    idsb = gen.draw_ids_uniform(10, 2048, 32, 4)
+    _check_ex(xb, idsb, 32, quant_mode=0, scale=[3.0], offset=[0.5])
 
 
 def test_dynamic_int8_with_smooth_scale():
