@@ -312,12 +312,12 @@ cudaError_t init_routing_enqueue(RouteArgs ra, int32_t base, int32_t range, cons
   int nl = 0;
   cudaError_t err = launch_routing(ra, st, &nl);
   if (err != cudaSuccess) return err;
-  // Token-driven move (each token quantized once, written to its pairs' rows)
-  // for every expert, no Active limit and a row that does not depend on the
-  // expert (static int8's scalar scale and offset, or no input scale);
-  // row-driven (scatter form) for the others.
-  const bool plain = base == 0 && range == shape->num_experts && o->active_num <= 0 &&
-                     (o->quant_mode == 0 || !o->scale);
+  // Token-driven move (each token quantized once, written to its routed
+  // pairs' rows; pairs outside the expert range have no row) when there is
+  // no Active limit and the row does not depend on the expert (static int8's
+  // scalar scale and offset, or no input scale); row-driven (scatter form)
+  // for the others.  Drop/pad always spans every expert.
+  const bool plain = o->active_num <= 0 && (o->quant_mode == 0 || !o->scale);
   float* sc_out = (o->quant_mode == 1 || (o->quant_mode == -1 && o->scale)) ? expanded_scale : nullptr;
   if (plain) {
     InitMoveArgs ma{};

@@ -562,6 +562,7 @@ __global__ void __launch_bounds__(256) init_rows_kernel(const InitRowsArgs a) {
 // experts, or key_value rows), expanded_row_idx in scatter form (formula 2)
 // or -- after a row-driven move -- in gather form, availableIdxNum (formula
 // 6), and the zero fill of unfilled drop/pad slots.
+static_assert(4 * 256 >= kMaxExperts, "init_finish: four experts per thread of one 256-thread block");
 __global__ void __launch_bounds__(256) init_finish_kernel(const InitFinishArgs a) {
   pdl_wait();
   pdl_launch_dependents();
@@ -569,21 +570,42 @@ __global__ void __launch_bounds__(256) init_finish_kernel(const InitFinishArgs a
   const int64_t nthr = (int64_t)gridDim.x * 256;
   const int64_t avail = a.hdr[HDR_NVALID];
   if (a.tokens_num_type == 2) {
-    // key_value: (expert id, count) of the routed experts with a non-zero count, in expert order, then zeros
+    // key_value: (expert id, count) of the routed experts with a non-zero
+    // count, in expert order, then zeros.  Thread t holds experts 4t..4t+3
+    // (E <= 1024); a block scan of the non-zero flags places each pair.
     if (blockIdx.x == 0) {
-      __shared__ int s_n;
-      if (threadIdx.x == 0) {
-        int n = 0;
-        for (int e = 0; e < a.E; ++e)
-          if (a.count[e] > 0) {
-            a.tokens_out[2 * n] = a.id_base + e;
-            a.tokens_out[2 * n + 1] = a.count[e];
-            ++n;
-          }
-        s_n = n;
+      __shared__ int s_warp[8];
+      const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+      int cnt[4], nz = 0;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int e = 4 * tid + j;
+        cnt[j] = e < a.E ? a.count[e] : 0;
+        nz += cnt[j] > 0 ? 1 : 0;
       }
+      int incl = nz;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += v;
+      }
+      if (lane == 31) s_warp[warp] = incl;
       __syncthreads();
-      for (int64_t j = 2 * (int64_t)s_n + threadIdx.x; j < 2 * (int64_t)a.E_all; j += 256) a.tokens_out[j] = 0;
+      int before = 0, n = 0;
+#pragma unroll
+      for (int w = 0; w < 8; ++w) {
+        before += w < warp ? s_warp[w] : 0;
+        n += s_warp[w];
+      }
+      int pos = before + incl - nz;
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        if (cnt[j] > 0) {
+          a.tokens_out[2 * pos] = a.id_base + 4 * tid + j;
+          a.tokens_out[2 * pos + 1] = cnt[j];
+          ++pos;
+        }
+      for (int64_t j = 2 * (int64_t)n + tid; j < 2 * (int64_t)a.E_all; j += 256) a.tokens_out[j] = 0;
     }
   } else {
     for (int64_t e = gtid; e < a.E; e += nthr) a.tokens_out[e] = a.tokens_num_type == 1 ? a.count[e] : a.cumsum[e];
