@@ -21,6 +21,15 @@
  *    wait that gave up) never trap: they are OR-ed into a status word in the
  *    workspace, read by moe_read_status.
  *  - Concurrent calls need separate workspace and output buffers.
+ *
+ * Tuning overrides, read from the environment (none is needed; the defaults
+ * are the measured best):
+ *  - NVFP4MOE_PDL=0: launch without programmatic dependent launch (each
+ *    kernel then starts only after its predecessor has finished); read once.
+ *  - NVFP4MOE_FC1_PAIR=1 or 2: W13 tiles per FC1 work unit (default 1 up to
+ *    16 tokens, else 2); read at every forward.
+ *  - NVFP4MOE_ACC_PASS_MB=n: L2 budget in MiB of one FC2 pass over H (the
+ *    accumulator slice T x H/passes fp32; default 64); read at every forward.
  */
 #ifndef NVFP4MOE_H_
 #define NVFP4MOE_H_

@@ -46,8 +46,12 @@ __global__ void fill_f32_kernel(float* p, int n, float v) {
 
 // Programmatic dependent launch: a kernel may be scheduled while its
 // predecessor drains; every kernel of this library waits (griddepcontrol.wait)
-// before it touches memory the predecessor writes.  NVFP4MOE_PDL=0 turns the
-// attribute off.
+// before it reads memory an earlier kernel of the call writes, or writes
+// memory an earlier kernel may still read.  The one exception is by design:
+// the X quantization writes its token-major codes and zeroes the accumulator
+// before its wait, which is safe because the routing kernel before it starts
+// only after the previous forward has completed and touches neither buffer.
+// NVFP4MOE_PDL=0 turns the attribute off.
 static bool pdl_enabled() {
   static const bool on = [] {
     const char* v = std::getenv("NVFP4MOE_PDL");
