@@ -100,6 +100,25 @@ def test_null_and_bad_args_rejected_without_device(L):
     assert L.moe_test_codec_sweep(0xFFFFFFF0, 100, None, None, None, None) == 1
 
 
+
+def test_forward_token_count_alignment_and_capacity_checked_before_launch(L):
+    """An empty or negative batch, a misaligned activation pointer, a batch
+    larger than the workspace holds and a workspace never prepared are each
+    refused on the host with their own status; the (aligned, fake) device
+    pointers are never touched."""
+    shp = api.shape(512, 128, 32, 4)
+    n = api.moe_workspace_size(shp, 64)
+    p = ctypes.c_void_p(1 << 20)
+
+    def fwd(T, x=p):
+        return L.moe_forward(ctypes.byref(shp), T, x, p, p, p, p, p, p, p, p, p, p, None, None, p, n, p, None)
+
+    assert fwd(0) == 1                                  # empty batch
+    assert fwd(-5) == 1
+    assert fwd(16, x=ctypes.c_void_p((1 << 20) + 8)) == 1   # x not 16-byte aligned
+    assert fwd(1 << 20) == 3                            # more tokens than the workspace holds
+    assert fwd(16) == 4                                 # never prepared
+
 def test_launch_count(L):
     assert api.moe_forward_launch_count(api.shape(3584, 384, 896, 16), 1) == 5
     assert api.moe_forward_launch_count(api.shape(3584, 384, 896, 16), 4096) == 6
