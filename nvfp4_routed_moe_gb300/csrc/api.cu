@@ -234,8 +234,10 @@ static RouteArgs route_args(const Shape& s, const WsLayout& L, uint8_t* ws, cons
 }
 
 // Above this many routed pairs the X block scales are written token-major
-// and laid out in atoms by a second kernel.
-constexpr int64_t kSfTwoPassMin = 65536;
+// and laid out in atoms by a second kernel (scattered 4-byte atom writes from
+// the quantizer cost more from here on; the same bound as routing's one-CTA
+// path).
+constexpr int64_t kSfTwoPassMin = 4096;
 // Largest batch for which FC1 works on one W13 tile per unit.
 constexpr int64_t kFc1SingleMaxTokens = 16;
 

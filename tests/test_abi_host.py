@@ -121,5 +121,5 @@ def test_forward_token_count_alignment_and_capacity_checked_before_launch(L):
 
 def test_launch_count(L):
     assert api.moe_forward_launch_count(api.shape(3584, 384, 896, 16), 1) == 5
-    assert api.moe_forward_launch_count(api.shape(3584, 384, 896, 16), 4096) == 6
+    assert api.moe_forward_launch_count(api.shape(3584, 384, 896, 16), 4096) == 7
     assert api.moe_forward_launch_count(api.shape(3584, 384, 896, 16), 16384) == 7

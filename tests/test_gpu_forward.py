@@ -77,7 +77,7 @@ def test_tiny_intermediates(tiny):
 
 
 def test_two_pass_scale_layout_bit_exact():
-    """Above 65536 routed pairs the X block scales are written per token and
+    """Above 4096 routed pairs the X block scales are written per token and
     then laid out in atoms by a second pass.  On sampled tiles (and the last,
     partly filled one) the atoms equal the oracle's scales of each row's token
     scattered through the oracle's atom layout, zero on rows past the tile's
