@@ -22,7 +22,7 @@ cudaError_t launch_with_pdl(const void* fn, dim3 grid, dim3 block, size_t smem, 
 // stores each pair's route weight (fp32) at the pair's padded row for FC2,
 // and zeroes the token's fp32 combine accumulator row, into which FC2 adds
 // the token's route-weighted expert outputs.  Block scales go straight into
-// the atom layout of every routed row (few tokens), or, for large batches,
+// the atom layout of every routed row (up to 4096 routed pairs), or, above that,
 // once per token into token-major rows that sf_atoms_kernel then lays out
 // with whole-atom writes (a token's scales land in 56 different atoms, and
 // scattered 4-byte writes cost more than the extra pass).
