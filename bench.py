@@ -16,9 +16,14 @@ Also measured: per-stage times from timing events recorded between the
 stages inside the timed steps (the dominant kernel's roofline uses them),
 an end-to-end pass through moe_forward with pinned host buffers (every
 step's input copy and output read-back inside the timed region, pipelined on
-copy-in / compute / copy-out streams with double buffers), SM clocks during the timed region, a decode/prefill sweep (L2
-flushed between steps), and the CPU oracle on a bounded sample of the same
-workload (rank 0, one GPU only).
+copy-in / compute / copy-out streams with double buffers), SM clocks during
+the timed region, a decode/prefill sweep (L2 flushed between steps; each
+forward also replayed from a CUDA graph), init-routing alone in its modes
+(dynamic and static int8, drop/pad, an expert range with the key_value
+histogram), the widened paths beside the plain forward of the same batch
+(streamed chunks, one expert-parallel rank's slice, per-expert SiTU
+parameters), and the CPU oracle on a bounded sample of the same workload
+(rank 0, one GPU only).
 
 --impl reference times the CPU oracle alone (there is no other implementation
 to run): each step evaluates a bounded sample of the same workload on the
