@@ -326,6 +326,34 @@ def test_back_to_back_forwards_share_a_workspace(full_model, T):
     for c, out, name in zip(cases_ab, outs, ("first", "second")):
         assert_close(out_bits(out)[sample], cases.run_oracle(c, tokens=sample), f"back to back, {name}, T={T}")
 
+
+def test_concurrent_forwards_on_two_streams(full_model):
+    """Two forwards with their own workspaces and outputs, enqueued on two
+    streams without ordering between them (the library's contract for
+    concurrent calls): both match the oracle on sampled tokens."""
+    minp, m = full_model
+    T = 2048
+    cases_ab = (_full_case(minp, T, "uniform", seed=80), _full_case(minp, T, "zipf", seed=81))
+    streams = (torch.cuda.Stream(), torch.cuda.Stream())
+    staged, wss, outs = [], [], []
+    for c in cases_ab:
+        staged.append((dev(c.x, torch.bfloat16), dev(c.expert_ids), dev(c.route_weights, torch.bfloat16),
+                       dev(np.array([c.qX], np.float32))))
+        ws = m.workspace(T)
+        api.moe_prepare_workspace(m.shape, ws, T)
+        wss.append(ws)
+        outs.append(torch.empty((T, c.H), dtype=torch.bfloat16, device="cuda"))
+    torch.cuda.synchronize()
+    for (x, ids, rw, qx), ws, out, st in zip(staged, wss, outs, streams):
+        api.moe_forward(m.shape, T, x, ids, rw, m.w13, m.sf13, m.w2, m.sf2, qx, m.dXdW13, m.qA, m.dAdW2, None,
+                        None, ws, out, st)
+    torch.cuda.synchronize()
+    rs = np.random.default_rng(5)
+    sample = np.unique(np.concatenate([[0, T - 1], rs.choice(T, 10, replace=False)]))
+    for c, ws, out, name in zip(cases_ab, wss, outs, ("first", "second")):
+        assert api.moe_read_status(ws) == (0, 0)
+        assert_close(out_bits(out)[sample], cases.run_oracle(c, tokens=sample), f"concurrent, {name}")
+
 def test_full_shape_streamed_chunks(full_model):
     """The chunk-ready streaming front end at full shape: T = 4096 published
     as four 1024-token chunks through a two-slot ring, each routed on its own;
