@@ -49,6 +49,50 @@ def test_situ_special_cases():
             assert abs(lin) <= 25.0 + 1e-12
 
 
+def _golden_rows(name):
+    path = __file__.rsplit("/", 1)[0] + "/golden/" + name
+    return [list(map(float, ln.split())) for ln in open(path) if ln.strip() and not ln.startswith("#")]
+
+
+def test_situ_distinct_parameters_golden():
+    """Gate and linear smoothing parameters in their own places ("Cake SiTU
+    backend": situ_beta smooths the gate, situ_linear_beta the linear half):
+    values worked by hand from the closed form, and the exchanged call, which
+    a swap of the two parameters would give, differs from each of them."""
+    rows = _golden_rows("situ_distinct_parameters.txt")
+    assert len(rows) == 4
+    for g, u, beta, lam, want, swapped in rows:
+        got = oracle.situ(g, u, beta, lam)
+        assert abs(got - want) <= 1e-13 * abs(want), (g, u, beta, lam, got, want)
+        assert abs(oracle.situ(g, u, lam, beta) - swapped) <= 1e-13 * abs(swapped)
+        assert abs(got - swapped) > 1e-3 * abs(want)
+
+
+def test_dequant_rows_matches_independent_decode():
+    """oracle.nvfp4_dequant_rows (the reference of the tile-product check)
+    against this file's own decode (E2M1 grid table, torch's float8_e4m3fn
+    cast): every code byte, every scale byte including zero and subnormal
+    scales, low nibble first."""
+    rs = np.random.default_rng(17)
+    rows, cols = 256, 64
+    packed = rs.integers(0, 256, size=(rows, cols // 2), dtype=np.uint8)
+    packed[0] = np.arange(32, dtype=np.uint8)           # every byte value appears
+    packed[1] = np.arange(32, 64, dtype=np.uint8)
+    packed[2:8].reshape(-1)[:192] = np.arange(64, 256, dtype=np.uint8)
+    sf = np.arange(rows * cols // 16, dtype=np.int64).reshape(rows, cols // 16) % 256
+    sf = sf.astype(np.uint8)
+    sf[sf == 0x7F] = 0x7E                                # E4M3 NaN codes are never produced
+    sf[sf == 0xFF] = 0xFE
+    got = oracle.nvfp4_dequant_rows(packed, sf)
+    np.testing.assert_array_equal(got, _dense(packed, sf))
+    # a hand-checked element: byte 0x9E holds code 0xE (-4) low, 0x9 (-0.5) high;
+    # scale 0x38 is 1.0 and 0x01 is the smallest subnormal 2^-9
+    one = oracle.nvfp4_dequant_rows(np.full((1, 8), 0x9E, np.uint8), np.array([[0x38]], np.uint8))
+    assert one[0, 0] == -4.0 and one[0, 1] == -0.5
+    tiny_sf = oracle.nvfp4_dequant_rows(np.full((1, 8), 0x07, np.uint8), np.array([[0x01]], np.uint8))
+    assert tiny_sf[0, 0] == 6.0 * 2.0 ** -9 and tiny_sf[0, 1] == 0.0
+
+
 def test_situ_limit_is_swiglu():
     """As beta, lambda -> infinity SiTU becomes SiLU(g) * u (textbook SwiGLU)."""
     g = torch.linspace(-8, 8, 41, dtype=torch.float64)
