@@ -63,12 +63,16 @@ typedef struct {
 #define MOE_DEVSTAT_INVALID_EXPERT 1  /* an expert id outside [0, E) was skipped */
 #define MOE_DEVSTAT_TIMEOUT 2         /* a bounded wait inside a kernel gave up */
 #define MOE_DEVSTAT_BAD_TILE 4        /* a tile descriptor failed a bounds check */
+#define MOE_DEVSTAT_NOT_PREPARED 32   /* the workspace held no preparation stamp: the call did nothing
+                                         (its output is left zero or untouched) */
 
 /* Workspace bytes for any token count 1..max_tokens ("Cake SiTU backend",
  * "The size query uses host metadata only").  *bytes is a HOST pointer.
- * The workspace holds the routing arrays, the quantized activations, the
- * quantized intermediate, the fp32 FC2 output of every routed pair and the
- * default SiTU constants.  Its carve-up depends only on the shape and its byte size, so
+ * The workspace holds a header (status word, counts, preparation stamp), the
+ * routing arrays, the quantized activations, the quantized intermediate, the
+ * fp32 combine accumulator [max_tokens, H] (the route-weighted sum of a
+ * token's FC2 outputs before the BF16 rounding) and the default SiTU
+ * constants.  Its carve-up depends only on the shape and its byte size, so
  * a maximum-size workspace serves every smaller token count. */
 moe_status_t moe_workspace_size(const moe_shape_t* shape, int64_t max_tokens, size_t* bytes);
 
@@ -94,10 +98,15 @@ moe_status_t moe_prepare_weights(const moe_shape_t* shape, const uint8_t* w13, c
 /* Per-token-count preparation ("Cake SiTU backend": "Prepare every token
  * count before its first submission"; it initializes the default SiTU
  * constants and allocates nothing).  Writes the default beta = 4 and
- * lambda = 25 arrays and clears the status word in `ws` (256-byte aligned),
- * and records (ws, ws_bytes, num_tokens) as prepared in a host-side table.
- * Must be stream-ordered before the first moe_forward / moe_init_routing
- * with this num_tokens. */
+ * lambda = 25 arrays, clears the status word and writes a preparation stamp
+ * (shape and token capacity) into the header of `ws` (256-byte aligned), and
+ * records (ws, ws_bytes, num_tokens) as prepared in a host-side table (one
+ * entry per workspace address; a preparation with another size or shape
+ * replaces it).  Must be stream-ordered before the first moe_forward /
+ * moe_init_routing with this num_tokens.  The first kernel of every call
+ * checks the stamp: memory that is no longer the prepared workspace (freed,
+ * then handed out again at the same address) makes the call skip its work
+ * and set MOE_DEVSTAT_NOT_PREPARED instead of computing from stale state. */
 moe_status_t moe_prepare_workspace(const moe_shape_t* shape, void* ws, size_t ws_bytes, int64_t num_tokens,
                                    cudaStream_t stream);
 

@@ -22,7 +22,7 @@ MOE_OK = 0
 STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_WORKSPACE_TOO_SMALL",
                 4: "MOE_ERR_NOT_PREPARED", 5: "MOE_ERR_CUDA", 6: "MOE_ERR_DEVICE_STATUS"}
 DEVSTAT_INVALID_EXPERT, DEVSTAT_TIMEOUT, DEVSTAT_BAD_TILE = 1, 2, 4
-DEVSTAT_STREAM_WAIT, DEVSTAT_STREAM_BOUNDS = 8, 16
+DEVSTAT_STREAM_WAIT, DEVSTAT_STREAM_BOUNDS, DEVSTAT_NOT_PREPARED = 8, 16, 32
 STREAM_ROUTE, STREAM_LAYOUT = 1, 2
 STREAM_PRODUCER_TIMEOUT = 1
 

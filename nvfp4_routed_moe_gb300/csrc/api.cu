@@ -5,6 +5,8 @@
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
+#include <set>
+#include <unordered_map>
 #include <vector>
 
 #include "nvfp4moe.h"
@@ -42,6 +44,20 @@ cudaError_t launch_mma_check(const CUtensorMap& a, const CUtensorMap& b, const u
 
 __global__ void fill_f32_kernel(float* p, int n, float v) {
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) p[i] = v;
+}
+
+struct Stamp {
+  int32_t w[kStampWords];
+};
+
+__global__ void stamp_kernel(int32_t* hdr, const Stamp st) {
+  if (threadIdx.x < kStampWords) hdr[HDR_STAMP + threadIdx.x] = st.w[threadIdx.x];
+}
+
+// The preparation stamp of a workspace: the shape and the token capacity of
+// its carve-up, behind a magic word.
+static Stamp make_stamp(const moe_shape_t* s, int64_t cap) {
+  return Stamp{{kStampMagic, s->hidden, s->inter, s->num_experts, s->top_k, (int32_t)cap}};
 }
 
 // Programmatic dependent launch: a kernel may be scheduled while its
@@ -153,14 +169,21 @@ static bool make_row_maps(RowMaps* m, const void* base, uint64_t row_bytes, uint
 }
 
 // ------------------------------------------------------------ validation
-static bool shape_ok(const moe_shape_t* s) {
-  return s && s->hidden > 0 && s->inter > 0 && s->num_experts > 0 && s->top_k > 0;
-}
-static moe_status_t shape_supported(const moe_shape_t* s) {
-  if (!shape_ok(s)) return MOE_ERR_INVALID_ARG;
-  if (s->hidden % 256 != 0 || s->inter % 128 != 0 || s->inter > 512) return MOE_ERR_UNSUPPORTED;
+moe_status_t routing_shape_supported(const moe_shape_t* s) {
+  if (!s || s->hidden <= 0 || s->num_experts <= 0 || s->top_k <= 0) return MOE_ERR_INVALID_ARG;
+  if (s->hidden % 256 != 0) return MOE_ERR_UNSUPPORTED;
   if (s->num_experts > kMaxExperts || s->top_k > kMaxTopK || s->top_k > s->num_experts) return MOE_ERR_UNSUPPORTED;
   if ((int64_t)s->hidden * s->top_k > (int64_t)1 << 30) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+// The routing limits plus the intermediate size the GEMMs (and the workspace
+// carve-up) support.
+static moe_status_t shape_supported(const moe_shape_t* s) {
+  const moe_status_t st = routing_shape_supported(s);
+  if (st != MOE_OK) return st;
+  if (s->inter <= 0) return MOE_ERR_INVALID_ARG;
+  if (s->inter % 128 != 0 || s->inter > 512) return MOE_ERR_UNSUPPORTED;
   return MOE_OK;
 }
 static Shape to_shape(const moe_shape_t* s) { return Shape{s->hidden, s->inter, s->num_experts, s->top_k}; }
@@ -181,21 +204,36 @@ static int64_t capacity_tokens(const Shape& s, size_t bytes) {
   return lo;
 }
 
+// Host record of prepared workspaces: one entry per workspace address, with
+// the byte size and shape it was prepared for and the token counts prepared
+// on it.  A preparation with another size or shape at the same address
+// replaces the entry.  The device-side stamp is the second check: it catches
+// an address whose memory was freed and handed out again since.
 struct PreparedEntry {
-  const void* ws;
   size_t bytes;
-  int64_t T;
   Shape shape;
+  std::set<int64_t> T;
 };
-static std::vector<PreparedEntry> g_prepared;
+static std::unordered_map<const void*, PreparedEntry> g_prepared;
+
+static bool same_shape(const Shape& a, const Shape& b) { return a.H == b.H && a.I == b.I && a.E == b.E && a.k == b.k; }
 
 static bool is_prepared(const void* ws, size_t bytes, int64_t T, const Shape& s) {
   std::lock_guard<std::mutex> lock(g_mu);
-  for (const auto& p : g_prepared)
-    if (p.ws == ws && p.bytes == bytes && p.T == T && p.shape.H == s.H && p.shape.I == s.I && p.shape.E == s.E &&
-        p.shape.k == s.k)
-      return true;
-  return false;
+  const auto it = g_prepared.find(ws);
+  return it != g_prepared.end() && it->second.bytes == bytes && same_shape(it->second.shape, s) &&
+         it->second.T.count(T) != 0;
+}
+
+static void record_prepared(const void* ws, size_t bytes, int64_t T, const Shape& s) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  PreparedEntry& p = g_prepared[ws];
+  if (p.bytes != bytes || !same_shape(p.shape, s)) {
+    p.bytes = bytes;
+    p.shape = s;
+    p.T.clear();
+  }
+  p.T.insert(T);
 }
 
 static bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -205,8 +243,13 @@ static bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_
     if ((x) != cudaSuccess) return MOE_ERR_CUDA; \
   } while (0)
 
-static RouteArgs route_args(const Shape& s, const WsLayout& L, uint8_t* ws, const int32_t* ids, int64_t T) {
+static RouteArgs route_args(const moe_shape_t* shape, const WsLayout& L, uint8_t* ws, const int32_t* ids,
+                            int64_t T) {
+  const Shape s = to_shape(shape);
   RouteArgs a{};
+  const Stamp st = make_stamp(shape, L.max_tokens);
+  a.check_stamp = 1;
+  for (int i = 0; i < kStampWords; ++i) a.stamp[i] = st.w[i];
   a.ids = ids;
   a.P = T * s.k;
   a.k = s.k;
@@ -327,6 +370,7 @@ cudaError_t init_routing_enqueue(RouteArgs ra, int32_t base, int32_t range, cons
   float* sc_out = (o->quant_mode == 1 || (o->quant_mode == -1 && o->scale)) ? expanded_scale : nullptr;
   if (plain) {
     InitMoveArgs ma{};
+    ma.hdr = ra.hdr;
     ma.x = static_cast<const uint16_t*>(x);
     ma.ids = ids;
     ma.gather = ra.gather;
@@ -444,7 +488,7 @@ static moe_status_t forward_impl(const moe_shape_t* shape, int32_t expert_begin,
 
   // 1. routing
   prof_mark(0, stream);
-  RouteArgs ra = route_args(s, L, w, expert_ids, T);
+  RouteArgs ra = route_args(shape, L, w, expert_ids, T);
   ra.id_base = expert_begin;
   ra.E_all = id_limit;
   int nl = 0;
@@ -622,11 +666,9 @@ moe_status_t moe_prepare_workspace(const moe_shape_t* shape, void* ws, size_t ws
   MOE_CUDA(cudaMemsetAsync(w + L.header, 0, HDR_WORDS * 4, stream));
   fill_f32_kernel<<<4, 256, 0, stream>>>(reinterpret_cast<float*>(w + L.beta_def), s.E, 4.0f);
   fill_f32_kernel<<<4, 256, 0, stream>>>(reinterpret_cast<float*>(w + L.lam_def), s.E, 25.0f);
+  stamp_kernel<<<1, 32, 0, stream>>>(reinterpret_cast<int32_t*>(w + L.header), make_stamp(shape, cap));
   MOE_CUDA(cudaGetLastError());
-  if (!is_prepared(ws, ws_bytes, num_tokens, s)) {
-    std::lock_guard<std::mutex> lock(g_mu);
-    g_prepared.push_back(PreparedEntry{ws, ws_bytes, num_tokens, s});
-  }
+  record_prepared(ws, ws_bytes, num_tokens, s);
   return MOE_OK;
 }
 
@@ -673,7 +715,7 @@ moe_status_t moe_init_routing(const moe_shape_t* shape, int64_t num_rows, const 
   const WsLayout L = make_layout(s, cap);
   int sms = 0;
   MOE_CUDA(device_ready(&sms));
-  RouteArgs ra = route_args(s, L, static_cast<uint8_t*>(ws), expert_ids, num_rows);
+  RouteArgs ra = route_args(shape, L, static_cast<uint8_t*>(ws), expert_ids, num_rows);
   MOE_CUDA(init_routing_enqueue(ra, base, range, shape, num_rows, x, expert_ids, opts, expanded_x, expanded_row_idx,
                                 tokens_cumsum_or_count, expanded_scale, sms, stream));
   return MOE_OK;

@@ -32,9 +32,18 @@ enum : int {
   HDR_MAXROWS = 6,     // largest number of pairs routed to one expert this call
   HDR_STREAM_OK = 7,   // streamed chunk: 1 once its generations were seen published
   HDR_STREAM_N = 8,    // streamed chunk: valid tokens
+  HDR_SKIP = 9,        // 1: routing found no valid preparation stamp and did nothing; later kernels skip too
   HDR_STREAM_BASE = 10,  // streamed chunk: first logical token (int64, words 10-11)
+  HDR_STAMP = 16,      // preparation stamp, kStampWords words: magic, H, I, E, k, token capacity
   HDR_WORDS = 64,
 };
+
+// Written into the header by moe_prepare_workspace and checked by the first
+// kernel of every call, so that memory handed back by an allocator at the
+// address of a workspace prepared earlier is not mistaken for a prepared one.
+constexpr int kStampWords = 6;
+constexpr int32_t kStampMagic = 0x4E564634;   // "NVF4"
+
 
 // One tensor map per activation-row box height (16, 32, 64, 128 rows).
 struct RowMaps {
@@ -120,6 +129,8 @@ struct RouteArgs {
   int32_t* blockhist;
   int32_t nblk;
   int32_t chunk;      // pairs per CTA of the multi-CTA kernels (a multiple of 256)
+  int32_t check_stamp;            // 1: compare hdr[HDR_STAMP..] with `stamp` before any work
+  int32_t stamp[kStampWords];
 };
 
 struct Fc1Args {
@@ -160,6 +171,7 @@ struct Fc2Args {
 };
 
 struct InitMoveArgs {
+  const int32_t* hdr;         // workspace header (HDR_SKIP)
   const uint16_t* x;          // [T, H] bf16
   const int32_t* ids;         // [T, k]
   const int32_t* gather;      // dropless sorted position per flat pair (ws)
@@ -312,6 +324,10 @@ cudaError_t launch_stream_gate(const StreamArgs& r, int64_t C, int32_t* ws_hdr, 
 cudaError_t launch_stream_release(const StreamArgs& r, const int32_t* ws_hdr, cudaStream_t st);
 cudaError_t launch_finalize_rows(const float* acc, uint16_t* out, int64_t out_rows, int H, int32_t* ws_hdr,
                                  int64_t C, int num_sms, cudaStream_t st);
+
+// Shape check of the routing kernels alone (H, E, k; I is not used by them),
+// shared by moe_init_routing and moe_init_routing_static.
+moe_status_t routing_shape_supported(const moe_shape_t* s);
 
 // Init-routing shared by moe_init_routing and moe_init_routing_static: the
 // host check of the options (fills the routed expert range) and the

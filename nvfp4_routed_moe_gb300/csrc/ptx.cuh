@@ -16,6 +16,7 @@ enum : int32_t {
   DEVSTAT_BAD_TILE = 4,         // a tile descriptor failed its bounds check
   DEVSTAT_STREAM_WAIT = 8,      // a streamed chunk's generations were not published in time
   DEVSTAT_STREAM_BOUNDS = 16,   // a streamed chunk's output rows fell outside the output
+  DEVSTAT_NOT_PREPARED = 32,    // the workspace header held no valid preparation stamp; the call did nothing
 };
 
 __device__ __forceinline__ void set_status(int32_t* status, int32_t code) {

@@ -218,6 +218,28 @@ __device__ void scan_experts(const RouteArgs& a, const int* cnt_s, int* s_offs, 
   __syncthreads();
 }
 
+// The preparation stamp written by moe_prepare_workspace.  A workspace whose
+// header does not hold it (memory an allocator handed back at the address of
+// a workspace prepared earlier, or never prepared) is left alone: the call
+// records DEVSTAT_NOT_PREPARED and zeroes the tile and row counts, so every
+// later kernel of the call finds nothing to do.
+__device__ __forceinline__ bool stamp_bad(const RouteArgs& a) {
+  if (!a.check_stamp) return false;
+  bool bad = false;
+#pragma unroll
+  for (int i = 0; i < kStampWords; ++i) bad |= __ldcg(a.hdr + HDR_STAMP + i) != a.stamp[i];
+  return bad;
+}
+
+__device__ __forceinline__ void mark_not_prepared(const RouteArgs& a) {
+  a.hdr[HDR_NUM_TT] = 0;
+  a.hdr[HDR_PPAD] = 0;
+  a.hdr[HDR_NVALID] = 0;
+  a.hdr[HDR_MAXROWS] = 0;
+  a.hdr[HDR_SKIP] = 1;
+  atomicOr(a.hdr + HDR_STATUS, DEVSTAT_NOT_PREPARED);
+}
+
 // ---------------------------------------------------------------- small path
 // One CTA of 1024 threads sorts up to kRouteSmallMax pairs in one launch.
 // The ids are staged in shared memory once; as many warps as there are
@@ -235,6 +257,14 @@ __global__ void __launch_bounds__(1024, 1) route_small_kernel(const RouteArgs a)
   const int tid = threadIdx.x, warp = tid >> 5;
   pdl_wait();
   pdl_launch_dependents();
+  __shared__ int s_bad;
+  if (tid == 0) {
+    s_bad = stamp_bad(a);
+    if (s_bad) mark_not_prepared(a);
+    else a.hdr[HDR_SKIP] = 0;
+  }
+  __syncthreads();
+  if (s_bad) return;
   for (int i = tid; i < NHW * E; i += 1024) hist[i] = 0;
   for (int64_t i = tid; i < a.P; i += 1024) s_ids[i] = __ldg(a.ids + i);
   __syncthreads();
@@ -274,10 +304,19 @@ __global__ void __launch_bounds__(256) route_hist_kernel(const RouteArgs a) {
   int* s_offs = s_cnt + E;        // [E]
   int* s_poffs = s_offs + E;      // [E]
   int* s_tmp = s_poffs + E;       // [256]
-  __shared__ int s_last;
+  __shared__ int s_last, s_bad;
   const int tid = threadIdx.x, warp = tid >> 5;
   pdl_wait();
   pdl_launch_dependents();
+  if (tid == 0) {
+    s_bad = stamp_bad(a);
+    if (blockIdx.x == 0) {
+      if (s_bad) mark_not_prepared(a);
+      else a.hdr[HDR_SKIP] = 0;
+    }
+  }
+  __syncthreads();
+  if (s_bad) return;   // before the ticket, which a foreign header does not hold at zero
   for (int i = tid; i < 8 * E; i += 256) hist[i] = 0;
   __syncthreads();
   const int64_t cb = (int64_t)blockIdx.x * a.chunk;
@@ -341,6 +380,10 @@ __global__ void __launch_bounds__(256) route_rank_kernel(const RouteArgs a) {
   // the quantization reads nothing that routing writes before its own wait.
   pdl_launch_dependents();
   pdl_wait();
+  __shared__ int s_bad;
+  if (tid == 0) s_bad = stamp_bad(a);
+  __syncthreads();
+  if (s_bad) return;
   if (blockIdx.x == 0 && tid == 0) a.hdr[HDR_DONE] = 0;  // re-arm the ticket for the next call
   for (int i = tid; i < 8 * E; i += 256) hist[i] = 0;
   for (int e = tid; e < E; e += 256) {
@@ -381,7 +424,7 @@ __global__ void __launch_bounds__(256) init_move_kernel(const InitMoveArgs a) {
   const int64_t t = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
   pdl_wait();
   pdl_launch_dependents();
-  if (t >= a.T) return;
+  if (t >= a.T || a.hdr[HDR_SKIP]) return;
   const uint16_t* xr = a.x + t * a.H;
   int dest = -1;
   if (lane < a.k) {
@@ -483,6 +526,7 @@ __global__ void __launch_bounds__(256) init_move_kernel(const InitMoveArgs a) {
 __global__ void __launch_bounds__(256) init_rows_kernel(const InitRowsArgs a) {
   pdl_wait();
   pdl_launch_dependents();
+  if (a.hdr[HDR_SKIP]) return;
   const int lane = threadIdx.x & 31;
   const int64_t w0 = ((int64_t)blockIdx.x * 256 + threadIdx.x) >> 5, nw = ((int64_t)gridDim.x * 256) >> 5;
   const int64_t avail = a.hdr[HDR_NVALID];
@@ -566,6 +610,7 @@ static_assert(4 * 256 >= kMaxExperts, "init_finish: four experts per thread of o
 __global__ void __launch_bounds__(256) init_finish_kernel(const InitFinishArgs a) {
   pdl_wait();
   pdl_launch_dependents();
+  if (a.hdr[HDR_SKIP]) return;
   const int64_t gtid = (int64_t)blockIdx.x * 256 + threadIdx.x;
   const int64_t nthr = (int64_t)gridDim.x * 256;
   const int64_t avail = a.hdr[HDR_NVALID];

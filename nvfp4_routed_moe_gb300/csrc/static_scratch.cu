@@ -40,7 +40,8 @@ struct StaticLayout {
 static StaticLayout static_layout() {
   StaticLayout L{};
   const size_t P = kStaticMaxPairs, E = kMaxExperts;
-  const size_t ppad = P + (size_t)(kTileRows - 1) * E;
+  // the same bound as the workspace carve-up: every expert padded to whole tiles
+  const size_t ppad = align_up(P + (size_t)(kTileRows - 1) * E, kTileRows);
   const size_t tiles = P / kTileRows + E;
   const size_t nblk = (P + kRouteChunk - 1) / kRouteChunk;
   size_t o = 0;
@@ -110,10 +111,10 @@ extern "C" moe_status_t moe_init_routing_static(const moe_shape_t* shape, int64_
                                                 void* expanded_x, int32_t* expanded_row_idx,
                                                 int32_t* tokens_cumsum_or_count, float* expanded_scale,
                                                 cudaStream_t stream) {
-  if (!shape || shape->hidden <= 0 || shape->num_experts <= 0 || shape->top_k <= 0) return MOE_ERR_INVALID_ARG;
-  if (shape->hidden % 256 != 0 || shape->num_experts > kMaxExperts || shape->top_k > kMaxTopK ||
-      shape->top_k > shape->num_experts)
-    return MOE_ERR_UNSUPPORTED;
+  // the routing kernels' own limits, as moe_init_routing applies them (the
+  // intermediate size is not used here)
+  const moe_status_t sst = routing_shape_supported(shape);
+  if (sst != MOE_OK) return sst;
   if (!x || !expert_ids || !opts || !expanded_x || !expanded_row_idx || !tokens_cumsum_or_count || num_rows < 1)
     return MOE_ERR_INVALID_ARG;
   if (num_rows > kStaticMaxPairs / shape->top_k) return MOE_ERR_WORKSPACE_TOO_SMALL;  // beyond the static scratch
@@ -152,6 +153,7 @@ extern "C" moe_status_t moe_init_routing_static(const moe_shape_t* shape, int64_
   ra.tt_list = reinterpret_cast<int32_t*>(w + L.tt_list);
   ra.blockhist = reinterpret_cast<int32_t*>(w + L.blockhist);
   ra.chunk = kRouteChunk;
+  ra.check_stamp = 0;   // the header was cleared just above; there is no caller workspace to stamp
   ra.nblk = (int32_t)((ra.P + kRouteChunk - 1) / kRouteChunk);
   if (init_routing_enqueue(ra, base, range, shape, num_rows, x, expert_ids, opts, expanded_x, expanded_row_idx,
                            tokens_cumsum_or_count, expanded_scale, sms, stream) != cudaSuccess)

@@ -434,3 +434,33 @@ def test_local_expert_slices_sum_to_the_full_forward():
         assert_close(part, cases.run_oracle(sl), f"slice {begin}")
         total += gen.bf16_bits_to_f32(part)
     assert_close(gen.f32_to_bf16_bits(total.astype(np.float32)), full, "sum of slices")
+
+
+def test_recycled_workspace_memory_is_refused_on_the_device(tiny):
+    """A prepared workspace is freed and the caching allocator hands the
+    same block back (same address, same size) holding other data: the host
+    record still says "prepared", but the header's preparation stamp is gone,
+    so the forward sets MOE_DEVSTAT_NOT_PREPARED and leaves the output zero
+    instead of computing from foreign bytes.  Preparing it again restores
+    the normal result."""
+    inp, m = tiny
+    nbytes = api.moe_workspace_size(m.shape, inp.T + 77)    # a size no other test uses
+    ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    api.moe_prepare_workspace(m.shape, ws, inp.T)
+    torch.cuda.synchronize()
+    addr = ws.data_ptr()
+    del ws
+    ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    if ws.data_ptr() != addr:
+        pytest.skip("the caching allocator returned another block")
+    ws.fill_(0xA5)
+    out, _ = m.forward_inputs(ws=ws, prepare=False)
+    torch.cuda.synchronize()
+    status, _ = api.moe_read_status(ws)
+    assert status & api.DEVSTAT_NOT_PREPARED
+    assert not out.float().abs().sum().item()
+    api.moe_prepare_workspace(m.shape, ws, inp.T)
+    out, _ = m.forward_inputs(ws=ws, prepare=False)
+    torch.cuda.synchronize()
+    assert api.moe_read_status(ws) == (0, 0)
+    assert_close(out_bits(out), cases.run_oracle(inp), "re-prepared")

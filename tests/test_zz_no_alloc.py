@@ -92,3 +92,24 @@ def test_static_scratch_rejects_too_many_pairs():
     with pytest.raises(api.MoeError) as e:
         api.moe_init_routing_static(shp, T, buf, buf, opts, buf, buf, buf, buf)
     assert e.value.status == 3
+
+
+@pytest.mark.parametrize("T,E,k", [(40, 32, 4), (2000, 128, 16)])
+def test_static_scratch_skips_out_of_range_ids_like_the_workspace_version(T, E, k):
+    """Ids outside [0, E) are skipped by both entry points alike: those pairs
+    get expanded_row_idx -1, the histograms count only the valid ids, and
+    the moved rows are the same (one-CTA and multi-CTA routing).  The static
+    version has no status word to report; only the outputs are compared."""
+    x = gen.draw_x(6, T, 512)
+    ids = gen.draw_ids_uniform(6, T, E, k)
+    ids[3, 1] = -1
+    ids[17, 0] = E
+    ids[T - 1, k - 1] = 1 << 30
+    opts = api.moe_routing_opts_t(0, 0, 0, 1, 1)
+    ref, results = _run_both(x, ids, E, opts)
+    nvalid = T * k - 3
+    ridx = ref[1].cpu().numpy()
+    assert ridx[3 * k + 1] == -1 and ridx[17 * k] == -1 and ridx[T * k - 1] == -1
+    assert int(ref[2].sum()) == nvalid
+    for got in results:
+        _compare(ref, got, nvalid)
