@@ -13,7 +13,10 @@ own GPU with replicated weights (weak scaling, no collective on the data
 path); rank 0 prints one JSON line.
 
 Also measured: per-stage times from timing events recorded between the
-stages inside the timed steps (the dominant kernel's roofline uses them),
+stages in a separate pass after the timed steps (events between kernels
+serialize the chain; the dominant kernel's roofline uses these times), the
+block-scaled FP4 tensor-core peak of this GPU from the library's own MMA
+microbenchmark (the denominator of the tensor fraction),
 an end-to-end pass through moe_forward with pinned host buffers (every
 step's input copy and output read-back inside the timed region, pipelined on
 copy-in / compute / copy-out streams with double buffers), SM clocks during
@@ -203,21 +206,81 @@ def step_bytes(T, n_active):
 
 
 def fc1_bytes(T, n_active):
-    """Algorithmic bytes of one FC1 launch: W13 codes + scales of the active
-    experts, each token's quantized row once, the quantized intermediate of
-    every routed pair written once."""
-    return n_active * FC1_BYTES_PER_EXPERT + T * (H // 2 + H // 16) + T * K * (I // 2 + I // 16)
+    """Algorithmic bytes of one FC1 launch: W13 codes + block scales of the
+    active experts and each token's quantized row (codes + scales) once.  The
+    requantized intermediate it writes is activation-requant traffic, which
+    counts as overhead, not as algorithmic bytes."""
+    return n_active * FC1_BYTES_PER_EXPERT + T * (H // 2 + H // 16)
 
 
 def fc2_bytes(T, n_active):
-    """Algorithmic bytes of one FC2 launch: W2 codes + scales of the active
-    experts, the quantized intermediate of every routed pair read once, the
-    fp32 combine accumulator [T, H] written once."""
-    return n_active * FC2_BYTES_PER_EXPERT + T * K * (I // 2 + I // 16) + T * H * 4
+    """Algorithmic bytes of one FC2 launch: W2 codes + block scales of the
+    active experts.  The intermediate it reads and the fp32 combine
+    accumulator are requant and scratch traffic (overhead)."""
+    return n_active * FC2_BYTES_PER_EXPERT
 
 
-KERNEL_BYTES = {"fc1": (fc1_bytes, "n_active*1548288 + T*2016 + T*k*216"),
-                "fc2": (fc2_bytes, "n_active*774144 + T*k*216 + T*H*4")}
+KERNEL_BYTES = {"fc1": (fc1_bytes, "n_active*1548288 + T*2016"),
+                "fc2": (fc2_bytes, "n_active*774144")}
+FLOPS_PER_PAIR = 2 * H * 2 * I + 2 * I * H                        # FC1 + FC2, 8,257,536
+KERNEL_FLOPS_PER_PAIR = {"fc1": 2 * H * 2 * I, "fc2": 2 * I * H}
+
+
+def fp4_peak(sms):
+    """Block-scaled FP4 MMA throughput measured on this GPU with the
+    library's own microbenchmark (moe_test_mma_peak): every SM issues
+    back-to-back M=128, N=256, K=64 kind::mxf4nvf4 MMAs from resident
+    operands; CUDA-event time of the launch, best of 5.  Also the tensor
+    pipe's cycles per FC1 k-block (four MMAs plus the scale-atom copies that
+    FC1 issues with them) for the two FC1 unit shapes."""
+    import torch
+    from nvfp4_routed_moe_gb300 import api
+    cyc = torch.zeros(sms, dtype=torch.int64, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+
+    def run(n, mmas, copies, reps=5):
+        best, cycles = None, None
+        for _ in range(reps + 1):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            api.moe_test_mma_peak(sms, n, mmas, copies, cyc, st)
+            b.record()
+            torch.cuda.synchronize()
+            ms = a.elapsed_time(b)
+            c = cyc.cpu().numpy()
+            if best is None or ms < best:
+                best, cycles = ms, float(np.median(c))
+        assert int(st.item()) == 0 and cycles > 0
+        return best, cycles
+
+    mmas = 16384
+    ms, cyc256 = run(256, mmas, 0)
+    flops = 2.0 * 128 * 256 * 64 * mmas * sms
+    res = {"tflops": flops / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "source":
+           f"moe_test_mma_peak: {sms} SMs x {mmas} back-to-back M128 N256 K64 kind::mxf4nvf4 scale_vec::4X MMAs, "
+           "CUDA events, best of 5", "cycles_per_mma_n256": cyc256 / mmas,
+           "sm_mhz_effective": cyc256 / (ms * 1e3)}
+    _, c = run(128, 4096, 0)
+    res["cycles_per_mma_n128"] = c / 4096
+    _, c = run(256, 4096, 12)
+    res["fc1_kblock_cycles_pair2"] = c / 1024          # 4 N=256 MMAs + 12 scale-atom copies
+    _, c = run(128, 4096, 8)
+    res["fc1_kblock_cycles_pair1"] = c / 1024          # 4 N=128 MMAs + 8 scale-atom copies
+    del cyc, st
+    return res
+
+
+def cpu_model():
+    """The host CPU's model name (lscpu), e.g. an Arm Neoverse core on Grace."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    import platform
+    return platform.processor() or platform.machine()
 
 
 # Sources compiled into the GEMM kernels (the file and everything it includes).
@@ -330,9 +393,31 @@ def cpu_baseline(inp, target_s=12.0, max_tokens=512):
         n = min(2 * n, max_tokens - done) if done < max_tokens else 0
         if n <= 0 or done >= inp.T:
             break
-    wall = time.time() - t_start
     return {"value": done / spent, "unit": "tokens/s", "cores": oracle.num_threads(), "kind": "oracle",
-            "sample": f"first {done} tokens of the timed workload (same weights and routing), {spent:.1f} s"}
+            "sample": f"first {done} tokens of the timed workload (same weights and routing), {spent:.1f} s",
+            "cpu": cpu_model()}
+
+
+def cpu_baseline_decode(winp, E):
+    """The oracle at decode (T=16, uniform ids) on all host threads and on
+    one thread, the second timing the plan asks for at T <= 16."""
+    import oracle
+    from oracle import cases
+    oracle.build()
+    b = gen.full(116, T=16, routing="uniform", weights=False, E=E)
+    b.w13, b.sf13, b.w2, b.sf2 = winp.w13, winp.sf13, winp.w2, winp.sf2
+    b.dXdW13, b.qA, b.dAdW2 = winp.dXdW13, winp.qA, winp.dAdW2
+    res = {}
+    cores = oracle.num_threads()
+    for name, threads, toks in (("all_threads", cores, np.arange(16)), ("one_thread", 1, np.arange(4))):
+        oracle.set_num_threads(threads)
+        t0 = time.time()
+        cases.run_oracle(b, tokens=toks)
+        dt = time.time() - t0
+        res[name] = {"value": len(toks) / dt, "unit": "tokens/s", "cores": threads,
+                     "sample": f"{len(toks)} tokens of the T=16 decode batch, {dt:.2f} s"}
+    oracle.set_num_threads(cores)
+    return res
 
 
 def run_reference(args):
@@ -428,7 +513,8 @@ def main():
     def make_batch(b):
         return dict(x=dev(b.x, torch.bfloat16), ids=dev(b.expert_ids), rw=dev(b.route_weights, torch.bfloat16),
                     qX=dev(np.array([b.qX], np.float32)), T=b.T,
-                    n_active=int((np.bincount(b.expert_ids.ravel(), minlength=E) > 0).sum()))
+                    n_active=int((np.bincount(b.expert_ids.ravel(), minlength=E) > 0).sum()),
+                    pairs=int(((b.expert_ids >= 0) & (b.expert_ids < E)).sum()))
 
     def forward(bt, ws, out, stream=None):
         api.moe_forward(shp, bt["T"], bt["x"], bt["ids"], bt["rw"], *w, bt["qX"], *scales, None, None, ws, out,
@@ -455,8 +541,6 @@ def main():
     time.sleep(0.5)
     stage = None
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    if not args.no_stage_events:
-        api.moe_profile_start(args.steps)
     barrier()
     torch.cuda.synchronize()
     clocks.mark("start")
@@ -468,10 +552,17 @@ def main():
     clocks.mark("end")
     barrier()
     ms = ev0.elapsed_time(ev1)
+    clk = clocks.stop()
     if not args.no_stage_events:
+        # stage breakdown in a separate pass: events recorded between the
+        # kernels serialize the chain, so they stay out of the timed steps
+        n_stage = min(args.steps, 50)
+        api.moe_profile_start(n_stage)
+        for _ in range(n_stage):
+            forward(batch, ws, out)
+        torch.cuda.synchronize()
         stage_ms, ncalls = api.moe_profile_stop()
         stage = {k: v / max(ncalls, 1) for k, v in stage_ms.items()}
-    clk = clocks.stop()
     ms, value = job_throughput(ms, T, args.steps, world)
     ms_per_step = ms / args.steps
     launches = api.moe_forward_launch_count(shp, T) * args.steps
@@ -537,20 +628,33 @@ def main():
     peak, peak_src = peaks()
     n_active = batch["n_active"]
     roof_all = {}
+    fp4 = fp4_peak(torch.cuda.get_device_properties(local).multi_processor_count) if world == 1 or rank == 0 \
+        else None
+    pairs = int(batch["pairs"])
     for kname, (fn, formula) in KERNEL_BYTES.items():
         b_k = fn(T, n_active)
+        traffic = traffic_from_profile(kname, args.workload)
         r = {"kernel": f"{kname}_kernel", "bound": "hbm", "achieved": None, "peak": peak, "unit": "GB/s",
-             "frac": None, "traffic": traffic_from_profile(kname, args.workload), "peak_source": peak_src,
-             "bytes_per_launch": b_k, "bytes_formula": formula}
+             "frac": None, "traffic": traffic, "peak_source": peak_src, "bytes_per_launch": b_k,
+             "bytes_formula": formula,
+             "traffic_over_algorithmic": traffic / b_k if traffic else None}
         if stage:
             ach = b_k / (stage[kname] * 1e-3) / 1e9
             r.update(achieved=ach, frac=ach / peak, ms=stage[kname])
+            if fp4:
+                tf = pairs * KERNEL_FLOPS_PER_PAIR[kname] / (stage[kname] * 1e-3) / 1e12
+                r["tensor"] = {"achieved_tflops": tf, "frac": tf / fp4["tflops"]}
         roof_all[kname] = r
     dominant = max(roof_all, key=lambda k: stage[k] if stage else 0.0)
     roof = roof_all[dominant]
     step_b = step_bytes(T, n_active)
     fwd_roof = {"bytes_per_step": step_b, "achieved": step_b / (ms_per_step * 1e-3) / 1e9}
     fwd_roof["frac"] = fwd_roof["achieved"] / peak
+    tensor = None
+    if fp4:
+        tf = pairs * FLOPS_PER_PAIR / (ms_per_step * 1e-3) / 1e12
+        tensor = {"flops_per_step": pairs * FLOPS_PER_PAIR, "achieved_tflops": tf, "peak_tflops": fp4["tflops"],
+                  "frac": tf / fp4["tflops"], "peak": fp4}
 
     # ------------------------------------------------------------ sweep
     sweep = None
@@ -601,7 +705,10 @@ def main():
                            "tokens_per_s": T_s / (t_ms * 1e-3),
                            "hbm_frac": byt / (t_ms * 1e-3) / 1e9 / peak, "n_active": b["n_active"],
                            "fc1_ms": round(st_ms["fc1"] / nc, 4), "fc2_ms": round(st_ms["fc2"] / nc, 4),
-                           "fc1_hbm_frac": fc1_bytes(T_s, b["n_active"]) / (st_ms["fc1"] / nc * 1e-3) / 1e9 / peak}
+                           "fc1_hbm_frac": fc1_bytes(T_s, b["n_active"]) / (st_ms["fc1"] / nc * 1e-3) / 1e9 / peak,
+                           "fc2_hbm_frac": fc2_bytes(T_s, b["n_active"]) / (st_ms["fc2"] / nc * 1e-3) / 1e9 / peak}
+            if fp4:
+                sweep[name]["tensor_frac"] = (b["pairs"] * FLOPS_PER_PAIR / (t_ms * 1e-3) / 1e12) / fp4["tflops"]
         sweep["init_routing"] = init_routing_sweep(shp, flush, dev)
         sweep["next_rows"] = next_rows_sweep(shp, flush, dev, w, scales, winp, peak)
         del flush
@@ -613,6 +720,7 @@ def main():
         inp_w.w13, inp_w.sf13, inp_w.w2, inp_w.sf2 = winp.w13, winp.sf13, winp.w2, winp.sf2
         inp_w.dXdW13, inp_w.qA, inp_w.dAdW2 = winp.dXdW13, winp.qA, winp.dAdW2
         cpu = cpu_baseline(inp_w)
+        cpu["decode"] = cpu_baseline_decode(winp, E)
 
     if rank == 0:
         line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
@@ -622,7 +730,8 @@ def main():
                 "config": {"workload": f"{args.workload}: {wl['text']}", "T": T, "n_active_experts": n_active,
                            "l2": "inputs larger than L2 (2.08 GB of weights read per step)",
                            "parallelism": f"replicas x{world} (data parallel, weak scaling)"},
-                "roofline": roof, "roofline_kernels": roof_all, "forward_roofline": fwd_roof, "stages_ms": stage,
+                "roofline": roof, "roofline_kernels": roof_all, "forward_roofline": fwd_roof, "tensor": tensor,
+                "tensor_frac": tensor["frac"] if tensor else None, "stages_ms": stage,
                 "cpu_baseline": cpu,
                 "e2e": {"value": e2e_val, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                         "steps": e2e_steps, "pipeline": "copy-in, compute and copy-out streams, double-buffered"},

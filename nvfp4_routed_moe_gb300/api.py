@@ -28,7 +28,7 @@ STREAM_PRODUCER_TIMEOUT = 1
 
 EXPORTED = ["moe_workspace_size", "moe_prepared_weight_bytes", "moe_prepare_weights", "moe_prepare_workspace",
             "moe_forward", "moe_forward_local_experts", "moe_init_routing", "moe_init_routing_static", "moe_read_status", "moe_status_string", "moe_test_codec_sweep",
-            "moe_test_quantize_rows", "moe_test_situ_requant", "moe_test_requant_lanes", "moe_test_mma_fp4",
+            "moe_test_quantize_rows", "moe_test_situ_requant", "moe_test_requant_lanes", "moe_test_mma_fp4", "moe_test_mma_peak",
             "moe_workspace_layout", "moe_forward_launch_count", "moe_profile_start", "moe_profile_stop",
             "moe_stream_ring_size", "moe_stream_ring_init", "moe_stream_begin", "moe_stream_publish",
             "moe_stream_forward", "moe_stream_read_status"]
@@ -94,6 +94,7 @@ def lib():
         "moe_test_situ_requant": [P, i64, i32, f32, f32, f32, P, P, P, P],
         "moe_test_requant_lanes": [P, i64, i32, f32, P, P, P],
         "moe_test_mma_fp4": [P, P, P, P, i32, i32, P, P, P],
+        "moe_test_mma_peak": [i32, i32, i32, i32, P, P, P],
         "moe_workspace_layout": [S, sz, ctypes.POINTER(moe_ws_layout_t)],
         "moe_forward_launch_count": [S, i64, ctypes.POINTER(i32)],
         "moe_profile_start": [i32],
@@ -237,6 +238,11 @@ def moe_test_requant_lanes(act, qA, packed, sf, stream=None):
 def moe_test_mma_fp4(a, sfa_atoms, b, sfb_atoms, n, k, d, status, stream=None):
     _check(lib().moe_test_mma_fp4(_p(a), _p(sfa_atoms), _p(b), _p(sfb_atoms), n, k, _p(d), _p(status),
                                   _stream(stream)), "moe_test_mma_fp4")
+
+
+def moe_test_mma_peak(grid: int, n: int, mmas: int, copies: int, cycles, status, stream=None):
+    _check(lib().moe_test_mma_peak(grid, n, mmas, copies, _p(cycles), _p(status), _stream(stream)),
+           "moe_test_mma_peak")
 
 
 def moe_workspace_layout(shp, ws_bytes: int) -> moe_ws_layout_t:

@@ -814,8 +814,71 @@ __global__ void __launch_bounds__(128, 1)
   if (warp == 0) tmem_dealloc(tmem, 256);
 }
 
+// ================================================================ MMA peak
+// Tensor-pipe throughput of the block-scaled FP4 MMA as the GEMMs issue it:
+// every CTA (one per SM) keeps one A tile [128 x 256 FP4], one B tile
+// [n x 256 FP4] and their scale atoms resident in shared memory, copies the
+// atoms to TMEM once, and one thread issues `mmas` MMAs (M = 128, N = n,
+// K = 64, cycling over the four K-steps of the tile) into one accumulator,
+// plus `copies` scale-atom copies (tcgen05.cp 32x128b.warpx4, into TMEM
+// columns no MMA reads) after every fourth MMA, as FC1 issues them per
+// k-block.  The operand values do not matter for throughput; they are
+// fixed bytes.  cycles[blockIdx.x] = SM clock cycles from the first issue to
+// the completion of the last MMA.
+__global__ void __launch_bounds__(128, 1)
+    mma_peak_kernel(int n, int mmas, int copies, long long* cycles, int32_t* status) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = aligned_smem(smem_raw);
+  uint8_t* sA = smem;              // 16 KB: 128 rows x 128 B, 128B-swizzled
+  uint8_t* sB = smem + 16384;      // 32 KB: up to 256 rows x 128 B
+  uint8_t* sSF = smem + 49152;     // 16 atoms of 512 B: 4 for A, 8 for B, 4 spare copy sources
+  Barriers* bars = reinterpret_cast<Barriers*>(smem + 57344);
+  const int warp = threadIdx.x >> 5;
+  for (int i = threadIdx.x; i < 57344 / 16; i += blockDim.x) {
+    const uint32_t v = i < 49152 / 16 ? 0x3A2B1C0Du ^ (uint32_t)(i * 0x9E37u) : 0x38383838u;   // codes; scales 1.0
+    reinterpret_cast<uint4*>(smem)[i] = make_uint4(v, v ^ 0x11111111u, v ^ 0x22222222u, v ^ 0x44444444u);
+  }
+  if (threadIdx.x == 0) {
+    mbar_init(&bars->drain, 1);
+    fence_barrier_init();
+  }
+  fence_proxy_async_shared();
+  if (warp == 0) {
+    tmem_alloc(&bars->tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+  if (threadIdx.x == 0) {
+    // TMEM: accumulator columns [0, n); A atoms at 256 + 4 ks; B atoms at
+    // 272 + 8 ks + 4 j; copy targets at 320 .. 383 (read by no MMA).
+    for (int a = 0; a < 4; ++a) tmem_cp_32x128b_x4(tmem + 256 + a * 4, sf_desc(sSF + a * 512));
+    for (int a = 0; a < 8; ++a) tmem_cp_32x128b_x4(tmem + 272 + a * 4, sf_desc(sSF + 2048 + a * 512));
+    const uint32_t idesc = idesc_mxf4nvf4(128, (uint32_t)n);
+    const long long t0 = clock64();
+    for (int i = 0; i < mmas; ++i) {
+      const int ks = i & 3;
+      const uint64_t ad = smem_desc(smem_u32(sA) + ks * 32, 16, 1024, kLayoutSW128);
+      const uint64_t bd = smem_desc(smem_u32(sB) + ks * 32, 16, 1024, kLayoutSW128);
+      mma_mxf4nvf4(tmem, ad, bd, idesc, tmem + 256 + ks * 4, tmem + 272 + ks * 8, i ? 1u : 0u);
+      if (ks == 3)
+        for (int c = 0; c < copies; ++c) tmem_cp_32x128b_x4(tmem + 320 + (c & 15) * 4, sf_desc(sSF + (c & 15) * 512));
+    }
+    tc_commit(&bars->drain);
+    const bool ok = mbar_wait(&bars->drain, 0, status);
+    cycles[blockIdx.x] = ok ? clock64() - t0 : -1;
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0) tmem_dealloc(tmem, kTmemCols);
+}
+
 // ------------------------------------------------------------------ launchers
 constexpr size_t kMmaCheckSmem = 36864 + sizeof(Barriers) + 1024;
+constexpr size_t kMmaPeakSmem = 57344 + sizeof(Barriers) + 1024;
 
 cudaError_t gemm_set_attributes() {
   cudaError_t err =
@@ -826,6 +889,9 @@ cudaError_t gemm_set_attributes() {
                              (int)Fc1Cfg<2>::kSmem);
   if (err != cudaSuccess) return err;
   err = cudaFuncSetAttribute((const void*)fc2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kFc2Smem);
+  if (err != cudaSuccess) return err;
+  err = cudaFuncSetAttribute((const void*)mma_peak_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kMmaPeakSmem);
   if (err != cudaSuccess) return err;
   return cudaFuncSetAttribute((const void*)mma_check_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               (int)kMmaCheckSmem);
@@ -851,6 +917,12 @@ cudaError_t launch_fc2(const CUtensorMap& w2, const RowMaps& aq, const Fc2Args& 
 cudaError_t launch_mma_check(const CUtensorMap& a, const CUtensorMap& b, const uint8_t* sfa, const uint8_t* sfb,
                              int N, int K, float* d, int32_t* status, cudaStream_t st) {
   mma_check_kernel<<<1, 128, kMmaCheckSmem, st>>>(a, b, sfa, sfb, N, K, d, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_mma_peak(int grid, int n, int mmas, int copies, long long* cycles, int32_t* status,
+                            cudaStream_t st) {
+  mma_peak_kernel<<<grid, 128, kMmaPeakSmem, st>>>(n, mmas, copies, cycles, status);
   return cudaGetLastError();
 }
 

@@ -93,6 +93,8 @@ def _load():
         lib.oracle_scale_atom_offset.argtypes = [i64, i64, i64]
         lib.oracle_num_threads.restype = ctypes.c_int
         lib.oracle_num_threads.argtypes = []
+        lib.oracle_set_num_threads.restype = None
+        lib.oracle_set_num_threads.argtypes = [ctypes.c_int]
         _lib = lib
         return lib
 
@@ -107,6 +109,11 @@ def _c(a, dtype):
 
 def num_threads() -> int:
     return int(_load().oracle_num_threads())
+
+
+def set_num_threads(n: int) -> None:
+    """Threads of the oracle's parallel loops from now on."""
+    _load().oracle_set_num_threads(int(n))
 
 
 # --------------------------------------------------------------------- codecs

@@ -640,3 +640,13 @@ int oracle_num_threads(void) {
     return 1;
 #endif
 }
+
+/* Threads used by the parallel loops from here on (the CPU baseline times the
+ * oracle on all host cores and on one). */
+void oracle_set_num_threads(int n) {
+#ifdef _OPENMP
+    if (n > 0) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}

@@ -282,7 +282,7 @@ def test_full_shape_per_expert_situ_parameters(full_model, T):
     assert not np.array_equal(ref[:4], default)      # the parameters do change the result
 
 
-@pytest.mark.parametrize("T,routing,big", [(512, "uniform", 0.0), (4096, "zipf", 0.0), (16384, "uniform", 0.01)])
+@pytest.mark.parametrize("T,routing,big", [(512, "uniform", 0.0)])
 def test_full_shape_sampled_tokens(full_model, T, routing, big):
     minp, m = full_model
     inp = _full_case(minp, T, routing, big)
@@ -302,6 +302,146 @@ def test_full_shape_sampled_tokens(full_model, T, routing, big):
     np.testing.assert_array_equal(ws_i32(ws, lay.count, inp.E), counts)
 
 
+
+def _tile_boundary_tokens(ids, E):
+    """Tokens of the rows where the tiling changes: for every expert, the
+    first row of its group, the first row of each further 128-row tile and
+    the last row (the last, partly filled tile's end), in the stable expert
+    order of the routing ("npu_moe_init_routing_v2", keyValueSort)."""
+    r = oracle.routing(ids, E)
+    k = ids.shape[1]
+    start = r["cumsum"] - r["count"]
+    rows = []
+    for e in np.nonzero(r["count"])[0]:
+        n = int(r["count"][e])
+        rows += [int(start[e]) + j for j in range(0, n, 128)] + [int(start[e]) + n - 1]
+    return np.unique(r["sorted_row"][np.array(rows)] // k)
+
+
+@pytest.mark.parametrize("T,routing,big", [(4096, "zipf", 0.0), (16384, "uniform", 0.01)])
+def test_full_shape_tile_boundary_tokens(full_model, T, routing, big):
+    """Prefill (Zipf routing) and max batch (uniform, 1% of rows x50) at full
+    shape: the tokens at every expert's first row, 128-row tile boundaries and
+    last row -- the rows where tiles, padding and partly filled last tiles
+    start and end -- plus the largest rows, against the oracle."""
+    minp, m = full_model
+    inp = _full_case(minp, T, routing, big)
+    out, ws = m.forward_inputs(inp)
+    torch.cuda.synchronize()
+    assert api.moe_read_status(ws) == (0, 0)
+    sample = _tile_boundary_tokens(inp.expert_ids, inp.E)
+    if big:
+        xf = np.abs(gen.bf16_bits_to_f32(inp.x)).max(axis=1)
+        sample = np.unique(np.concatenate([sample, np.argsort(-xf)[:8]]))
+    assert len(sample) >= (900 if T == 4096 else 2500)
+    ref = cases.run_oracle(inp, tokens=sample)
+    assert_close(out_bits(out)[sample], ref, f"T={T} {routing} tile boundaries")
+    assert torch.isfinite(out.float()).all()
+    counts = np.bincount(inp.expert_ids.ravel(), minlength=inp.E)
+    lay = ws_view(m, ws)
+    np.testing.assert_array_equal(ws_i32(ws, lay.count, inp.E), counts)
+
+
+@pytest.mark.parametrize("T", [32, 128, 1024, 8192])
+def test_full_shape_sweep_points(full_model, T):
+    """The decode-to-prefill sweep's batch sizes (uniform ids): every token at
+    T = 32 and 128 (FC1's two-tile units start above 16 tokens; FC2's
+    accumulator slots widen at 32 and 64 rows), 256 sampled tokens plus the
+    tile-boundary tokens of the first 64 experts above that."""
+    minp, m = full_model
+    inp = _full_case(minp, T, "uniform", seed=200 + T)
+    out, ws = m.forward_inputs(inp)
+    torch.cuda.synchronize()
+    assert api.moe_read_status(ws) == (0, 0)
+    if T <= 128:
+        sample = np.arange(T)
+    else:
+        rs = np.random.default_rng(T)
+        ids = inp.expert_ids
+        bound = _tile_boundary_tokens(np.where(ids < 64, ids, 10 ** 6).astype(np.int32), 64)
+        sample = np.unique(np.concatenate([rs.choice(T, 256, replace=False), bound, [0, T - 1]]))
+    ref = cases.run_oracle(inp, tokens=sample)
+    assert_close(out_bits(out)[sample], ref, f"sweep T={T}")
+
+
+def _fc1_abs_sums(inp, toks):
+    """sum_h |x^_h| |w^_{e,n,h}| for every listed token's pairs and FC1 row,
+    from the oracle's quantized X and dequantized weights (fp64)."""
+    xq, xsf = oracle.nvfp4_quant_rows(gen.bf16_bits_to_f32(inp.x[toks]), q=inp.qX)
+    X = np.abs(oracle.nvfp4_dequant_rows(xq, xsf))
+    out = np.zeros((len(toks), inp.k, 2 * inp.I))
+    for ti, t in enumerate(toks):
+        for j in range(inp.k):
+            e = inp.expert_ids[t, j]
+            W = np.abs(oracle.nvfp4_dequant_rows(inp.w13[e], inp.sf13[e]))
+            out[ti, j] = W @ X[ti]
+    return out
+
+
+def test_full_shape_decode_intermediate_codes(full_model):
+    """The requantized intermediate A of every routed pair at T = 16, read from
+    the workspace, against the oracle's codes.  FC1's fp32 sums round in the
+    hardware's order, so a code may differ only where the oracle's SiTU value,
+    moved by at most the fp32 summation error of its pre-activations
+    (57 fp32 roundings of the sum of absolute products: one per K = 64 MMA
+    step and one for the product), crosses an E2M1 rounding midpoint -- or
+    where the group's block scale itself differs because its amax crosses an
+    E4M3 midpoint the same way.  The mismatch rate is reported."""
+    minp, m = full_model
+    T = 16
+    inp = _full_case(minp, T, "uniform", seed=T)
+    out, ws = m.forward_inputs(inp)
+    torch.cuda.synchronize()
+    assert api.moe_read_status(ws) == (0, 0)
+    lay = ws_view(m, ws)
+    I, k = inp.I, inp.k
+    toks = np.arange(T)
+    _, mid = cases.run_oracle(inp, tokens=toks, want_intermediates=True)
+    row_pos = ws_i32(ws, lay.row_pos, T * k)
+    npad = int(row_pos.max()) + 1
+    aq = ws_u8(ws, lay.aq, npad * (I // 2)).reshape(npad, I // 2)
+    sfa = ws_u8(ws, lay.sfa, ((npad + 127) // 128) * (I // 64) * 512)
+    dz = 57 * 2.0 ** -24 * _fc1_abs_sums(inp, toks) * inp.dXdW13[inp.expert_ids][..., None]
+    table = np.array([oracle.e2m1_value(c) for c in range(16)])
+    e4 = np.array(sorted({oracle.e4m3_value(c) for c in range(0x7F)}))
+    e4_mids = (e4[1:] + e4[:-1]) / 2
+    e2_mids = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0])
+    n_codes = n_code_mis = n_sf_mis = 0
+    for t in range(T):
+        for j in range(k):
+            e = inp.expert_ids[t, j]
+            p = row_pos[t * k + j]
+            z = mid["z"][t, j].astype(np.float64)
+            g, u, dg, du = z[:I], z[I:], dz[t, j, :I], dz[t, j, I:]
+            corners = np.stack([[oracle.situ(g[i] + sg * dg[i], u[i] + su * du[i]) for i in range(I)]
+                                for sg in (-1, 1) for su in (-1, 1)] +
+                               [[oracle.situ(g[i], u[i]) for i in range(I)]])
+            a_lo, a_hi = corners.min(0), corners.max(0)
+            got_codes = np.stack([aq[p] & 15, aq[p] >> 4], -1).ravel()
+            ref_codes = np.stack([mid["aq"][t, j] & 15, mid["aq"][t, j] >> 4], -1).ravel()
+            qa = np.float64(np.float32(inp.qA[e]))
+            for grp in range(I // 16):
+                sl = slice(16 * grp, 16 * grp + 16)
+                got_sf = sfa[oracle.scale_atom_offset(p, grp, I // 16)]
+                ref_sf = mid["asf"][t, j, grp]
+                n_codes += 16
+                if got_sf != ref_sf:
+                    amax_lo = np.max(np.minimum(np.abs(a_lo[sl]), np.abs(a_hi[sl]))) * qa / 6
+                    amax_hi = np.max(np.maximum(np.abs(a_lo[sl]), np.abs(a_hi[sl]))) * qa / 6
+                    crossed = ((e4_mids >= amax_lo * (1 - 1e-7)) & (e4_mids <= amax_hi * (1 + 1e-7))).any()
+                    assert crossed, f"scale of token {t} pair {j} group {grp} differs away from a boundary"
+                    n_sf_mis += 1
+                    continue
+                S = oracle.e4m3_value(int(ref_sf))
+                r = 0.0 if S == 0 else qa / S
+                bad = table[got_codes[sl]] != table[ref_codes[sl]]
+                for i in np.nonzero(bad)[0]:
+                    y_lo, y_hi = sorted((abs(a_lo[sl][i]) * r, abs(a_hi[sl][i]) * r))
+                    crossed = ((e2_mids >= y_lo * (1 - 1e-7)) & (e2_mids <= y_hi * (1 + 1e-7))).any()
+                    assert crossed, f"code of token {t} pair {j} element {16 * grp + i} differs away from a boundary"
+                    n_code_mis += 1
+    print(f"A codes: {n_code_mis} of {n_codes} differ, {n_sf_mis} block scales differ (all at rounding boundaries)")
+    assert n_code_mis <= 0.01 * n_codes
 
 @pytest.mark.parametrize("T", [2048, 16384])
 def test_back_to_back_forwards_share_a_workspace(full_model, T):

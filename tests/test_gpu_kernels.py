@@ -159,3 +159,25 @@ def test_codec_sweep_exhaustive():
         assert bad.size == 0, (f"start={start:#x}: {bad.size} mismatches, first bits={start + int(bad[0]):#010x} "
                                f"lo={g_lo[bad[0]]} hi={g_hi[bad[0]]} e4={g_e4[bad[0]]} oracle e2m1={r2[bad[0]]} "
                                f"e4m3={r4[bad[0]]}")
+
+
+@pytest.mark.parametrize("n,copies", [(256, 0), (128, 8), (256, 12)])
+def test_mma_peak_microbenchmark_runs(n, copies):
+    """The FP4 tensor-peak microbenchmark completes on every SM with a clean
+    status, and a longer run takes proportionally more cycles: the MMAs are
+    really issued (a plausible cost per MMA, neither skipped nor stalled)."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    cyc = torch.zeros(sms, dtype=torch.int64, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    per = []
+    for mmas in (1024, 4096):
+        api.moe_test_mma_peak(sms, n, mmas, copies, cyc, st)
+        torch.cuda.synchronize()
+        assert int(st.item()) == 0
+        c = cyc.cpu().numpy()
+        assert (c > 0).all()
+        per.append(float(np.median(c)) / mmas)
+    assert per[1] <= per[0] * 1.2
+    assert 16 <= per[1] <= 1024
+    with pytest.raises(api.MoeError):
+        api.moe_test_mma_peak(sms + 1, n, 1024, copies, cyc, st)
