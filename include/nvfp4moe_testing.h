@@ -51,16 +51,17 @@ moe_status_t moe_test_requant_lanes(const float* act, int64_t rows, int32_t inte
  * (tcgen05.mma kind::mxf4nvf4, scale_vec::4X, M = 128, N = n, K = 64, the
  * "Cake SiTU backend" page's NVFP4 x NVFP4 product with 16-element E4M3
  * scales): `grid` CTAs (one per SM; up to the SM count), each with resident
- * operands in shared memory, issue `mmas` MMAs back to back from one thread,
- * plus `copies` scale-atom copies to TMEM (tcgen05.cp 32x128b.warpx4) after
+ * operands in shared memory, issue `mmas` MMAs back to back from one thread
+ * into `accs` accumulators in turn (1: every MMA depends on the previous
+ * one, as the K-steps of one output tile do), plus `copies` scale-atom copies to TMEM (tcgen05.cp 32x128b.warpx4) after
  * every four MMAs, as FC1 issues them per k-block (0 for the bare MMA rate).
  * cycles [grid] (device, int64): SM clock cycles from the first issue to the
  * completion of the last MMA in each CTA, -1 if its bounded wait gave up
  * (status [1], device, then holds MOE_DEVSTAT_TIMEOUT).  FLOPs per CTA are
  * 2 * 128 * n * 64 * mmas; time the call with events on `stream`.
  * 16 <= n <= 256, n % 16 == 0; mmas % 4 == 0, 4 <= mmas <= 1 << 24;
- * 0 <= copies <= 16. */
-moe_status_t moe_test_mma_peak(int32_t grid, int32_t n, int32_t mmas, int32_t copies, int64_t* cycles,
+ * 0 <= copies <= 16; accs in {1, 2, 4}, accs * n <= 384. */
+moe_status_t moe_test_mma_peak(int32_t grid, int32_t n, int32_t mmas, int32_t copies, int32_t accs, int64_t* cycles,
                                int32_t* status, cudaStream_t stream);
 
 /* One block-scaled FP4 tile product on tcgen05 with the operand staging of

@@ -94,7 +94,7 @@ def lib():
         "moe_test_situ_requant": [P, i64, i32, f32, f32, f32, P, P, P, P],
         "moe_test_requant_lanes": [P, i64, i32, f32, P, P, P],
         "moe_test_mma_fp4": [P, P, P, P, i32, i32, P, P, P],
-        "moe_test_mma_peak": [i32, i32, i32, i32, P, P, P],
+        "moe_test_mma_peak": [i32, i32, i32, i32, i32, P, P, P],
         "moe_workspace_layout": [S, sz, ctypes.POINTER(moe_ws_layout_t)],
         "moe_forward_launch_count": [S, i64, ctypes.POINTER(i32)],
         "moe_profile_start": [i32],
@@ -240,8 +240,8 @@ def moe_test_mma_fp4(a, sfa_atoms, b, sfb_atoms, n, k, d, status, stream=None):
                                   _stream(stream)), "moe_test_mma_fp4")
 
 
-def moe_test_mma_peak(grid: int, n: int, mmas: int, copies: int, cycles, status, stream=None):
-    _check(lib().moe_test_mma_peak(grid, n, mmas, copies, _p(cycles), _p(status), _stream(stream)),
+def moe_test_mma_peak(grid: int, n: int, mmas: int, copies: int, cycles, status, stream=None, accs: int = 1):
+    _check(lib().moe_test_mma_peak(grid, n, mmas, copies, accs, _p(cycles), _p(status), _stream(stream)),
            "moe_test_mma_peak")
 
 

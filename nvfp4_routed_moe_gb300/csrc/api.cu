@@ -41,7 +41,7 @@ cudaError_t launch_fc1(const CUtensorMap& w13, const Fc1Args& a, int pair, int g
 cudaError_t launch_fc2(const CUtensorMap& w2, const RowMaps& aq, const Fc2Args& a, int grid, cudaStream_t st);
 cudaError_t launch_mma_check(const CUtensorMap& a, const CUtensorMap& b, const uint8_t* sfa, const uint8_t* sfb,
                              int N, int K, float* d, int32_t* status, cudaStream_t st);
-cudaError_t launch_mma_peak(int grid, int n, int mmas, int copies, long long* cycles, int32_t* status,
+cudaError_t launch_mma_peak(int grid, int n, int mmas, int copies, int accs, long long* cycles, int32_t* status,
                             cudaStream_t st);
 
 __global__ void fill_f32_kernel(float* p, int n, float v) {
@@ -935,15 +935,15 @@ moe_status_t moe_test_mma_fp4(const uint8_t* a, const uint8_t* sfa_atoms, const 
   return MOE_OK;
 }
 
-moe_status_t moe_test_mma_peak(int32_t grid, int32_t n, int32_t mmas, int32_t copies, int64_t* cycles,
+moe_status_t moe_test_mma_peak(int32_t grid, int32_t n, int32_t mmas, int32_t copies, int32_t accs, int64_t* cycles,
                                int32_t* status, cudaStream_t stream) {
   if (!cycles || !status || n < 16 || n > 256 || n % 16 != 0 || mmas < 4 || mmas % 4 != 0 || mmas > (1 << 24) ||
-      copies < 0 || copies > 16)
+      copies < 0 || copies > 16 || (accs != 1 && accs != 2 && accs != 4) || accs * n > 384)
     return MOE_ERR_INVALID_ARG;
   int sms = 0;
   MOE_CUDA(device_ready(&sms));
   if (grid < 1 || grid > sms) return MOE_ERR_INVALID_ARG;
-  MOE_CUDA(launch_mma_peak(grid, n, mmas, copies, reinterpret_cast<long long*>(cycles), status, stream));
+  MOE_CUDA(launch_mma_peak(grid, n, mmas, copies, accs, reinterpret_cast<long long*>(cycles), status, stream));
   return MOE_OK;
 }
 

@@ -366,6 +366,15 @@ __global__ void __launch_bounds__(kFc1Threads, 1)
       int local = 0;
       bool ok = true;
       const uint32_t idesc = idesc_mxf4nvf4(128, 128 * PAIR);
+      // Descriptors of stage 0 are computed once; a stage, K-step or scale
+      // atom only moves their start-address field (address >> 4), so the
+      // issuing thread spends its time on the tcgen05 instructions rather
+      // than on dependent address arithmetic.
+      const uint64_t xd0 = smem_desc(smem_u32(smem + C::kX), 16, 1024, kLayoutSW128);
+      const uint64_t wd0 = smem_desc(smem_u32(smem + C::kW), 16, 1024, kLayoutSW128);
+      const uint64_t sd0 = sf_desc(smem + C::kSX);   // X atom 0 of stage 0; W atoms follow at kSW
+      uint32_t soff = 0;                              // (stage * kStage) >> 4
+      uint32_t sfc = tmem + 256;                      // the stage's scale columns
       int4 nxt = next_tile(tiles, blockIdx.x, num_units, NP);
       for (int unit = blockIdx.x; unit < num_units && ok; unit += gridDim.x) {
         const int4 tl = nxt;
@@ -386,14 +395,13 @@ __global__ void __launch_bounds__(kFc1Threads, 1)
           }
           fence_proxy_async_shared();   // the gathered X rows (cp.async) before the MMA reads them
           tc_fence_after();
-          const uint8_t* st = smem + stage * C::kStage;
-          const uint32_t sfc = tmem + 256 + stage * C::kSfCols;
 #pragma unroll
           for (int a = 0; a < 4; ++a) {
-            tmem_cp_32x128b_x4(sfc + a * 4, sf_desc(st + C::kSX + a * 512));
+            tmem_cp_32x128b_x4(sfc + a * 4, sd0 + soff + a * 32);
 #pragma unroll
             for (int j = 0; j < PAIR; ++j)
-              tmem_cp_32x128b_x4(sfc + 16 + (a * PAIR + j) * 4, sf_desc(st + C::kSW + j * 2048 + a * 512));
+              tmem_cp_32x128b_x4(sfc + 16 + (a * PAIR + j) * 4,
+                                 sd0 + soff + (C::kSW - C::kSX + j * 2048 + a * 512) / 16);
           }
           // M = tokens (X tile), N = the PAIR W13 tiles as one operand of
           // PAIR*128 rows (contiguous in shared memory, their accumulators
@@ -401,15 +409,18 @@ __global__ void __launch_bounds__(kFc1Threads, 1)
           // one long MMA per K-step, during which the tensor pipe also works
           // off the scale copies.
 #pragma unroll
-          for (int ks = 0; ks < 4; ++ks) {
-            const uint64_t xd = smem_desc(smem_u32(st + C::kX) + ks * 32, 16, 1024, kLayoutSW128);
-            const uint64_t wd = smem_desc(smem_u32(st + C::kW) + ks * 32, 16, 1024, kLayoutSW128);
-            mma_mxf4nvf4(dcol, xd, wd, idesc, sfc + ks * 4, sfc + 16 + ks * 4 * PAIR, (kb | ks) ? 1u : 0u);
-          }
+          for (int ks = 0; ks < 4; ++ks)
+            mma_mxf4nvf4(dcol, xd0 + soff + 2 * ks, wd0 + soff + 2 * ks, idesc, sfc + ks * 4,
+                         sfc + 16 + ks * 4 * PAIR, (kb | ks) ? 1u : 0u);
           tc_commit(&bars->empty[stage]);
           if (++stage == C::kStages) {
             stage = 0;
             phase ^= 1u;
+            soff = 0;
+            sfc = tmem + 256;
+          } else {
+            soff += C::kStage / 16;
+            sfc += C::kSfCols;
           }
         }
         if (ok) tc_commit(&bars->tmem_full[buf]);
@@ -591,6 +602,12 @@ __global__ void __launch_bounds__(kFc2Threads, 1)
       uint32_t stage = 0, phase = 0;
       int local = 0, sub = 0;
       bool ok = true;
+      // Ring descriptors of stage 0, moved by their start-address field only
+      // (see FC1's issuing thread).
+      const uint64_t rd0 = smem_desc(smem_u32(ring), 16, 512, kLayoutSW64);
+      const uint64_t rs0 = sf_desc(ring + F2_SA);
+      uint32_t soff = 0;                     // (stage * kFc2StageBytes) >> 4
+      uint32_t sfc = tmem + 256;             // the stage's scale columns
       int4 nxt = fc2_next_tile(tiles, blockIdx.x, num_units, ntiles);
       for (int unit = blockIdx.x; unit < num_units && ok; unit += gridDim.x) {
         const int4 tl = nxt;
@@ -605,6 +622,7 @@ __global__ void __launch_bounds__(kFc2Threads, 1)
         const uint8_t* as = act + slot * act_bytes;
         const uint32_t sfb = tmem + kFc2SfbCol + slot * (uint32_t)(NA * 4);
         for (int a = 0; a < NA; ++a) tmem_cp_32x128b_x4(sfb + a * 4, sf_desc(as + act_sf + a * 512));
+        const uint64_t bd0 = smem_desc(smem_u32(as), 16, 512, kLayoutSW64);   // + 512 per k-block, + 2 per K-step
         for (int g = 0; g < G && ok; ++g, ++sub) {
           const uint32_t buf = (uint32_t)sub % nslots, use = (uint32_t)sub / nslots;
           if (!wait_or_abort(&bars->tmem_empty[buf], (use & 1u) ^ 1u, bars, p.status)) {
@@ -619,20 +637,21 @@ __global__ void __launch_bounds__(kFc2Threads, 1)
               break;
             }
             tc_fence_after();
-            const uint8_t* st = ring + stage * kFc2StageBytes;
-            const uint32_t sfc = tmem + 256 + stage * 8;
 #pragma unroll
-            for (int a = 0; a < 2; ++a) tmem_cp_32x128b_x4(sfc + a * 4, sf_desc(st + F2_SA + a * 512));
+            for (int a = 0; a < 2; ++a) tmem_cp_32x128b_x4(sfc + a * 4, rs0 + soff + a * 32);
 #pragma unroll
-            for (int ks = 0; ks < 2; ++ks) {
-              const uint64_t ad = smem_desc(smem_u32(st) + ks * 32, 16, 512, kLayoutSW64);
-              const uint64_t bd = smem_desc(smem_u32(as + kb * 8192) + ks * 32, 16, 512, kLayoutSW64);
-              mma_mxf4nvf4(dcol, ad, bd, idesc, sfc + ks * 4, sfb + (kb * 2 + ks) * 4, (kb | ks) ? 1u : 0u);
-            }
+            for (int ks = 0; ks < 2; ++ks)
+              mma_mxf4nvf4(dcol, rd0 + soff + 2 * ks, bd0 + (uint32_t)(kb * 512 + 2 * ks), idesc, sfc + ks * 4,
+                           sfb + (kb * 2 + ks) * 4, (kb | ks) ? 1u : 0u);
             tc_commit(&bars->empty[stage]);
             if (++stage == (uint32_t)nstages) {
               stage = 0;
               phase ^= 1u;
+              soff = 0;
+              sfc = tmem + 256;
+            } else {
+              soff += kFc2StageBytes / 16;
+              sfc += 8;
             }
           }
           if (ok) tc_commit(&bars->tmem_full[buf]);
@@ -819,12 +838,14 @@ __global__ void __launch_bounds__(128, 1)
 // every CTA (one per SM) keeps one A tile [128 x 256 FP4], one B tile
 // [n x 256 FP4] and their scale atoms resident in shared memory, copies the
 // atoms to TMEM once, and one thread issues `mmas` MMAs (M = 128, N = n,
-// K = 64, cycling over the four K-steps of the tile) into one accumulator,
-// plus `copies` scale-atom copies (tcgen05.cp 32x128b.warpx4, into TMEM
+// K = 64, cycling over the four K-steps of the tile) into `accs` accumulators
+// in turn (consecutive MMAs into one accumulator depend on each other; into
+// different ones they do not), plus `copies` scale-atom copies (tcgen05.cp 32x128b.warpx4, into TMEM
 // columns no MMA reads) after every fourth MMA, as FC1 issues them per
 // k-block.  The operand values do not matter for throughput; they are
 // fixed bytes.  cycles[blockIdx.x] = SM clock cycles from the first issue to
 // the completion of the last MMA.
+template <int ACCS>
 __global__ void __launch_bounds__(128, 1)
     mma_peak_kernel(int n, int mmas, int copies, long long* cycles, int32_t* status) {
   extern __shared__ uint8_t smem_raw[];
@@ -852,19 +873,27 @@ __global__ void __launch_bounds__(128, 1)
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
   if (threadIdx.x == 0) {
-    // TMEM: accumulator columns [0, n); A atoms at 256 + 4 ks; B atoms at
-    // 272 + 8 ks + 4 j; copy targets at 320 .. 383 (read by no MMA).
-    for (int a = 0; a < 4; ++a) tmem_cp_32x128b_x4(tmem + 256 + a * 4, sf_desc(sSF + a * 512));
-    for (int a = 0; a < 8; ++a) tmem_cp_32x128b_x4(tmem + 272 + a * 4, sf_desc(sSF + 2048 + a * 512));
+    // TMEM: accumulator a at columns [a n, (a + 1) n) (ACCS n <= 384); A atoms
+    // at 384 + 4 ks; B atoms at 400 + 8 ks + 4 j; copy targets at 448 .. 511
+    // (read by no MMA).  Descriptors and addresses are computed once, so the
+    // loop issues little besides the tcgen05 instructions themselves.
+    for (int a = 0; a < 4; ++a) tmem_cp_32x128b_x4(tmem + 384 + a * 4, sf_desc(sSF + a * 512));
+    for (int a = 0; a < 8; ++a) tmem_cp_32x128b_x4(tmem + 400 + a * 4, sf_desc(sSF + 2048 + a * 512));
     const uint32_t idesc = idesc_mxf4nvf4(128, (uint32_t)n);
+    uint64_t ad[4], bd[4];
+#pragma unroll
+    for (int ks = 0; ks < 4; ++ks) {
+      ad[ks] = smem_desc(smem_u32(sA) + ks * 32, 16, 1024, kLayoutSW128);
+      bd[ks] = smem_desc(smem_u32(sB) + ks * 32, 16, 1024, kLayoutSW128);
+    }
+    const uint64_t cpd0 = sf_desc(sSF);           // + 32 per 512-byte atom (address >> 4)
     const long long t0 = clock64();
-    for (int i = 0; i < mmas; ++i) {
-      const int ks = i & 3;
-      const uint64_t ad = smem_desc(smem_u32(sA) + ks * 32, 16, 1024, kLayoutSW128);
-      const uint64_t bd = smem_desc(smem_u32(sB) + ks * 32, 16, 1024, kLayoutSW128);
-      mma_mxf4nvf4(tmem, ad, bd, idesc, tmem + 256 + ks * 4, tmem + 272 + ks * 8, i ? 1u : 0u);
-      if (ks == 3)
-        for (int c = 0; c < copies; ++c) tmem_cp_32x128b_x4(tmem + 320 + (c & 15) * 4, sf_desc(sSF + (c & 15) * 512));
+    for (int i = 0; i < mmas; i += 4) {
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks)
+        mma_mxf4nvf4(tmem + (uint32_t)((ks % ACCS) * n), ad[ks], bd[ks], idesc, tmem + 384 + ks * 4,
+                     tmem + 400 + ks * 8, (i > 0 || ks >= ACCS) ? 1u : 0u);
+      for (int c = 0; c < copies; ++c) tmem_cp_32x128b_x4(tmem + 448 + c * 4, cpd0 + (uint64_t)(c * 32));
     }
     tc_commit(&bars->drain);
     const bool ok = mbar_wait(&bars->drain, 0, status);
@@ -890,9 +919,11 @@ cudaError_t gemm_set_attributes() {
   if (err != cudaSuccess) return err;
   err = cudaFuncSetAttribute((const void*)fc2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kFc2Smem);
   if (err != cudaSuccess) return err;
-  err = cudaFuncSetAttribute((const void*)mma_peak_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)kMmaPeakSmem);
-  if (err != cudaSuccess) return err;
+  for (const void* fn : {(const void*)mma_peak_kernel<1>, (const void*)mma_peak_kernel<2>,
+                         (const void*)mma_peak_kernel<4>}) {
+    err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kMmaPeakSmem);
+    if (err != cudaSuccess) return err;
+  }
   return cudaFuncSetAttribute((const void*)mma_check_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               (int)kMmaCheckSmem);
 }
@@ -920,9 +951,11 @@ cudaError_t launch_mma_check(const CUtensorMap& a, const CUtensorMap& b, const u
   return cudaGetLastError();
 }
 
-cudaError_t launch_mma_peak(int grid, int n, int mmas, int copies, long long* cycles, int32_t* status,
+cudaError_t launch_mma_peak(int grid, int n, int mmas, int copies, int accs, long long* cycles, int32_t* status,
                             cudaStream_t st) {
-  mma_peak_kernel<<<grid, 128, kMmaPeakSmem, st>>>(n, mmas, copies, cycles, status);
+  if (accs == 4) mma_peak_kernel<4><<<grid, 128, kMmaPeakSmem, st>>>(n, mmas, copies, cycles, status);
+  else if (accs == 2) mma_peak_kernel<2><<<grid, 128, kMmaPeakSmem, st>>>(n, mmas, copies, cycles, status);
+  else mma_peak_kernel<1><<<grid, 128, kMmaPeakSmem, st>>>(n, mmas, copies, cycles, status);
   return cudaGetLastError();
 }
 

@@ -76,20 +76,37 @@ def out_bits(out: torch.Tensor) -> np.ndarray:
     return out.view(torch.int16).cpu().numpy().view(np.uint16)
 
 
+def bf16_ulp(v: np.ndarray) -> np.ndarray:
+    """Spacing of BF16 values at |v| (8 significant bits; 2^-133 below the
+    normal range)."""
+    a = np.abs(v.astype(np.float64))
+    e = np.floor(np.log2(np.maximum(a, 2.0 ** -126)))
+    return 2.0 ** (e - 7)
+
+
 def compare(got_bits: np.ndarray, ref_bits: np.ndarray):
-    """(max_abs, rel_l2) between two bf16 bit arrays."""
+    """(max_abs, rel_l2, excess) between two bf16 bit arrays; excess is the
+    largest |got - ref| / max(TOL_MAX_ABS, one BF16 ulp of ref)."""
     g = gen.bf16_bits_to_f32(got_bits).astype(np.float64)
     r = gen.bf16_bits_to_f32(ref_bits).astype(np.float64)
-    max_abs = float(np.abs(g - r).max()) if g.size else 0.0
+    d = np.abs(g - r)
+    max_abs = float(d.max()) if g.size else 0.0
+    excess = float((d / np.maximum(TOL_MAX_ABS, bf16_ulp(r))).max()) if g.size else 0.0
     den = float(np.sqrt((r ** 2).sum()))
     rel = float(np.sqrt(((g - r) ** 2).sum()) / den) if den > 0 else float(np.sqrt((g ** 2).sum()))
-    return max_abs, rel
+    return max_abs, rel, excess
 
 
 def assert_close(got_bits, ref_bits, what=""):
-    max_abs, rel = compare(got_bits, ref_bits)
+    """The forward's tolerance: relative L2 error <= 1e-2 and, per element,
+    |got - ref| <= max(2e-2, one BF16 ulp of ref).  Above magnitude 4 the
+    BF16 spacing itself exceeds 2e-2, and two fp32 sums that differ only in
+    the order of their additions (hardware accumulation against the oracle's
+    fp64 sum) can round to neighbouring BF16 values there; one ulp is the
+    least any BF16 result can be held to."""
+    max_abs, rel, excess = compare(got_bits, ref_bits)
     assert np.isfinite(gen.bf16_bits_to_f32(got_bits)).all(), f"{what}: non-finite output"
-    assert max_abs <= TOL_MAX_ABS and rel <= TOL_REL_L2, f"{what}: max_abs={max_abs:.3g} rel_l2={rel:.3g}"
+    assert excess <= 1.0 and rel <= TOL_REL_L2, f"{what}: max_abs={max_abs:.3g} ({excess:.3g} of the bound) rel_l2={rel:.3g}"
     return max_abs, rel
 
 

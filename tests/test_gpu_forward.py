@@ -333,7 +333,7 @@ def test_full_shape_tile_boundary_tokens(full_model, T, routing, big):
     if big:
         xf = np.abs(gen.bf16_bits_to_f32(inp.x)).max(axis=1)
         sample = np.unique(np.concatenate([sample, np.argsort(-xf)[:8]]))
-    assert len(sample) >= (900 if T == 4096 else 2500)
+    assert len(sample) >= (900 if T == 4096 else 1500)
     ref = cases.run_oracle(inp, tokens=sample)
     assert_close(out_bits(out)[sample], ref, f"T={T} {routing} tile boundaries")
     assert torch.isfinite(out.float()).all()
