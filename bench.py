@@ -110,7 +110,7 @@ def init_routing_sweep(shp, flush, dev):
             call()
         evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(20)]
         for a, c in evs:
-            flush.fill_(1)
+            flush()
             a.record()
             call()
             c.record()
@@ -122,6 +122,22 @@ def init_routing_sweep(shp, flush, dev):
     return res
 
 
+class L2Flush:
+    """Evicts this step's data from L2 between timed steps: writes a 512 MB
+    buffer (larger than the 129 MB L2), then reads a second 256 MB one, so
+    that the lines the write left dirty are written back here, outside the
+    timed region, and not by the next step's kernels."""
+
+    def __init__(self):
+        import torch
+        self.w = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
+        self.r = torch.zeros(256 << 20, dtype=torch.uint8, device="cuda")
+
+    def __call__(self):
+        self.w.fill_(1)
+        self.r.max()
+
+
 def median_ms(call, flush, n=20):
     """Median CUDA-event time of `call` over n runs, L2 flushed before each."""
     import torch
@@ -129,7 +145,7 @@ def median_ms(call, flush, n=20):
         call()
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
     for a, c in evs:
-        flush.fill_(1)
+        flush()
         a.record()
         call()
         c.record()
@@ -660,7 +676,7 @@ def main():
     sweep = None
     if not args.no_sweep and world == 1:
         sweep = {}
-        flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
+        flush = L2Flush()
         for name, T_s, routing in (("decode1", 1, "uniform"), ("decode8", 8, "uniform"), ("decode16", 16, "uniform"),
                                    ("T32", 32, "uniform"), ("T128", 128, "uniform"), ("T512", 512, "uniform"),
                                    ("T1024", 1024, "uniform"), ("T2048", 2048, "uniform"), ("prefill", 4096, "zipf"),
@@ -674,7 +690,7 @@ def main():
             n_s = 20
             evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_s)]
             for a, c in evs:
-                flush.fill_(1)
+                flush()
                 a.record()
                 forward(b, ws_s, out_s)
                 c.record()
@@ -687,7 +703,7 @@ def main():
             for _ in range(3):
                 g.replay()
             for a, c in evs:
-                flush.fill_(1)
+                flush()
                 a.record()
                 g.replay()
                 c.record()
@@ -696,7 +712,7 @@ def main():
             del g
             api.moe_profile_start(n_s)           # stage breakdown in a separate pass
             for _ in range(n_s):
-                flush.fill_(1)
+                flush()
                 forward(b, ws_s, out_s)
             torch.cuda.synchronize()
             st_ms, nc = api.moe_profile_stop()
@@ -709,6 +725,7 @@ def main():
                            "fc2_hbm_frac": fc2_bytes(T_s, b["n_active"]) / (st_ms["fc2"] / nc * 1e-3) / 1e9 / peak}
             if fp4:
                 sweep[name]["tensor_frac"] = (b["pairs"] * FLOPS_PER_PAIR / (t_ms * 1e-3) / 1e12) / fp4["tflops"]
+        sweep["l2_flush"] = "between timed steps: 512 MB written, then 256 MB read (write-backs outside the timed region)"
         sweep["init_routing"] = init_routing_sweep(shp, flush, dev)
         sweep["next_rows"] = next_rows_sweep(shp, flush, dev, w, scales, winp, peak)
         del flush
