@@ -299,6 +299,24 @@ static int fc1_pair(const Shape& s, int64_t T) {
 
 static int forward_launches(int64_t P) { return (P <= kRouteSmallMax ? 1 : 2) + 4 + (P > kSfTwoPassMin ? 1 : 0); }
 
+// FC2's CTAs take their units from a work counter that routing seeds on every
+// call (NVFP4MOE_FC2_DYNAMIC=0: the static stride instead).
+static int fc2_dynamic() {
+  const char* v = std::getenv("NVFP4MOE_FC2_DYNAMIC");
+  return (v && v[0] == '0') ? 0 : 1;
+}
+
+// FC2's ring stages hold a whole output tile (all I/128 k-blocks) up to this
+// many tokens and one k-block above: whole-tile stages halve the issuing
+// thread's per-stage waits and commits, while large batches, bound by the
+// combine's reductions, keep more and smaller stages in flight
+// (NVFP4MOE_FC2_TILE_STAGES=0/1 overrides).
+constexpr int64_t kFc2TileStageMaxTokens = 8192;
+static bool fc2_tile_stages(int64_t T) {
+  if (const char* v = std::getenv("NVFP4MOE_FC2_TILE_STAGES")) return v[0] == '1';
+  return T <= kFc2TileStageMaxTokens;
+}
+
 // Passes of the FC2 combine over H: the fewest (a divisor of H/128) whose
 // accumulator slice, T x H/nq fp32, fits the L2 budget (NVFP4MOE_ACC_PASS_MB
 // overrides the default budget).
@@ -569,6 +587,9 @@ static moe_status_t forward_impl(const moe_shape_t* shape, int32_t expert_begin,
   f2.dAdW2 = dA_dW2;
   f2.acc = reinterpret_cast<float*>(w + L.acc);
   f2.nq = nq;
+  f2.kbs_per_stage = fc2_tile_stages(T) ? NKB2 : 1;
+  f2.next = ra.hdr + HDR_FC2_NEXT;
+  f2.dynamic = fc2_dynamic();
   f2.status = ra.hdr + HDR_STATUS;
   f2.H = s.H;
   f2.I = s.I;

@@ -74,16 +74,20 @@ constexpr int kFc1Gather = 32 * kFc1Producer;   // gather threads (warps 0 and 1
 constexpr int kFc1Threads = 32 * (kFc1Epi0 + kFc1EpiWarps);
 // FC2 shared memory: barriers (1 KB) | two activation slots (a token tile's
 // A codes [I/128 k-blocks][128 rows x 64 B] + its I/64 scale atoms) | ring of
-// W2 stages (A [128 x 64 B] | SF 2 atoms); the stage count follows from I.
+// W2 stages of KS k-blocks of one 128-feature output tile: their codes
+// [KS][128 rows x 64 B] then their 2*KS scale atoms (9 KB per k-block).  KS
+// is 1 or I/128 (a whole output tile, so that the issuing thread waits,
+// fences and commits once per tile, which pays at small and medium batches);
+// the stage count follows from I and KS.
 constexpr int kMaxStages = 24;
-constexpr int kFc2StageBytes = 9216;
-constexpr int F2_SA = 8192;
+constexpr int kFc2KbBytes = 9216;   // codes (8 KB) + scale atoms (1 KB) of one k-block
 constexpr int kFc2EpiWarps = 16;
 constexpr int kFc2Threads = 64 + 32 * kFc2EpiWarps;
 constexpr int kFc2MaxI = 512;
 constexpr uint32_t kFc2SfbCol = 448;   // TMEM column of the activation slots' scale factors
 
 constexpr int kMaxAccSlots = 16;
+constexpr int kUnitQueue = 8;   // entries of a CTA's work-unit queue
 
 struct Barriers {
   uint64_t full[kMaxStages];
@@ -93,6 +97,10 @@ struct Barriers {
   uint64_t act_full[2];
   uint64_t act_empty[2];
   uint64_t drain;
+  uint64_t uq_full[kUnitQueue];   // work-unit queue: entry published by the producer thread
+  uint64_t uq_empty[kUnitQueue];  // ... read by every consuming role
+  int4 uq_tile[kUnitQueue];
+  int32_t uq_unit[kUnitQueue];
   uint32_t tmem_base;
   volatile int32_t abort_flag;
   int32_t fc2_g;         // FC2: output tiles per work unit, chosen by thread 0 during setup
@@ -102,12 +110,18 @@ static_assert(sizeof(Barriers) <= 1024, "barrier block");
 constexpr size_t kFc2Smem = 232448;    // the opt-in maximum; carved up at run time
 
 __host__ __device__ constexpr int fc2_act_bytes(int I) { return (128 * (I / 2) + (I / 64) * 512 + 1023) / 1024 * 1024; }
-__host__ __device__ constexpr int fc2_stages(int I) {
-  return ((int)kFc2Smem - 1024 - 1024 - 2 * fc2_act_bytes(I)) / kFc2StageBytes < kMaxStages
-             ? ((int)kFc2Smem - 1024 - 1024 - 2 * fc2_act_bytes(I)) / kFc2StageBytes
+__host__ __device__ constexpr int fc2_stages(int I, int KS) {
+  return ((int)kFc2Smem - 1024 - 1024 - 2 * fc2_act_bytes(I)) / (KS * kFc2KbBytes) < kMaxStages
+             ? ((int)kFc2Smem - 1024 - 1024 - 2 * fc2_act_bytes(I)) / (KS * kFc2KbBytes)
              : kMaxStages;
 }
-static_assert(fc2_stages(kFc2MaxI) >= 8 && 256 + 8 * kMaxStages <= (int)kFc2SfbCol &&
+// per stage 2*KS scale atoms of 4 TMEM columns from column 256, below the
+// activation slots' scale columns
+constexpr bool fc2_plan_ok(int I) {
+  return fc2_stages(I, I / 128) >= 4 && 256 + fc2_stages(I, I / 128) * (I / 64) * 4 <= (int)kFc2SfbCol &&
+         256 + fc2_stages(I, 1) * 8 <= (int)kFc2SfbCol;
+}
+static_assert(fc2_plan_ok(128) && fc2_plan_ok(256) && fc2_plan_ok(384) && fc2_plan_ok(512) &&
                   kFc2SfbCol + 2 * (kFc2MaxI / 64) * 4 <= kTmemCols,
               "FC2 shared memory / TMEM plan");
 
@@ -137,7 +151,8 @@ __device__ __forceinline__ uint8_t* aligned_smem(uint8_t* raw) {
 __device__ __forceinline__ uint64_t sf_desc(const uint8_t* p) { return smem_desc(smem_u32(p), 0, 128, kLayoutNone); }
 
 template <int STAGES, int EPI_WARPS>
-__device__ void gemm_setup(Barriers* bars, int warp, int tmem_warp, uint32_t full_arrivals = 1) {
+__device__ void gemm_setup(Barriers* bars, int warp, int tmem_warp, uint32_t full_arrivals = 1,
+                           uint32_t uq_consumers = 1) {
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&bars->full[s], full_arrivals);
@@ -152,6 +167,10 @@ __device__ void gemm_setup(Barriers* bars, int warp, int tmem_warp, uint32_t ful
       mbar_init(&bars->act_empty[b], 1);
     }
     mbar_init(&bars->drain, 1);
+    for (int q = 0; q < kUnitQueue; ++q) {
+      mbar_init(&bars->uq_full[q], 1);
+      mbar_init(&bars->uq_empty[q], uq_consumers);
+    }
     bars->abort_flag = 0;
     fence_barrier_init();
   }
@@ -172,6 +191,36 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, Ba
   bars->abort_flag = 1;
   return false;
 }
+
+// Work-unit queue of a persistent GEMM CTA.  The producer thread takes the
+// CTA's next unit (from the call's work counter, or the static stride) and
+// publishes (unit, tile descriptor) entries in order, one entry ahead of the
+// unit it streams; the other roles read them in the same order, each entry
+// and the one after it, and release an entry once past it.  Unit -1 ends the
+// sequence.  Waits are bounded like every other.
+__device__ __forceinline__ bool uq_publish(Barriers* bars, int j, int unit, int4 tile, int32_t* status) {
+  const int q = j % kUnitQueue;
+  if (!wait_or_abort(&bars->uq_empty[q], ((uint32_t)(j / kUnitQueue) & 1u) ^ 1u, bars, status)) return false;
+  volatile int* t = reinterpret_cast<volatile int*>(bars->uq_tile + q);
+  t[0] = tile.x;
+  t[1] = tile.y;
+  t[2] = tile.z;
+  t[3] = tile.w;
+  reinterpret_cast<volatile int32_t*>(bars->uq_unit)[q] = unit;
+  mbar_arrive(&bars->uq_full[q]);
+  return true;
+}
+
+// Unit of entry j (-1: the end; -2: the wait gave up) and its tile descriptor.
+__device__ __forceinline__ int uq_read(Barriers* bars, int j, int4& tile, int32_t* status) {
+  const int q = j % kUnitQueue;
+  if (!wait_or_abort(&bars->uq_full[q], (uint32_t)(j / kUnitQueue) & 1u, bars, status)) return -2;
+  const volatile int* t = reinterpret_cast<const volatile int*>(bars->uq_tile + q);
+  tile = make_int4(t[0], t[1], t[2], t[3]);
+  return reinterpret_cast<const volatile int32_t*>(bars->uq_unit)[q];
+}
+
+__device__ __forceinline__ void uq_release(Barriers* bars, int j) { mbar_arrive(&bars->uq_empty[j % kUnitQueue]); }
 
 // A tile descriptor from the routing kernel is trusted only after a bounds
 // check; a bad one is skipped by every role alike and flagged.
@@ -500,6 +549,9 @@ __global__ void __launch_bounds__(kFc1Threads, 1)
 }
 
 // ================================================================== FC2
+// WHOLE: ring stages of a whole output tile (KS = I/128 k-blocks); else one
+// k-block per stage.
+template <bool WHOLE>
 __global__ void __launch_bounds__(kFc2Threads, 1)
     fc2_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_constant__ RowMaps tm_aq,
                const Fc2Args p) {
@@ -508,9 +560,10 @@ __global__ void __launch_bounds__(kFc2Threads, 1)
   Barriers* bars = reinterpret_cast<Barriers*>(smem);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int NMT = p.H / 128, NKB = p.I / kFc2KBlock, NA = p.I / 64, npu = NMT / p.nq;
-  const int act_bytes = fc2_act_bytes(p.I), nstages = fc2_stages(p.I);
+  const int KS = WHOLE ? NKB : 1;   // k-blocks per ring stage
+  const int act_bytes = fc2_act_bytes(p.I), nstages = fc2_stages(p.I, KS), stage_bytes = KS * kFc2KbBytes;
   uint8_t* act = smem + 1024;                       // slot s at act + s * act_bytes
-  uint8_t* ring = act + 2 * act_bytes;              // stage s at ring + s * kFc2StageBytes
+  uint8_t* ring = act + 2 * act_bytes;              // stage s at ring + s * stage_bytes
   const uint32_t act_sf = (uint32_t)(NKB * 8192);   // scale atoms after the codes of a slot
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tm_w2);
@@ -523,7 +576,7 @@ __global__ void __launch_bounds__(kFc2Threads, 1)
     // group size and the setup barrier shares it.
     bars->fc2_g = fc2_group(clamp_tiles(__ldcg(p.hdr + HDR_NUM_TT), p.max_tiles), NMT, npu, gridDim.x);
   }
-  gemm_setup<kMaxStages, kFc2EpiWarps>(bars, warp, 1);
+  gemm_setup<kMaxStages, kFc2EpiWarps>(bars, warp, 1, 1, 1 + kFc2EpiWarps);
   const uint32_t tmem = bars->tmem_base;
   pdl_wait();
   pdl_launch_dependents();
@@ -547,16 +600,34 @@ __global__ void __launch_bounds__(kFc2Threads, 1)
       uint32_t act_armed = 0, act_last = 0;  // activation slots
       int local = 0;
       bool ok = true;
-      int4 nxt = fc2_next_tile(tiles, blockIdx.x, num_units, ntiles);
-      for (int unit = blockIdx.x; unit < num_units && ok; unit += gridDim.x) {
-        const int4 tl = nxt;
-        nxt = fc2_next_tile(tiles, unit + gridDim.x, num_units, ntiles);
-        if (!tile_ok(tl, p.E, p.max_rows)) {
+      // The CTA's units: taken from the work counter (seeded by routing on
+      // every call) or by the static stride, each published one unit ahead
+      // of the W2 stream that serves it.
+      int taken = 0;
+      auto take = [&]() -> int {
+        const int u = p.dynamic ? atomicAdd(p.next, 1) : (int)blockIdx.x + taken * (int)gridDim.x;
+        ++taken;
+        return (u >= 0 && u < num_units) ? u : -1;
+      };
+      int qj = 0;
+      int unit = take();
+      int4 tl = fc2_next_tile(tiles, unit < 0 ? num_units : unit, num_units, ntiles);
+      ok = uq_publish(bars, qj++, unit, tl, p.status);
+      while (ok && unit >= 0) {
+        const int un = take();
+        const int4 tn = fc2_next_tile(tiles, un < 0 ? num_units : un, num_units, ntiles);
+        if (!uq_publish(bars, qj++, un, tn, p.status)) break;
+        const int cur = unit;
+        const int4 ct = tl;
+        unit = un;
+        tl = tn;
+        if (!tile_ok(ct, p.E, p.max_rows)) {
           set_status(p.status, DEVSTAT_BAD_TILE);
           continue;
         }
-        const int mt0 = (unit / ntiles) * G;
-        const int e = tl.x, row0 = tl.y, rows = tl.z;
+        const int4 tlc = ct;
+        const int mt0 = (cur / ntiles) * G;
+        const int e = tlc.x, row0 = tlc.y, rows = tlc.z;
         const int nch = (rows + kTokChunk - 1) / kTokChunk;
         // the token tile's activations, once per unit
         const uint32_t slot = (uint32_t)local & 1u, sph = ((uint32_t)local >> 1) & 1u;
@@ -571,18 +642,19 @@ __global__ void __launch_bounds__(kFc2Threads, 1)
         // the group's W2 tiles through the ring
         for (int g = 0; g < G && ok; ++g) {
           const int mt = mt0 + g;
-          for (int kb = 0; kb < NKB; ++kb) {
+          for (int kb0 = 0; kb0 < NKB; kb0 += KS) {
             if (!wait_or_abort(&bars->empty[stage], phase ^ 1u, bars, p.status)) {
               ok = false;
               break;
             }
-            uint8_t* st = ring + stage * kFc2StageBytes;
-            mbar_arrive_expect_tx(&bars->full[stage], 8192u + 1024u);
+            uint8_t* st = ring + stage * stage_bytes;
+            mbar_arrive_expect_tx(&bars->full[stage], (uint32_t)stage_bytes);
             armed |= 1u << stage;
             last_phase = (last_phase & ~(1u << stage)) | (phase << stage);
-            tma_load_3d(st, &tm_w2, 0, 0, (e * NMT + mt) * NKB + kb, &bars->full[stage]);
-            bulk_g2s(st + F2_SA, p.sf2p + ((size_t)(e * NMT + mt) * NA + (size_t)kb * 2) * 512u, 1024u,
-                     &bars->full[stage]);
+            for (int j = 0; j < KS; ++j)
+              tma_load_3d(st + j * 8192, &tm_w2, 0, 0, (e * NMT + mt) * NKB + kb0 + j, &bars->full[stage]);
+            bulk_g2s(st + KS * 8192, p.sf2p + ((size_t)(e * NMT + mt) * NA + (size_t)kb0 * 2) * 512u,
+                     (uint32_t)(KS * 1024), &bars->full[stage]);
             if (++stage == (uint32_t)nstages) {
               stage = 0;
               phase ^= 1u;
@@ -604,14 +676,18 @@ __global__ void __launch_bounds__(kFc2Threads, 1)
       bool ok = true;
       // Ring descriptors of stage 0, moved by their start-address field only
       // (see FC1's issuing thread).
-      const uint64_t rd0 = smem_desc(smem_u32(ring), 16, 512, kLayoutSW64);
-      const uint64_t rs0 = sf_desc(ring + F2_SA);
-      uint32_t soff = 0;                     // (stage * kFc2StageBytes) >> 4
+      const uint64_t rd0 = smem_desc(smem_u32(ring), 16, 512, kLayoutSW64);   // + 512 per k-block, + 2 per K-step
+      const uint64_t rs0 = sf_desc(ring + KS * 8192);                          // + 32 per scale atom
+      uint32_t soff = 0;                     // (stage * stage_bytes) >> 4
       uint32_t sfc = tmem + 256;             // the stage's scale columns
-      int4 nxt = fc2_next_tile(tiles, blockIdx.x, num_units, ntiles);
-      for (int unit = blockIdx.x; unit < num_units && ok; unit += gridDim.x) {
-        const int4 tl = nxt;
-        nxt = fc2_next_tile(tiles, unit + gridDim.x, num_units, ntiles);
+      int qj = 0;
+      int4 tn;
+      int unit = uq_read(bars, 0, tn, p.status);
+      while (unit >= 0 && ok) {
+        const int4 tl = tn;
+        unit = uq_read(bars, qj + 1, tn, p.status);   // the next entry (published already or soon)
+        uq_release(bars, qj++);
+        if (unit == -2) break;
         if (!tile_ok(tl, p.E, p.max_rows)) continue;
         const uint32_t ncols = (uint32_t)((tl.z + kTokChunk - 1) / kTokChunk * kTokChunk);
         const uint32_t idesc = idesc_mxf4nvf4(128, ncols);
@@ -631,18 +707,22 @@ __global__ void __launch_bounds__(kFc2Threads, 1)
           }
           tc_fence_after();
           const uint32_t dcol = tmem + buf * slot_cols;
-          for (int kb = 0; kb < NKB; ++kb) {
+          for (int kb0 = 0; kb0 < NKB && ok; kb0 += KS) {
             if (!wait_or_abort(&bars->full[stage], phase, bars, p.status)) {
               ok = false;
               break;
             }
             tc_fence_after();
+#pragma unroll 2
+            for (int a = 0; a < 2 * KS; ++a) tmem_cp_32x128b_x4(sfc + a * 4, rs0 + soff + a * 32);
+#pragma unroll 1
+            for (int j = 0; j < KS; ++j) {
+              const int kb = kb0 + j;
 #pragma unroll
-            for (int a = 0; a < 2; ++a) tmem_cp_32x128b_x4(sfc + a * 4, rs0 + soff + a * 32);
-#pragma unroll
-            for (int ks = 0; ks < 2; ++ks)
-              mma_mxf4nvf4(dcol, rd0 + soff + 2 * ks, bd0 + (uint32_t)(kb * 512 + 2 * ks), idesc, sfc + ks * 4,
-                           sfb + (kb * 2 + ks) * 4, (kb | ks) ? 1u : 0u);
+              for (int ks = 0; ks < 2; ++ks)
+                mma_mxf4nvf4(dcol, rd0 + soff + (uint32_t)(j * 512 + 2 * ks), bd0 + (uint32_t)(kb * 512 + 2 * ks),
+                             idesc, sfc + (j * 2 + ks) * 4, sfb + (kb * 2 + ks) * 4, (kb | ks) ? 1u : 0u);
+            }
             tc_commit(&bars->empty[stage]);
             if (++stage == (uint32_t)nstages) {
               stage = 0;
@@ -650,8 +730,8 @@ __global__ void __launch_bounds__(kFc2Threads, 1)
               soff = 0;
               sfc = tmem + 256;
             } else {
-              soff += kFc2StageBytes / 16;
-              sfc += 8;
+              soff += (uint32_t)(stage_bytes / 16);
+              sfc += (uint32_t)(KS * 8);
             }
           }
           if (ok) tc_commit(&bars->tmem_full[buf]);
@@ -685,15 +765,19 @@ __global__ void __launch_bounds__(kFc2Threads, 1)
         }
       }
     };
-    int4 nxt = fc2_next_tile(tiles, blockIdx.x, num_units, ntiles);
+    // The unit after the current one comes from the queue one entry ahead,
+    // so its scale and columns load while the current unit drains.
+    int qj = 0;
+    int4 nxt;
+    int unit_nxt = uq_read(bars, 0, nxt, p.status);
     float s2_nxt = (nxt.x >= 0 && nxt.x < p.E) ? __ldg(p.dAdW2 + nxt.x) : 0.0f;
     float wgt_nxt[NI];
     int tok_nxt[NI];
     if (tile_ok(nxt, p.E, p.max_rows)) columns(nxt, wgt_nxt, tok_nxt);
     else columns(make_int4(-1, 0, 0, 0), wgt_nxt, tok_nxt);
-    int4 nxt2 = fc2_next_tile(tiles, blockIdx.x + gridDim.x, num_units, ntiles);
     bool ok = true;
-    for (int unit = blockIdx.x; unit < num_units && ok; unit += gridDim.x) {
+    while (unit_nxt >= 0 && ok) {
+      const int unit = unit_nxt;
       const int4 tl = nxt;
       const float s2 = s2_nxt;
       float wgt[NI];
@@ -703,11 +787,14 @@ __global__ void __launch_bounds__(kFc2Threads, 1)
         wgt[i] = wgt_nxt[i];
         tok[i] = tok_nxt[i];
       }
-      nxt = nxt2;
+      unit_nxt = uq_read(bars, qj + 1, nxt, p.status);
+      __syncwarp();
+      if (lane == 0) uq_release(bars, qj);
+      ++qj;
+      if (unit_nxt == -2) break;
       s2_nxt = (nxt.x >= 0 && nxt.x < p.E) ? __ldg(p.dAdW2 + nxt.x) : 0.0f;
       if (tile_ok(nxt, p.E, p.max_rows)) columns(nxt, wgt_nxt, tok_nxt);
       else columns(make_int4(-1, 0, 0, 0), wgt_nxt, tok_nxt);
-      nxt2 = fc2_next_tile(tiles, unit + 2 * gridDim.x, num_units, ntiles);
       if (!tile_ok(tl, p.E, p.max_rows)) continue;
       const int mt0 = (unit / ntiles) * G;
       const int rows = tl.z;
@@ -917,7 +1004,11 @@ cudaError_t gemm_set_attributes() {
   err = cudaFuncSetAttribute((const void*)fc1_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)Fc1Cfg<2>::kSmem);
   if (err != cudaSuccess) return err;
-  err = cudaFuncSetAttribute((const void*)fc2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kFc2Smem);
+  err = cudaFuncSetAttribute((const void*)fc2_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kFc2Smem);
+  if (err != cudaSuccess) return err;
+  err = cudaFuncSetAttribute((const void*)fc2_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kFc2Smem);
   if (err != cudaSuccess) return err;
   for (const void* fn : {(const void*)mma_peak_kernel<1>, (const void*)mma_peak_kernel<2>,
                          (const void*)mma_peak_kernel<4>}) {
@@ -942,7 +1033,8 @@ cudaError_t launch_fc2(const CUtensorMap& w2, const RowMaps& aq, const Fc2Args& 
   RowMaps m1 = aq;
   Fc2Args args = a;
   void* kargs[] = {&m0, &m1, &args};
-  return launch_with_pdl((const void*)fc2_kernel, dim3(grid), dim3(kFc2Threads), kFc2Smem, st, kargs);
+  const void* fn = a.kbs_per_stage > 1 ? (const void*)fc2_kernel<true> : (const void*)fc2_kernel<false>;
+  return launch_with_pdl(fn, dim3(grid), dim3(kFc2Threads), kFc2Smem, st, kargs);
 }
 
 cudaError_t launch_mma_check(const CUtensorMap& a, const CUtensorMap& b, const uint8_t* sfa, const uint8_t* sfb,

@@ -34,6 +34,7 @@ enum : int {
   HDR_STREAM_N = 8,    // streamed chunk: valid tokens
   HDR_SKIP = 9,        // 1: routing found no valid preparation stamp and did nothing; later kernels skip too
   HDR_STREAM_BASE = 10,  // streamed chunk: first logical token (int64, words 10-11)
+  HDR_FC2_NEXT = 12,   // FC2's work counter: next unit to take (seeded to 0 by routing on every call)
   HDR_STAMP = 16,      // preparation stamp, kStampWords words: magic, H, I, E, k, token capacity
   HDR_WORDS = 64,
 };
@@ -165,6 +166,9 @@ struct Fc2Args {
   int32_t* status;
   int32_t H, I, E, k;
   int32_t nq;               // passes over H (H/128 divisible by nq)
+  int32_t kbs_per_stage;    // k-blocks per W2 ring stage: I/128 (a whole output tile) or 1 (selects the kernel)
+  int32_t* next;            // work counter (hdr + HDR_FC2_NEXT): CTAs take units from it when `dynamic`
+  int32_t dynamic;          // 1: units by the work counter; 0: the static stride blockIdx.x + i * gridDim.x
   int32_t max_tiles;
   int64_t max_rows;
   int64_t num_pairs;      // T * k of this call
