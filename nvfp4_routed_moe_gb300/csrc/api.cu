@@ -299,10 +299,11 @@ static int fc1_pair(const Shape& s, int64_t T) {
 
 static int forward_launches(int64_t P) { return (P <= kRouteSmallMax ? 1 : 2) + 4 + (P > kSfTwoPassMin ? 1 : 0); }
 
-// FC2's CTAs take their units from a work counter that routing seeds on every
-// call (NVFP4MOE_FC2_DYNAMIC=0: the static stride instead).
-static int fc2_dynamic() {
-  const char* v = std::getenv("NVFP4MOE_FC2_DYNAMIC");
+// The GEMMs' CTAs take their units from work counters that routing seeds on
+// every call (NVFP4MOE_FC1_DYNAMIC=0 / NVFP4MOE_FC2_DYNAMIC=0: the static
+// stride instead).
+static int gemm_dynamic(const char* env) {
+  const char* v = std::getenv(env);
   return (v && v[0] == '0') ? 0 : 1;
 }
 
@@ -571,6 +572,8 @@ static moe_status_t forward_impl(const moe_shape_t* shape, int32_t expert_begin,
   f1.E = s.E;
   f1.max_tiles = (int32_t)L.TTmax;
   f1.max_rows = L.PpadMax;
+  f1.next = ra.hdr + HDR_FC1_NEXT;
+  f1.dynamic = gemm_dynamic("NVFP4MOE_FC1_DYNAMIC");
   const int pair = fc1_pair(s, T);
   const int grid1 = (int)std::min<int64_t>(sms, tt * (s.I / 64 / pair));
   prof_mark(2, stream);
@@ -589,7 +592,7 @@ static moe_status_t forward_impl(const moe_shape_t* shape, int32_t expert_begin,
   f2.nq = nq;
   f2.kbs_per_stage = fc2_tile_stages(T) ? NKB2 : 1;
   f2.next = ra.hdr + HDR_FC2_NEXT;
-  f2.dynamic = fc2_dynamic();
+  f2.dynamic = gemm_dynamic("NVFP4MOE_FC2_DYNAMIC");
   f2.status = ra.hdr + HDR_STATUS;
   f2.H = s.H;
   f2.I = s.I;

@@ -301,7 +301,7 @@ __global__ void __launch_bounds__(kFc1Threads, 1)
   const int NIT = p.I / 64, NP = NIT / PAIR, NKB = p.H / kFc1KBlock;
   if (warp == kFc1Producer && lane == 0) tma_prefetch_desc(&tm_w13);
   // a stage is full once the producer's copies and every gather thread's rows have landed
-  gemm_setup<C::kStages, kFc1EpiWarps>(bars, warp, kFc1Mma, 1u + kFc1Gather);
+  gemm_setup<C::kStages, kFc1EpiWarps>(bars, warp, kFc1Mma, 1u + kFc1Gather, kFc1Producer + 1 + kFc1EpiWarps);
   const uint32_t tmem = bars->tmem_base;
   pdl_wait();
   pdl_launch_dependents();
@@ -331,17 +331,21 @@ __global__ void __launch_bounds__(kFc1Threads, 1)
     };
     uint32_t stage = 0, phase = 0;
     bool ok = true;
-    int4 nxt = next_tile(tiles, blockIdx.x, num_units, NP);
-    int4 nxt2 = next_tile(tiles, blockIdx.x + gridDim.x, num_units, NP);
+    int qj = 0;
+    int4 nxt;
+    int unit_nxt = uq_read(bars, 0, nxt, p.status);
     int f_nxt[16];
     pairs(nxt, f_nxt);
-    for (int unit = blockIdx.x; unit < num_units && ok; unit += gridDim.x) {
+    while (unit_nxt >= 0 && ok) {
       const int4 tl = nxt;
       int tok[16];
 #pragma unroll
       for (int i = 0; i < 16; ++i) tok[i] = (f_nxt[i] >= 0 && f_nxt[i] < p.num_pairs) ? f_nxt[i] / p.k : -1;
-      nxt = nxt2;
-      nxt2 = next_tile(tiles, unit + 2 * gridDim.x, num_units, NP);
+      unit_nxt = uq_read(bars, qj + 1, nxt, p.status);
+      __syncwarp();
+      if (lane == 0) uq_release(bars, qj);
+      ++qj;
+      if (unit_nxt == -2) break;
       pairs(nxt, f_nxt);                                      // in flight while this unit streams
       if (!tile_ok(tl, p.E, p.max_rows)) continue;
       for (int kb = 0; kb < NKB; ++kb) {
@@ -368,16 +372,47 @@ __global__ void __launch_bounds__(kFc1Threads, 1)
       uint32_t stage = 0, phase = 0;
       uint32_t armed = 0, last_phase = 0;  // bit s: stage s armed; its last armed phase
       bool ok = true;
-      int4 nxt = next_tile(tiles, blockIdx.x, num_units, NP);
-      for (int unit = blockIdx.x; unit < num_units && ok; unit += gridDim.x) {
-        const int4 tl = nxt;
-        nxt = next_tile(tiles, unit + gridDim.x, num_units, NP);   // in flight while this unit streams
+      // The CTA's units: taken from the work counter (seeded by routing on
+      // every call) or by the static stride, and published two units ahead
+      // of the one whose loads this thread issues (the gather warps look one
+      // unit ahead as they start a unit, about when this thread does).
+      int taken = 0;
+      auto take = [&]() -> int {
+        const int u = p.dynamic ? atomicAdd(p.next, 1) : (int)blockIdx.x + taken * (int)gridDim.x;
+        ++taken;
+        return (u >= 0 && u < num_units) ? u : -1;
+      };
+      int qj = 0;
+      int unit = take();
+      int4 tl0 = next_tile(tiles, unit < 0 ? num_units : unit, num_units, NP);
+      ok = uq_publish(bars, qj++, unit, tl0, p.status);
+      int unit1 = -1;
+      int4 tl1 = make_int4(-1, 0, 0, 0);
+      if (ok && unit >= 0) {
+        unit1 = take();
+        tl1 = next_tile(tiles, unit1 < 0 ? num_units : unit1, num_units, NP);
+        ok = uq_publish(bars, qj++, unit1, tl1, p.status);
+      }
+      while (ok && unit >= 0) {
+        int unit2 = -1;
+        int4 tl2 = make_int4(-1, 0, 0, 0);
+        if (unit1 >= 0) {
+          unit2 = take();
+          tl2 = next_tile(tiles, unit2 < 0 ? num_units : unit2, num_units, NP);
+          if (!uq_publish(bars, qj++, unit2, tl2, p.status)) break;
+        }
+        const int4 tl = tl0;
+        const int cur = unit;
+        unit = unit1;
+        tl0 = tl1;
+        unit1 = unit2;
+        tl1 = tl2;
         if (!tile_ok(tl, p.E, p.max_rows)) {
           set_status(p.status, DEVSTAT_BAD_TILE);
           continue;
         }
         const int e = tl.x, row0 = tl.y;
-        const int w0 = (e * NIT + PAIR * (unit % NP)) * NKB;   // first W13 tile; the next is NKB later
+        const int w0 = (e * NIT + PAIR * (cur % NP)) * NKB;   // first W13 tile; the next is NKB later
         const uint32_t tx = (uint32_t)PAIR * 16384u + (1u + PAIR) * 2048u;
         for (int kb = 0; kb < NKB; ++kb) {
           if (!wait_or_abort(&bars->empty[stage], phase ^ 1u, bars, p.status)) {
@@ -424,10 +459,14 @@ __global__ void __launch_bounds__(kFc1Threads, 1)
       const uint64_t sd0 = sf_desc(smem + C::kSX);   // X atom 0 of stage 0; W atoms follow at kSW
       uint32_t soff = 0;                              // (stage * kStage) >> 4
       uint32_t sfc = tmem + 256;                      // the stage's scale columns
-      int4 nxt = next_tile(tiles, blockIdx.x, num_units, NP);
-      for (int unit = blockIdx.x; unit < num_units && ok; unit += gridDim.x) {
+      int qj = 0;
+      int4 nxt;
+      int unit_nxt = uq_read(bars, 0, nxt, p.status);
+      while (unit_nxt >= 0 && ok) {
         const int4 tl = nxt;
-        nxt = next_tile(tiles, unit + gridDim.x, num_units, NP);
+        unit_nxt = uq_read(bars, qj + 1, nxt, p.status);
+        uq_release(bars, qj++);
+        if (unit_nxt == -2) break;
         if (!tile_ok(tl, p.E, p.max_rows)) continue;
         const uint32_t buf = (uint32_t)local % C::kBufs, par = (((uint32_t)local / C::kBufs) & 1u) ^ 1u;
         const uint32_t dcol = tmem + buf * PAIR * 128;
@@ -487,15 +526,20 @@ __global__ void __launch_bounds__(kFc1Threads, 1)
     const int I2 = p.I / 2, KC = p.I / 16;
     const int r = q * 32 + lane;                      // token row within the tile
     int local = 0;
-    int4 nxt = next_tile(tiles, blockIdx.x, num_units, NP);
+    int qj = 0;
+    int4 nxt;
+    int unit_nxt = uq_read(bars, 0, nxt, p.status);
     float4 sc_nxt = unit_scalars(p, nxt);
-    int4 nxt2 = next_tile(tiles, blockIdx.x + gridDim.x, num_units, NP);
-    for (int unit = blockIdx.x; unit < num_units; unit += gridDim.x) {
+    while (unit_nxt >= 0) {
+      const int unit = unit_nxt;
       const int4 tl = nxt;
       const float4 sc = sc_nxt;
-      nxt = nxt2;
+      unit_nxt = uq_read(bars, qj + 1, nxt, p.status);
+      __syncwarp();
+      if (lane == 0) uq_release(bars, qj);
+      ++qj;
+      if (unit_nxt == -2) break;
       sc_nxt = unit_scalars(p, nxt);                                  // one unit ahead
-      nxt2 = next_tile(tiles, unit + 2 * gridDim.x, num_units, NP);  // two units ahead
       if (!tile_ok(tl, p.E, p.max_rows)) continue;
       const int row0 = tl.y, rows = tl.z;
       const uint32_t buf = (uint32_t)local % C::kBufs;

@@ -35,6 +35,7 @@ enum : int {
   HDR_SKIP = 9,        // 1: routing found no valid preparation stamp and did nothing; later kernels skip too
   HDR_STREAM_BASE = 10,  // streamed chunk: first logical token (int64, words 10-11)
   HDR_FC2_NEXT = 12,   // FC2's work counter: next unit to take (seeded to 0 by routing on every call)
+  HDR_FC1_NEXT = 13,   // FC1's work counter, likewise
   HDR_STAMP = 16,      // preparation stamp, kStampWords words: magic, H, I, E, k, token capacity
   HDR_WORDS = 64,
 };
@@ -152,6 +153,8 @@ struct Fc1Args {
   int32_t max_tiles;      // capacity of the tile list
   int64_t max_rows;       // padded rows of the workspace
   int64_t num_pairs;      // T * k of this call
+  int32_t* next;          // work counter (hdr + HDR_FC1_NEXT): CTAs take units from it when `dynamic`
+  int32_t dynamic;        // 1: units by the work counter; 0: the static stride blockIdx.x + i * gridDim.x
 };
 
 struct Fc2Args {

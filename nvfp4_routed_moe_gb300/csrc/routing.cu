@@ -210,7 +210,8 @@ __device__ void scan_experts(const RouteArgs& a, const int* cnt_s, int* s_offs, 
     a.hdr[HDR_NVALID] = o0;
     a.hdr[HDR_PPAD] = o1;
     a.hdr[HDR_NUM_TT] = o2;
-    a.hdr[HDR_FC2_NEXT] = 0;   // FC2's work counter starts over on every call
+    a.hdr[HDR_FC2_NEXT] = 0;   // the GEMMs' work counters start over on every call
+    a.hdr[HDR_FC1_NEXT] = 0;
     int m = 0;
     for (int w = 0; w < NWARP; ++w) m = max(m, s_tmp[208 + w]);
     a.hdr[HDR_MAXROWS] = m;
@@ -238,6 +239,7 @@ __device__ __forceinline__ void mark_not_prepared(const RouteArgs& a) {
   a.hdr[HDR_NVALID] = 0;
   a.hdr[HDR_MAXROWS] = 0;
   a.hdr[HDR_FC2_NEXT] = 0;
+  a.hdr[HDR_FC1_NEXT] = 0;
   a.hdr[HDR_SKIP] = 1;
   atomicOr(a.hdr + HDR_STATUS, DEVSTAT_NOT_PREPARED);
 }
