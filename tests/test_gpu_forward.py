@@ -631,3 +631,27 @@ def test_full_shape_scheduling_options(full_model, env, monkeypatch):
         sample = _tile_boundary_tokens(np.where(ids < 32, ids, 10 ** 6).astype(np.int32), 32)[:200]
         assert_close(out_bits(out)[sample], cases.run_oracle(inp, tokens=sample), f"T={T} {env}")
         assert_close(out_bits(out), out_bits(ref_out), f"T={T} {env} against the default")
+
+
+def test_full_shape_zero_and_subnormal_weight_block_scales(full_model):
+    """Full-shape decode (T = 16, every token) with a fifth of the W13 and W2
+    block scales replaced by the zero scale (0x00) and E4M3 subnormals
+    (0x01-0x07): zero blocks must contribute nothing and subnormal ones
+    their exact 2^-9 multiples, in FC1 and FC2 alike."""
+    minp, _ = full_model
+    T = 16
+    inp = _full_case(minp, T, "uniform", seed=500)
+    rs = np.random.default_rng(500)
+    used = np.unique(inp.expert_ids)
+    sf13, sf2 = inp.sf13.copy(), inp.sf2.copy()
+    for sf in (sf13, sf2):
+        sub = sf[used]
+        mask = rs.random(sub.shape) < 0.2
+        sub[mask] = rs.integers(0, 8, size=int(mask.sum()), dtype=np.uint8)
+        sf[used] = sub
+    inp.sf13, inp.sf2 = sf13, sf2
+    m = Model(inp)
+    out, ws = m.forward_inputs(inp)
+    torch.cuda.synchronize()
+    assert api.moe_read_status(ws) == (0, 0)
+    assert_close(out_bits(out), cases.run_oracle(inp), "zero and subnormal weight scales")
