@@ -80,13 +80,16 @@ moe_status_t moe_test_mma_fp4(const uint8_t* a, const uint8_t* sfa_atoms, const 
  * xq holds the packed X codes once per token ([tokens, H/2]; FC1 gathers them
  * per tile row), aq the packed A codes of the padded expanded rows
  * ([rows, I/2]); sfx/sfa are the block scales of the padded expanded rows
- * (X and A) in the 128x4 atom layout; row_pos maps a
+ * (X and A) in the 128x4 atom layout; sft holds X's block scales once per
+ * token ([tokens, H/16]) where a forward writes them token-major (above 4096
+ * routed pairs, before the atom pass; and at the batch sizes where FC1 runs
+ * on the CUDA cores, which read them there and leave sfx unwritten); row_pos maps a
  * flat pair t*k+j to its padded row; acc [tokens, H] fp32 is the FC2
  * combine accumulator (route-weighted sums before the BF16 rounding). */
 typedef struct {
   int64_t max_tokens, pairs_max, padded_rows_max, tiles_max;
   int64_t header, count, cumsum, offs, poffs, sorted_row, gather, row_pos, prow_pair, tt_list;
-  int64_t xq, sfx, aq, sfa, acc, total;
+  int64_t xq, sfx, sft, aq, sfa, acc, total;
 } moe_ws_layout_t;
 
 moe_status_t moe_workspace_layout(const moe_shape_t* shape, size_t ws_bytes, moe_ws_layout_t* layout);

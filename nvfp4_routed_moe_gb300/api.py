@@ -55,7 +55,7 @@ class moe_routing_opts_t(ctypes.Structure):
 class moe_ws_layout_t(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int64) for n in
                 ("max_tokens", "pairs_max", "padded_rows_max", "tiles_max", "header", "count", "cumsum", "offs",
-                 "poffs", "sorted_row", "gather", "row_pos", "prow_pair", "tt_list", "xq", "sfx", "aq", "sfa",
+                 "poffs", "sorted_row", "gather", "row_pos", "prow_pair", "tt_list", "xq", "sfx", "sft", "aq", "sfa",
                  "acc", "total")]
 
 

@@ -20,7 +20,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIBDIR = os.path.join(HERE, "lib")
 LIB = os.path.join(LIBDIR, "libnvfp4moe.so")
-SOURCES = ["api.cu", "routing.cu", "quant.cu", "gemm.cu", "static_scratch.cu", "stream.cu"]
+SOURCES = ["api.cu", "routing.cu", "quant.cu", "gemm.cu", "gemv.cu", "static_scratch.cu", "stream.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

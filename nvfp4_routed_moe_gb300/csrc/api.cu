@@ -39,6 +39,9 @@ cudaError_t gemm_set_attributes();
 cudaError_t launch_fc1(const CUtensorMap& w13, const Fc1Args& a, int pair, int grid,
                        cudaStream_t st);
 cudaError_t launch_fc2(const CUtensorMap& w2, const RowMaps& aq, const Fc2Args& a, int grid, cudaStream_t st);
+cudaError_t gemv_set_attributes();
+size_t fc1_gemv_smem(int H);
+cudaError_t launch_fc1_gemv(const CUtensorMap& w13, const Fc1Args& a, int grid, cudaStream_t st);
 cudaError_t launch_mma_check(const CUtensorMap& a, const CUtensorMap& b, const uint8_t* sfa, const uint8_t* sfb,
                              int N, int K, float* d, int32_t* status, cudaStream_t st);
 cudaError_t launch_mma_peak(int grid, int n, int mmas, int copies, int accs, long long* cycles, int32_t* status,
@@ -113,6 +116,8 @@ static cudaError_t device_ready(int* sms) {
     err = routing_set_attributes(kMaxExperts);
     if (err != cudaSuccess) return err;
     err = gemm_set_attributes();
+    if (err != cudaSuccess) return err;
+    err = gemv_set_attributes();
     if (err != cudaSuccess) return err;
     d.attrs = true;
   }
@@ -297,7 +302,26 @@ static int fc1_pair(const Shape& s, int64_t T) {
   return T <= kFc1SingleMaxTokens ? 1 : 2;
 }
 
-static int forward_launches(int64_t P) { return (P <= kRouteSmallMax ? 1 : 2) + 4 + (P > kSfTwoPassMin ? 1 : 0); }
+// Largest batch for which FC1 runs on the CUDA cores (weights streamed at
+// HBM rate, a few tokens per expert tile); NVFP4MOE_FC1_GEMV=0/1 overrides.
+constexpr int64_t kFc1GemvMaxTokens = 32;
+
+static bool fc1_gemv(const Shape& s, int64_t T) {
+  if (fc1_gemv_smem(s.H) > kSmemOptin) return false;   // the X slots for this H do not fit
+  if (const char* v = std::getenv("NVFP4MOE_FC1_GEMV")) {
+    if (v[0] == '0') return false;
+    if (v[0] == '1') return true;
+  }
+  return T <= kFc1GemvMaxTokens;
+}
+
+// Above kSfTwoPassMin pairs the X scales take the token-major + atom pass
+// route, unless FC1 runs on the CUDA cores (which reads them token-major).
+static bool sf_atom_pass(const Shape& s, int64_t T) { return T * s.k > kSfTwoPassMin && !fc1_gemv(s, T); }
+
+static int forward_launches(const Shape& s, int64_t T) {
+  return (T * s.k <= kRouteSmallMax ? 1 : 2) + 4 + (sf_atom_pass(s, T) ? 1 : 0);
+}
 
 // The GEMMs' CTAs take their units from work counters that routing seeds on
 // every call (NVFP4MOE_FC1_DYNAMIC=0 / NVFP4MOE_FC2_DYNAMIC=0: the static
@@ -525,15 +549,16 @@ static moe_status_t forward_impl(const moe_shape_t* shape, int32_t expert_begin,
   qa.acc = reinterpret_cast<float*>(w + L.acc);
   qa.qX = qX;
   qa.xq = w + L.xq;
-  qa.sfx = w + L.sfx;
-  qa.sft = P > kSfTwoPassMin ? w + L.sft : nullptr;
+  const bool gemv = fc1_gemv(s, T);
+  qa.sfx = gemv ? nullptr : w + L.sfx;
+  qa.sft = (gemv || sf_atom_pass(s, T)) ? w + L.sft : nullptr;
   qa.T = T;
   qa.H = s.H;
   qa.k = s.k;
   qa.max_rows = L.PpadMax;
   prof_mark(1, stream);
   MOE_CUDA(launch_quant_x(qa, stream));
-  if (qa.sft) {
+  if (qa.sft && qa.sfx) {
     SfAtomArgs sa{};
     sa.sft = qa.sft;
     sa.prow_pair = ra.prow_pair;
@@ -552,8 +577,10 @@ static moe_status_t forward_impl(const moe_shape_t* shape, int32_t expert_begin,
   // 3. FC1 + SiTU + requant
   const int64_t tt = tt_bound(P, s.E);
   Fc1Args f1{};
+  f1.w13p = static_cast<const uint8_t*>(w13);
   f1.sf13p = sf13;
   f1.xq = w + L.xq;
+  f1.sft = w + L.sft;
   f1.prow_pair = ra.prow_pair;
   f1.k = s.k;
   f1.num_pairs = P;
@@ -574,10 +601,14 @@ static moe_status_t forward_impl(const moe_shape_t* shape, int32_t expert_begin,
   f1.max_rows = L.PpadMax;
   f1.next = ra.hdr + HDR_FC1_NEXT;
   f1.dynamic = gemm_dynamic("NVFP4MOE_FC1_DYNAMIC");
-  const int pair = fc1_pair(s, T);
-  const int grid1 = (int)std::min<int64_t>(sms, tt * (s.I / 64 / pair));
   prof_mark(2, stream);
-  MOE_CUDA(launch_fc1(tm_w13, f1, pair, grid1, stream));
+  if (gemv) {
+    MOE_CUDA(launch_fc1_gemv(tm_w13, f1, (int)std::min<int64_t>(sms, tt * (s.I / 64)), stream));
+  } else {
+    const int pair = fc1_pair(s, T);
+    const int grid1 = (int)std::min<int64_t>(sms, tt * (s.I / 64 / pair));
+    MOE_CUDA(launch_fc1(tm_w13, f1, pair, grid1, stream));
+  }
 
   // 4. FC2 with the route-weighted combine into the fp32 accumulator
   Fc2Args f2{};
@@ -995,6 +1026,7 @@ moe_status_t moe_workspace_layout(const moe_shape_t* shape, size_t ws_bytes, moe
   out->tt_list = (int64_t)L.tt_list;
   out->xq = (int64_t)L.xq;
   out->sfx = (int64_t)L.sfx;
+  out->sft = (int64_t)L.sft;
   out->aq = (int64_t)L.aq;
   out->sfa = (int64_t)L.sfa;
   out->acc = (int64_t)L.acc;
@@ -1043,7 +1075,7 @@ moe_status_t moe_forward_launch_count(const moe_shape_t* shape, int64_t num_toke
   moe_status_t st = shape_supported(shape);
   if (st != MOE_OK) return st;
   if (!launches || num_tokens < 1) return MOE_ERR_INVALID_ARG;
-  *launches = forward_launches(num_tokens * shape->top_k);
+  *launches = forward_launches(to_shape(shape), num_tokens);
   return MOE_OK;
 }
 

@@ -19,6 +19,7 @@ constexpr int kRouteChunk = 4096;     // largest number of pairs per CTA of the 
 constexpr int kRouteChunkMin = 512;   // smallest (more CTAs for mid-size batches)
 constexpr int kMaxExperts = 1024;
 constexpr int kMaxTopK = 32;
+constexpr size_t kSmemOptin = 232448;  // dynamic shared memory a CTA may opt into on sm_103 (227 KB)
 constexpr size_t kAccPassBytes = 64u << 20;  // default L2 budget of one combine pass over H
 
 // Workspace header words (int32).
@@ -136,8 +137,10 @@ struct RouteArgs {
 };
 
 struct Fc1Args {
+  const uint8_t* w13p;      // prepared W13 codes (the CUDA-core kernel's bulk copies; the MMA kernel uses a tensor map)
   const uint8_t* sf13p;
   const uint8_t* xq;        // [T, H/2] token-major X codes, gathered per tile row
+  const uint8_t* sft;       // [T, H/16] token-major X block scales (CUDA-core kernel)
   const int32_t* prow_pair; // [Ppad] flat pair of each padded row (-1: padding)
   const uint8_t* sfx;
   const int32_t* tt_list;
@@ -231,11 +234,12 @@ struct QuantXArgs {
   const uint16_t* x;        // [T, H] bf16
   const int32_t* row_pos;   // [T*k] padded expanded row of each pair, -1 if not routed
   const uint16_t* route_w;  // [T*k] bf16 route weights
-  float* wrow;              // [Ppad] out: route weight of each padded row (fp32), when sft is null
+  float* wrow;              // [Ppad] out: route weight of each padded row (fp32), unless the atom pass runs
   float* acc;               // [T, H] out: zeroed
   const float* qX;          // [1]
   uint8_t* xq;              // [T, H/2] token-major codes
-  uint8_t* sfx;             // atom layout, H/16 chunks per row (written here when sft is null)
+  uint8_t* sfx;             // atom layout, H/16 chunks per row: written here when sft is null, by the atom
+                            // pass when both are set; null: no atoms (FC1 on the CUDA cores reads sft)
   uint8_t* sft;             // [T, H/16] token-major block scales, or null
   int64_t T;
   int32_t H, k;

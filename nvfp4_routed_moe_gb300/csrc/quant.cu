@@ -25,7 +25,9 @@ cudaError_t launch_with_pdl(const void* fn, dim3 grid, dim3 block, size_t smem, 
 // the atom layout of every routed row (up to 4096 routed pairs), or, above that,
 // once per token into token-major rows that sf_atoms_kernel then lays out
 // with whole-atom writes (a token's scales land in 56 different atoms, and
-// scattered 4-byte writes cost more than the extra pass).
+// scattered 4-byte writes cost more than the extra pass).  When FC1 runs on
+// the CUDA cores (decode batches) it reads the token-major scales itself:
+// then no atoms are written and this kernel stores the route weights.
 __global__ void __launch_bounds__(256) quant_x_kernel(const QuantXArgs a) {
   // Warp w takes 32 groups (512 elements) of token w / S, S = ceil(H/512)
   // slices per token, so a token's slices run in parallel warps.
@@ -41,8 +43,9 @@ __global__ void __launch_bounds__(256) quant_x_kernel(const QuantXArgs a) {
   // the row-position work below waits.  With token-major scales the route
   // weights are placed by the scale-atom kernel, and one thread waits so
   // that this kernel still completes after routing.
+  const bool atom_pass = a.sft && a.sfx;   // token-major scales, laid out by sf_atoms_kernel
   pdl_launch_dependents();
-  if (a.sft && blockIdx.x == 0 && threadIdx.x == 0) pdl_wait();
+  if (atom_pass && blockIdx.x == 0 && threadIdx.x == 0) pdl_wait();
   if (t >= a.T) return;
   const float q = __ldg(a.qX);
   // this slice's share of the token's accumulator row
@@ -72,10 +75,11 @@ __global__ void __launch_bounds__(256) quant_x_kernel(const QuantXArgs a) {
   word |= __shfl_xor_sync(0xffffffffu, word, 2);
   if (a.sft && valid && (lane & 3) == 0) *reinterpret_cast<uint32_t*>(a.sft + t * G + g) = word;
   if (valid) *reinterpret_cast<uint2*>(a.xq + (size_t)t * (H / 2) + g * 8) = packed;
-  if (a.sft) return;
+  if (atom_pass) return;
   pdl_wait();   // routing's row positions
   const int rp = (lane < a.k) ? a.row_pos[t * a.k + lane] : -1;
   if (sl == 0 && rp >= 0 && rp < a.max_rows) a.wrow[rp] = bf16_bits_to_f32(a.route_w[t * a.k + lane]);
+  if (!a.sfx) return;
   for (int j = 0; j < a.k; ++j) {
     const int row = __shfl_sync(0xffffffffu, rp, j);
     if (row < 0 || row >= a.max_rows || !valid) continue;

@@ -70,7 +70,7 @@ def test_layout_regions_fit_and_are_aligned(L):
     lay = api.moe_workspace_layout(full, n)
     assert lay.max_tokens >= 4096 and lay.total <= n
     offs = [lay.header, lay.count, lay.cumsum, lay.offs, lay.poffs, lay.sorted_row, lay.gather, lay.row_pos,
-            lay.prow_pair, lay.tt_list, lay.xq, lay.sfx, lay.aq, lay.sfa, lay.acc]
+            lay.prow_pair, lay.tt_list, lay.xq, lay.sfx, lay.sft, lay.aq, lay.sfa, lay.acc]
     assert offs == sorted(offs) and all(o % 1024 == 0 for o in offs)
     assert lay.padded_rows_max % 128 == 0
     assert lay.padded_rows_max >= 4096 * 16 + 127 * 896
