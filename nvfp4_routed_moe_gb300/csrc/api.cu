@@ -42,6 +42,8 @@ cudaError_t launch_fc2(const CUtensorMap& w2, const RowMaps& aq, const Fc2Args& 
 cudaError_t gemv_set_attributes();
 size_t fc1_gemv_smem(int H);
 cudaError_t launch_fc1_gemv(const CUtensorMap& w13, const Fc1Args& a, int grid, cudaStream_t st);
+size_t fc2_gemv_smem(int I);
+cudaError_t launch_fc2_gemv(const Fc2Args& a, int grid, cudaStream_t st);
 cudaError_t launch_mma_check(const CUtensorMap& a, const CUtensorMap& b, const uint8_t* sfa, const uint8_t* sfb,
                              int N, int K, float* d, int32_t* status, cudaStream_t st);
 cudaError_t launch_mma_peak(int grid, int n, int mmas, int copies, int accs, long long* cycles, int32_t* status,
@@ -302,9 +304,9 @@ static int fc1_pair(const Shape& s, int64_t T) {
   return T <= kFc1SingleMaxTokens ? 1 : 2;
 }
 
-// Largest batch for which FC1 runs on the CUDA cores (weights streamed at
+// Largest batch for which FC1 runs on the decode kernel (weights streamed at
 // HBM rate, a few tokens per expert tile); NVFP4MOE_FC1_GEMV=0/1 overrides.
-constexpr int64_t kFc1GemvMaxTokens = 32;
+constexpr int64_t kFc1GemvMaxTokens = 16;
 
 static bool fc1_gemv(const Shape& s, int64_t T) {
   if (fc1_gemv_smem(s.H) > kSmemOptin) return false;   // the X slots for this H do not fit
@@ -315,8 +317,33 @@ static bool fc1_gemv(const Shape& s, int64_t T) {
   return T <= kFc1GemvMaxTokens;
 }
 
+// Largest batch for which FC2 runs the same way; NVFP4MOE_FC2_GEMV=0/1 overrides.
+constexpr int64_t kFc2GemvMaxTokens = 16;
+
+static bool fc2_gemv(const Shape& s, int64_t T) {
+  if (fc2_gemv_smem(s.I) > kSmemOptin) return false;
+  if (const char* v = std::getenv("NVFP4MOE_FC2_GEMV")) {
+    if (v[0] == '0') return false;
+    if (v[0] == '1') return true;
+  }
+  return T <= kFc2GemvMaxTokens;
+}
+
+// Output tiles per unit of the decode FC2: about three units per SM for the
+// batch's tile bound, between 2 and half of H (each job's A rows take a few
+// microseconds to arrive, so long units stream best; measured at T = 1..16:
+// 2, 4, 7-8 and 14 tiles).  NVFP4MOE_FC2_GROUP overrides.
+static int fc2_gemv_group(const Shape& s, int64_t tiles, int sms) {
+  if (const char* v = std::getenv("NVFP4MOE_FC2_GROUP")) {
+    const int g = std::atoi(v);
+    if (g >= 1) return g;
+  }
+  const int64_t nmt = s.H / 128, g = (tiles * nmt + 3 * (int64_t)sms - 1) / (3 * (int64_t)sms);
+  return (int)std::max<int64_t>(1, std::min<int64_t>(std::max<int64_t>(1, nmt / 2), std::max<int64_t>(2, g)));
+}
+
 // Above kSfTwoPassMin pairs the X scales take the token-major + atom pass
-// route, unless FC1 runs on the CUDA cores (which reads them token-major).
+// route, unless FC1 runs on the decode kernel (which reads them token-major).
 static bool sf_atom_pass(const Shape& s, int64_t T) { return T * s.k > kSfTwoPassMin && !fc1_gemv(s, T); }
 
 static int forward_launches(const Shape& s, int64_t T) {
@@ -612,7 +639,9 @@ static moe_status_t forward_impl(const moe_shape_t* shape, int32_t expert_begin,
 
   // 4. FC2 with the route-weighted combine into the fp32 accumulator
   Fc2Args f2{};
+  f2.w2p = w2;
   f2.sf2p = sf2;
+  f2.aq = w + L.aq;
   f2.sfa = w + L.sfa;
   f2.tt_list = ra.tt_list;
   f2.hdr = ra.hdr;
@@ -632,9 +661,14 @@ static moe_status_t forward_impl(const moe_shape_t* shape, int32_t expert_begin,
   f2.max_tiles = (int32_t)L.TTmax;
   f2.max_rows = L.PpadMax;
   f2.num_pairs = P;
-  const int grid2 = (int)std::min<int64_t>(sms, tt * NMT);
   prof_mark(3, stream);
-  MOE_CUDA(launch_fc2(tm_w2, tm_aq, f2, grid2, stream));
+  if (fc2_gemv(s, T)) {
+    f2.group = fc2_gemv_group(s, tt, sms);
+    const int64_t units = tt * ((NMT + f2.group - 1) / f2.group);
+    MOE_CUDA(launch_fc2_gemv(f2, (int)std::min<int64_t>(sms, units), stream));
+  } else {
+    MOE_CUDA(launch_fc2(tm_w2, tm_aq, f2, (int)std::min<int64_t>(sms, tt * NMT), stream));
+  }
 
   // 5. BF16 finalize
   prof_mark(4, stream);

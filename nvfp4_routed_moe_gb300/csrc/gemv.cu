@@ -1,4 +1,4 @@
-// gemv.cu -- FC1 at decode batch sizes: weights streamed at HBM rate, the
+// gemv.cu -- FC1 and FC2 at decode batch sizes: weights streamed at HBM rate, the
 // products on warp-level MMAs.
 //
 // ("Cake SiTU backend": FC1 over gate and up, SiTU, intermediate NVFP4
@@ -503,11 +503,392 @@ __global__ void __launch_bounds__(kGvThreads, 1)
   }
 }
 
+// ============================================================ FC2 (decode)
+// ("Cake SiTU backend": FC2, BF16 weighted finalization.)  The same scheme
+// for FC2: a unit is one token tile and a group of `group` consecutive
+// 128-feature output tiles of its expert; a job is a unit and up to kGvTok
+// of the tile's pairs.  Each ring stage holds one whole output tile (I/128
+// k-blocks of 128 rows x 64 B, plain bulk copies, + its I/64 scale atoms).
+// The sixteen consumer warps take alternate output tiles of the whole
+// sequence of jobs (warps 0-7 the even ring positions, 8-15 the odd ones),
+// warp w%8 the rows 16(w%8)..16(w%8)+15.  A converter warp turns each
+// job's A rows (codes by bulk copy, block scales from their atoms by 4-byte
+// cp.async) into pre-scaled f16 pairs in one of two A16 slots, one 20-word
+// segment per (k-block, t), so the consumers never wait for one another
+// between jobs.  Each output tile's sums are scaled by dA*dW2[e] and the
+// pair's route weight and added into the token's fp32 accumulator row (L2
+// reductions), as the tcgen05 FC2 does.
+constexpr int kG2Stages = 6;
+constexpr int kG2Seg = 20;                        // words per (k-block, t) segment of A16: 16 + 4 of padding
+
+constexpr int kG2Threads = (kGvWarps + 2) * 32;  // consumers, the producer warp, the converter warp
+
+struct G2Bars {
+  uint64_t full[kG2Stages], empty[kG2Stages];
+  uint64_t xfull[2], xempty[2];     // raw A slots (producer -> converter)
+  uint64_t aready[2], afree[2];     // A16 slots (converter -> consumers)
+  int4 job[2][3];                   // raw slot: {unit, expert, first padded row, m | mask << 8 | first output tile
+                                    // << 16}, the pairs' tokens, their route weights (fp32 bits)
+  int4 meta[2][4];                  // A16 slot: the same three, then {ring position of its first tile, 0, 0, 0}
+  int32_t abort_flag;
+};
+
+__host__ __device__ inline int a16_pair_words(int I) {
+  const int w = (I / 128) * 4 * kG2Seg;
+  return w + ((16 - w % 32) + 32) % 32;
+}
+__host__ __device__ inline int g2_stage_bytes(int I) { return (I / 128) * 8192 + (I / 64) * 512; }
+
+// Shared memory: ring | raw A codes [2][kGvTok][I/2] | raw A scales
+// [2][kGvTok][I/16] | A16 [2][kGvTok][pair words] | barriers; + 1 KB of alignment.
+static size_t g2_smem_bytes(int I) {
+  return (size_t)kG2Stages * g2_stage_bytes(I) + (size_t)2 * kGvTok * (I / 2) + (size_t)2 * kGvTok * (I / 16) +
+         (size_t)2 * kGvTok * a16_pair_words(I) * 4 + sizeof(G2Bars) + 1024;
+}
+
+__device__ __forceinline__ bool g2_wait(uint64_t* bar, uint32_t parity, G2Bars* bars, int32_t* status) {
+  if (mbar_try_wait(bar, parity)) return true;
+  if (lds_volatile_s32(&bars->abort_flag)) return false;
+  if (mbar_wait(bar, parity, status)) return true;
+  asm volatile("st.volatile.shared.s32 [%0], 1;" ::"r"(smem_u32(&bars->abort_flag)) : "memory");
+  return false;
+}
+
+__device__ __forceinline__ uint32_t lds16(uint32_t a) {
+  uint16_t v;
+  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(a));
+  return v;
+}
+
+// The job's pairs from the raw slot into A16 (by one warp): byte 16t+e of
+// k-block kb at word (kb*4 + t)*kG2Seg + e of the pair's A16.
+__device__ __forceinline__ void g2_fill_a16(uint32_t as, uint32_t asc, uint32_t a16, int m, int I, int lane) {
+  const int I2 = I / 2, I16 = I / 16, I8 = I / 8, PW = a16_pair_words(I);
+  for (int wi = lane; wi < m * I8; wi += 32) {
+    const int j = wi / I8, ww = wi - j * I8;
+    const uint32_t codes = lds32(as + j * I2 + 4 * ww);
+    const uint32_t s2 = h2_lo2(e4m3x2_to_h2(lds8(asc + j * I16 + (ww >> 1))));
+    uint32_t h[4];
+    e2m1x8_to_h2(codes, h);
+    const int seg = (ww >> 4) * 4 + ((ww & 15) >> 2);
+    sts128(a16 + 4 * (j * PW + seg * kG2Seg + 4 * (ww & 3)), hmul2(h[0], s2), hmul2(h[1], s2), hmul2(h[2], s2),
+           hmul2(h[3], s2));
+  }
+}
+
+// One output tile for thread (g, t): rows R0, R0 + 8, all I/128 k-blocks
+// (thread t's 16 bytes of each 64-byte k-block row); a16 is the thread's A16
+// segment of k-block 0.
+__device__ __forceinline__ void g2_tile(uint32_t st, uint32_t a16, int R0, int t, int NKB2, float (&sum)[4]) {
+  const int R1 = R0 + 8;
+  float cc[4][4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) cc[j][i] = 0.0f;
+  const uint32_t sfb = st + NKB2 * 8192;
+  for (int kb = 0; kb < NKB2; ++kb) {
+    const uint4 a = lds128(st + kb * 8192 + R0 * 64 + 16 * t), b = lds128(st + kb * 8192 + R1 * 64 + 16 * t);
+    // block scales of chunks 8kb+2t, 8kb+2t+1: atom 2kb + t/2, bytes 2(t%2), 2(t%2)+1 of row R
+    const uint32_t at = sfb + (2 * kb + (t >> 1)) * 512 + 2 * (t & 1);
+    const uint32_t sa = e4m3x2_to_h2(lds16(at + (R0 & 31) * 16 + (R0 >> 5) * 4));
+    const uint32_t sb = e4m3x2_to_h2(lds16(at + (R1 & 31) * 16 + (R1 >> 5) * 4));
+    const uint32_t SA[2] = {h2_lo2(sa), h2_hi2(sa)}, SB[2] = {h2_lo2(sb), h2_hi2(sb)};
+    uint32_t xw[16];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint4 v = lds128(a16 + 4 * kb * 4 * kG2Seg + 16 * j);
+      xw[4 * j] = v.x;
+      xw[4 * j + 1] = v.y;
+      xw[4 * j + 2] = v.z;
+      xw[4 * j + 3] = v.w;
+    }
+    const uint32_t wa[4] = {a.x, a.y, a.z, a.w}, wb[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      uint32_t ha[4], hb[4];
+      e2m1x8_to_h2(wa[q], ha);
+      e2m1x8_to_h2(wb[q], hb);
+      const uint32_t sA = SA[q >> 1], sB = SB[q >> 1];
+      mma16816(cc[(2 * q) & 3], hmul2(ha[0], sA), hmul2(hb[0], sB), hmul2(ha[1], sA), hmul2(hb[1], sB), xw[4 * q],
+               xw[4 * q + 1]);
+      mma16816(cc[(2 * q + 1) & 3], hmul2(ha[2], sA), hmul2(hb[2], sB), hmul2(ha[3], sA), hmul2(hb[3], sB),
+               xw[4 * q + 2], xw[4 * q + 3]);
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) sum[i] = (cc[0][i] + cc[1][i]) + (cc[2][i] + cc[3][i]);
+}
+
+// 4-byte asynchronous global->shared copy (completion counted by
+// cp.async.mbarrier.arrive).
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
+}
+
+__global__ void __launch_bounds__(kG2Threads, 1) fc2_gemv_kernel(const Fc2Args p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int I2 = p.I / 2, I16 = p.I / 16, NKB2 = p.I / 128, NMT = p.H / 128, SB = g2_stage_bytes(p.I);
+  const int G = max(1, min(p.group, NMT)), NG = (NMT + G - 1) / G;
+  uint8_t* acodes = ring + kG2Stages * SB;
+  uint8_t* ascales = acodes + 2 * kGvTok * I2;
+  uint8_t* a16 = ascales + 2 * kGvTok * I16;
+  const int PW = a16_pair_words(p.I);
+  G2Bars* bars = reinterpret_cast<G2Bars*>(a16 + (size_t)2 * kGvTok * PW * 4);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kG2Stages; ++s) {
+      mbar_init(&bars->full[s], 1);
+      mbar_init(&bars->empty[s], kGvWarps / 2);   // the warps of the output tile's parity
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&bars->xfull[b], 2);   // the producer's arrival (bulk copies) and its block-scale cp.asyncs'
+      mbar_init(&bars->xempty[b], 1);
+      mbar_init(&bars->aready[b], 1);
+      mbar_init(&bars->afree[b], kGvWarps);
+    }
+    bars->abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  pdl_wait();   // FC1's A and everything before it
+  pdl_launch_dependents();
+  const int num_units = min(max(p.hdr[HDR_NUM_TT], 0), p.max_tiles) * NG;   // (token tile, group of output tiles)
+  const int4* tiles = reinterpret_cast<const int4*>(p.tt_list);
+
+  if (warp == kGvWarps) {
+    if (lane == 0) {
+      // ---------------------------------------------------------- producer
+      uint32_t stage = 0, phase = 0, xb = 0, xph = 0;
+      uint32_t armed = 0, last_phase = 0;
+      uint32_t xarmed = 0, xlast = 0;
+      bool ok = true;
+      int taken = 0;
+      auto take = [&]() -> int {
+        const int u = p.dynamic ? atomicAdd(p.next, 1) : (int)blockIdx.x + taken * (int)gridDim.x;
+        ++taken;
+        return (u >= 0 && u < num_units) ? u : -1;
+      };
+      auto pairs = [&](const int4& t, int r0, int (&f)[kGvTok], float (&w)[kGvTok]) {
+        const bool okt = gv_tile_ok(t, p.E, p.max_rows);
+#pragma unroll
+        for (int j = 0; j < kGvTok; ++j) {
+          const bool in = okt && r0 + j < t.z;
+          f[j] = in ? __ldg(p.prow_pair + t.y + r0 + j) : -1;
+          w[j] = in ? __ldg(p.wrow + t.y + r0 + j) : 0.0f;
+        }
+      };
+      // As in FC1: three units in flight (u0 streamed, u1's tile and its first
+      // job's pairs and route weights, u2 taken).
+      int u0 = take();
+      int4 t0 = gv_tile(tiles, u0, NG);
+      int f0[kGvTok];
+      float w0[kGvTok];
+      pairs(t0, 0, f0, w0);
+      int u1 = u0 >= 0 ? take() : -1;
+      int4 t1 = gv_tile(tiles, u1, NG);
+      int u2 = u1 >= 0 ? take() : -1;
+      while (ok && u0 >= 0) {
+        int f1[kGvTok];
+        float w1[kGvTok];
+        pairs(t1, 0, f1, w1);
+        const int4 t2 = gv_tile(tiles, u2, NG);
+        const int u3 = u2 >= 0 ? take() : -1;
+        if (!gv_tile_ok(t0, p.E, p.max_rows)) {
+          set_status(p.status, DEVSTAT_BAD_TILE);
+        } else {
+          const int e = t0.x, mt0 = (u0 % NG) * G, cnt = min(G, NMT - mt0);
+          for (int r0 = 0; r0 < t0.z && ok; r0 += kGvTok) {
+            int f[kGvTok];
+            float w[kGvTok];
+            if (r0 == 0) {
+#pragma unroll
+              for (int j = 0; j < kGvTok; ++j) {
+                f[j] = f0[j];
+                w[j] = w0[j];
+              }
+            } else {
+              pairs(t0, r0, f, w);
+            }
+            const int m = min(kGvTok, t0.z - r0);
+            int tok[kGvTok];
+            uint32_t mask = 0;
+#pragma unroll
+            for (int j = 0; j < kGvTok; ++j) {
+              tok[j] = (j < m && f[j] >= 0 && f[j] < p.num_pairs) ? f[j] / p.k : -1;
+              if (tok[j] >= 0) mask |= 1u << j;
+            }
+            if (!g2_wait(&bars->xempty[xb], xph ^ 1u, bars, p.status)) {
+              ok = false;
+              break;
+            }
+            job_store(&bars->job[xb][0], make_int4(u0, e, t0.y + r0, m | (int)(mask << 8) | (mt0 << 16)));
+            job_store(&bars->job[xb][1], make_int4(tok[0], tok[1], tok[2], tok[3]));
+            job_store(&bars->job[xb][2], make_int4(__float_as_int(w[0]), __float_as_int(w[1]), __float_as_int(w[2]),
+                                                   __float_as_int(w[3])));
+            // the pairs' block-scale words (4 chunks each) from their atoms
+            const uint32_t asc = smem_u32(ascales + xb * kGvTok * I16);
+            for (int j = 0; j < m; ++j) {
+              const int64_t row = (int64_t)t0.y + r0 + j;
+              for (int a = 0; a < I16 / 4; ++a)
+                cp_async4(asc + j * I16 + 4 * a, p.sfa + ((size_t)(row >> 7) * (I16 / 4) + a) * 512 + (row & 31) * 16 +
+                                                     ((row >> 5) & 3) * 4);
+            }
+            cp_async_mbar_arrive(&bars->xfull[xb]);
+            mbar_arrive_expect_tx(&bars->xfull[xb], (uint32_t)m * (uint32_t)I2);
+            xarmed |= 1u << xb;
+            xlast = (xlast & ~(1u << xb)) | (xph << xb);
+            for (int j = 0; j < m; ++j)
+              bulk_g2s(acodes + (xb * kGvTok + j) * I2, p.aq + (size_t)(t0.y + r0 + j) * I2, (uint32_t)I2,
+                       &bars->xfull[xb]);
+            xb ^= 1u;
+            if (xb == 0) xph ^= 1u;
+            for (int i = 0; i < cnt; ++i) {
+              if (!g2_wait(&bars->empty[stage], phase ^ 1u, bars, p.status)) {
+                ok = false;
+                break;
+              }
+              uint8_t* st = ring + stage * SB;
+              const size_t tile = (size_t)e * NMT + mt0 + i;
+              mbar_arrive_expect_tx(&bars->full[stage], (uint32_t)SB);
+              armed |= 1u << stage;
+              last_phase = (last_phase & ~(1u << stage)) | (phase << stage);
+              bulk_g2s(st, p.w2p + tile * NKB2 * 8192, (uint32_t)(NKB2 * 8192), &bars->full[stage]);
+              bulk_g2s(st + NKB2 * 8192, p.sf2p + tile * (p.I / 64) * 512, (uint32_t)(NKB2 * 1024),
+                       &bars->full[stage]);
+              if (++stage == kG2Stages) {
+                stage = 0;
+                phase ^= 1u;
+              }
+            }
+          }
+        }
+        u0 = u1;
+        t0 = t1;
+#pragma unroll
+        for (int j = 0; j < kGvTok; ++j) {
+          f0[j] = f1[j];
+          w0[j] = w1[j];
+        }
+        u1 = u2;
+        t1 = t2;
+        u2 = u3;
+      }
+      if (ok && g2_wait(&bars->xempty[xb], xph ^ 1u, bars, p.status)) {
+        job_store(&bars->job[xb][0], make_int4(-1, 0, 0, 0));
+        xarmed |= 1u << xb;
+        xlast = (xlast & ~(1u << xb)) | (xph << xb);
+        cp_async_mbar_arrive(&bars->xfull[xb]);
+        mbar_arrive(&bars->xfull[xb]);
+      }
+      cp_async_wait_all();
+      for (int s = 0; s < kG2Stages; ++s)
+        if (armed & (1u << s)) mbar_wait(&bars->full[s], (last_phase >> s) & 1u, p.status);
+      for (int b = 0; b < 2; ++b)
+        if (xarmed & (1u << b)) mbar_wait(&bars->xfull[b], (xlast >> b) & 1u, p.status);
+    }
+  } else if (warp == kGvWarps + 1) {
+    // --------------------------------------------------------- converter
+    uint32_t xb = 0, xph = 0, ab = 0, aph = 0, base = 0;
+    while (true) {
+      if (!g2_wait(&bars->xfull[xb], xph, bars, p.status)) break;
+      const int4 jb = job_load(&bars->job[xb][0]);
+      if (!g2_wait(&bars->afree[ab], aph ^ 1u, bars, p.status)) break;
+      if (jb.x < 0) {
+        __syncwarp();
+        if (lane == 0) {
+          job_store(&bars->meta[ab][0], jb);
+          mbar_arrive(&bars->aready[ab]);
+        }
+        break;
+      }
+      const int m = jb.w & 0xFF, cnt = min(G, NMT - (jb.w >> 16));
+      g2_fill_a16(smem_u32(acodes + xb * kGvTok * I2), smem_u32(ascales + xb * kGvTok * I16),
+                  smem_u32(a16 + (size_t)ab * kGvTok * PW * 4), m, p.I, lane);
+      __syncwarp();
+      if (lane == 0) {
+        job_store(&bars->meta[ab][0], jb);
+        job_store(&bars->meta[ab][1], job_load(&bars->job[xb][1]));
+        job_store(&bars->meta[ab][2], job_load(&bars->job[xb][2]));
+        job_store(&bars->meta[ab][3], make_int4((int)base, 0, 0, 0));
+        mbar_arrive(&bars->xempty[xb]);
+        mbar_arrive(&bars->aready[ab]);
+      }
+      base += (uint32_t)cnt;
+      xb ^= 1u;
+      if (xb == 0) xph ^= 1u;
+      ab ^= 1u;
+      if (ab == 0) aph ^= 1u;
+    }
+  } else {
+    // ------------------------------------------------------------ consumers
+    const int g = lane >> 2, t = lane & 3, R0 = 16 * (warp & 7) + g, wp = warp >> 3;
+    const uint32_t ring_s = smem_u32(ring);
+    uint32_t ab = 0, aph = 0;
+    while (true) {
+      if (!g2_wait(&bars->aready[ab], aph, bars, p.status)) break;
+      const int4 jb = job_load(&bars->meta[ab][0]);
+      if (jb.x < 0) break;
+      const int4 tk = job_load(&bars->meta[ab][1]);
+      const int4 wq = job_load(&bars->meta[ab][2]);
+      const uint32_t base = (uint32_t)job_load(&bars->meta[ab][3]).x;
+      const int e = jb.y, m = jb.w & 0xFF, mask = (jb.w >> 8) & 0xFF, mt0 = jb.w >> 16;
+      const int cnt = min(G, NMT - mt0);
+      const float s2 = __ldg(p.dAdW2 + e);
+      // this thread's pairs 2t, 2t + 1 (their tokens, -1 if none, and route weights)
+      const int tok0 = (t == 0) ? tk.x : (t == 1) ? tk.z : -1, tok1 = (t == 0) ? tk.y : (t == 1) ? tk.w : -1;
+      const float wt0 = __int_as_float((t == 0) ? wq.x : wq.z), wt1 = __int_as_float((t == 0) ? wq.y : wq.w);
+      const bool use0 = 2 * t < m && ((mask >> (2 * t)) & 1) && tok0 >= 0;
+      const bool use1 = 2 * t + 1 < m && ((mask >> (2 * t + 1)) & 1) && tok1 >= 0;
+      const uint32_t a16_lane = smem_u32(a16) + 4 * (((int)ab * kGvTok + min(g, m - 1)) * PW + t * kG2Seg);
+      bool ok = true;
+      // the job's ring positions of this warp's parity
+      for (uint32_t n = base + ((base & 1u) != (uint32_t)wp ? 1u : 0u); n < base + (uint32_t)cnt; n += 2) {
+        const uint32_t stage = n % kG2Stages, phase = (n / kG2Stages) & 1u;
+        if (!g2_wait(&bars->full[stage], phase, bars, p.status)) {
+          ok = false;
+          break;
+        }
+        float sum[4];
+        g2_tile(ring_s + stage * SB, a16_lane, R0, t, NKB2, sum);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->empty[stage]);
+        float* accr = p.acc + (size_t)(mt0 + (int)(n - base)) * 128 + R0;
+        if (use0) {
+          atomicAdd(accr + (size_t)tok0 * p.H, __fmul_rn(__fmul_rn(sum[0], s2), wt0));
+          atomicAdd(accr + (size_t)tok0 * p.H + 8, __fmul_rn(__fmul_rn(sum[2], s2), wt0));
+        }
+        if (use1) {
+          atomicAdd(accr + (size_t)tok1 * p.H, __fmul_rn(__fmul_rn(sum[1], s2), wt1));
+          atomicAdd(accr + (size_t)tok1 * p.H + 8, __fmul_rn(__fmul_rn(sum[3], s2), wt1));
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->afree[ab]);
+      ab ^= 1u;
+      if (ab == 0) aph ^= 1u;
+      if (!ok) break;
+    }
+  }
+}
+
 size_t fc1_gemv_smem(int H) { return gv_smem_bytes(H); }
 
+size_t fc2_gemv_smem(int I) { return g2_smem_bytes(I); }
+
 cudaError_t gemv_set_attributes() {
-  return cudaFuncSetAttribute((const void*)fc1_gemv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  const cudaError_t err = cudaFuncSetAttribute((const void*)fc1_gemv_kernel,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemOptin);
+  if (err != cudaSuccess) return err;
+  return cudaFuncSetAttribute((const void*)fc2_gemv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               (int)kSmemOptin);
+}
+
+cudaError_t launch_fc2_gemv(const Fc2Args& a, int grid, cudaStream_t st) {
+  Fc2Args args = a;
+  void* kargs[] = {&args};
+  return launch_with_pdl((const void*)fc2_gemv_kernel, dim3(grid), dim3(kG2Threads), g2_smem_bytes(a.I), st, kargs);
 }
 
 cudaError_t launch_fc1_gemv(const CUtensorMap& w13, const Fc1Args& a, int grid, cudaStream_t st) {

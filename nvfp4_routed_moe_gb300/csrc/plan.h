@@ -137,10 +137,10 @@ struct RouteArgs {
 };
 
 struct Fc1Args {
-  const uint8_t* w13p;      // prepared W13 codes (the CUDA-core kernel's bulk copies; the MMA kernel uses a tensor map)
+  const uint8_t* w13p;      // prepared W13 codes (the decode kernel; the tcgen05 kernel uses a tensor map)
   const uint8_t* sf13p;
   const uint8_t* xq;        // [T, H/2] token-major X codes, gathered per tile row
-  const uint8_t* sft;       // [T, H/16] token-major X block scales (CUDA-core kernel)
+  const uint8_t* sft;       // [T, H/16] token-major X block scales (decode kernel)
   const int32_t* prow_pair; // [Ppad] flat pair of each padded row (-1: padding)
   const uint8_t* sfx;
   const int32_t* tt_list;
@@ -161,7 +161,9 @@ struct Fc1Args {
 };
 
 struct Fc2Args {
+  const uint8_t* w2p;       // prepared W2 codes (the decode kernel; the tcgen05 kernel uses a tensor map)
   const uint8_t* sf2p;
+  const uint8_t* aq;        // [Ppad, I/2] A codes (the decode kernel; the tcgen05 kernel uses tensor maps)
   const uint8_t* sfa;
   const int32_t* tt_list;
   const int32_t* hdr;
@@ -173,6 +175,7 @@ struct Fc2Args {
   int32_t H, I, E, k;
   int32_t nq;               // passes over H (H/128 divisible by nq)
   int32_t kbs_per_stage;    // k-blocks per W2 ring stage: I/128 (a whole output tile) or 1 (selects the kernel)
+  int32_t group;            // output tiles per work unit of the decode kernel
   int32_t* next;            // work counter (hdr + HDR_FC2_NEXT): CTAs take units from it when `dynamic`
   int32_t dynamic;          // 1: units by the work counter; 0: the static stride blockIdx.x + i * gridDim.x
   int32_t max_tiles;
@@ -239,7 +242,7 @@ struct QuantXArgs {
   const float* qX;          // [1]
   uint8_t* xq;              // [T, H/2] token-major codes
   uint8_t* sfx;             // atom layout, H/16 chunks per row: written here when sft is null, by the atom
-                            // pass when both are set; null: no atoms (FC1 on the CUDA cores reads sft)
+                            // pass when both are set; null: no atoms (FC1's decode kernel reads sft)
   uint8_t* sft;             // [T, H/16] token-major block scales, or null
   int64_t T;
   int32_t H, k;

@@ -26,7 +26,7 @@ cudaError_t launch_with_pdl(const void* fn, dim3 grid, dim3 block, size_t smem, 
 // once per token into token-major rows that sf_atoms_kernel then lays out
 // with whole-atom writes (a token's scales land in 56 different atoms, and
 // scattered 4-byte writes cost more than the extra pass).  When FC1 runs on
-// the CUDA cores (decode batches) it reads the token-major scales itself:
+// the decode kernel (small batches) it reads the token-major scales itself:
 // then no atoms are written and this kernel stores the route weights.
 __global__ void __launch_bounds__(256) quant_x_kernel(const QuantXArgs a) {
   // Warp w takes 32 groups (512 elements) of token w / S, S = ceil(H/512)

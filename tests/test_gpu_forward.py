@@ -35,14 +35,14 @@ def test_tiny_forward_matches_oracle(tiny):
     assert_close(out_bits(out), ref, "tiny")
 
 
-@pytest.mark.parametrize("fc1", ["cuda_cores", "tensor_cores"])
+@pytest.mark.parametrize("fc1", ["decode_kernel", "tcgen05"])
 def test_tiny_intermediates(tiny, fc1, monkeypatch):
     """Routing arrays, quantized X (codes and block scales) bit-exact and the
-    requantized A codes, with FC1 on the CUDA cores (the default at this
-    size: X's block scales token-major) and on the tensor cores (block
+    requantized A codes, with FC1 on the decode kernel (the default at this
+    size: X's block scales token-major) and on the tcgen05 GEMM (block
     scales in the atoms of every routed row)."""
     inp, m = tiny
-    if fc1 == "tensor_cores":
+    if fc1 == "tcgen05":
         monkeypatch.setenv("NVFP4MOE_FC1_GEMV", "0")
     out, ws = m.forward_inputs()
     torch.cuda.synchronize()
@@ -61,12 +61,12 @@ def test_tiny_intermediates(tiny, fc1, monkeypatch):
     rank = r["gather"] - (r["cumsum"] - r["count"])[inp.expert_ids.ravel()]
     np.testing.assert_array_equal(row_pos, pstart[inp.expert_ids.ravel()] + rank)
     # quantized X, bit-exact (oracle quantizes each token with qX): the codes
-    # once per token, the block scales once per token (CUDA-core FC1) or in
-    # the atoms of every routed row (tensor-core FC1)
+    # once per token, the block scales once per token (decode-kernel FC1) or
+    # in the atoms of every routed row (tcgen05 FC1)
     xq_ref, xsf_ref = oracle.nvfp4_quant_rows(gen.bf16_bits_to_f32(inp.x), q=inp.qX)
     npad = int(row_pos.max()) + 1
     np.testing.assert_array_equal(ws_u8(ws, lay.xq, T * (H // 2)).reshape(T, H // 2), xq_ref)
-    if fc1 == "cuda_cores":
+    if fc1 == "decode_kernel":
         np.testing.assert_array_equal(ws_u8(ws, lay.sft, T * (H // 16)).reshape(T, H // 16), xsf_ref)
     else:
         sfx = ws_u8(ws, lay.sfx, ((npad + 127) // 128) * (H // 64) * 512)
@@ -133,17 +133,19 @@ def test_tiny_shape_ragged_token_counts(T):
 
 
 @pytest.mark.parametrize("T", [33, 300])
-def test_tiny_shape_cuda_core_fc1_at_any_batch(T, monkeypatch):
-    """FC1 on the CUDA cores forced above its default range: expert tiles of
-    up to ~60 tokens (T = 300, 4 of 32 experts per token) take one job per 4
-    tokens over the same W13 tile, the last one ragged."""
+def test_tiny_shape_decode_kernels_at_any_batch(T, monkeypatch):
+    """FC1 and FC2 on the decode kernels forced above their default range:
+    expert tiles of up to ~60 tokens (T = 300, 4 of 32 experts per token)
+    take one job per 4 tokens over the same weight tiles, the last one
+    ragged."""
     monkeypatch.setenv("NVFP4MOE_FC1_GEMV", "1")
+    monkeypatch.setenv("NVFP4MOE_FC2_GEMV", "1")
     inp = cases.prepare_tiny(1, T=T)
     m = Model(inp)
     out, ws = m.forward_inputs()
     torch.cuda.synchronize()
     assert api.moe_read_status(ws) == (0, 0)
-    assert_close(out_bits(out), cases.run_oracle(inp), f"T={T}, FC1 on the CUDA cores")
+    assert_close(out_bits(out), cases.run_oracle(inp), f"T={T}, decode kernels")
 
 
 def test_zero_input_gives_zero_output(tiny):
@@ -288,31 +290,42 @@ def test_full_shape_decode_all_tokens(full_model, T):
     assert_close(out_bits(out), ref, f"decode T={T}")
 
 
+_GEMM_PATHS = [("1", "1"), ("0", "0"), ("1", "0"), ("0", "1")]
+
+
 @pytest.mark.parametrize("T", [1, 8, 16, 32])
-def test_full_shape_fc1_on_cuda_and_tensor_cores(full_model, T, monkeypatch):
-    """FC1 on the CUDA cores (the default up to 32 tokens) and on the tensor
-    cores: each against the oracle on every token, and the two within the
-    tolerance of each other."""
+def test_full_shape_decode_kernels_and_tensor_core_gemms(full_model, T, monkeypatch):
+    """FC1 and FC2 each on the decode kernels (warp-level MMAs over streamed
+    weights; the default up to 16 tokens) or on the tcgen05 GEMMs, in all
+    four combinations: each against the oracle on every token, and each
+    within the tolerance of the tcgen05 pair."""
     minp, m = full_model
     inp = _full_case(minp, T, "uniform", seed=700 + T)
     ref = cases.run_oracle(inp)
     outs = {}
-    for v in ("1", "0"):
-        monkeypatch.setenv("NVFP4MOE_FC1_GEMV", v)
+    for f1, f2 in _GEMM_PATHS:
+        monkeypatch.setenv("NVFP4MOE_FC1_GEMV", f1)
+        monkeypatch.setenv("NVFP4MOE_FC2_GEMV", f2)
         out, ws = m.forward_inputs(inp)
         torch.cuda.synchronize()
         assert api.moe_read_status(ws) == (0, 0)
-        outs[v] = out_bits(out)
-        assert_close(outs[v], ref, f"T={T}, NVFP4MOE_FC1_GEMV={v}")
-    assert_close(outs["1"], outs["0"], f"T={T}: CUDA-core FC1 against tensor-core FC1")
+        outs[f1, f2] = out_bits(out)
+        assert_close(outs[f1, f2], ref, f"T={T}, NVFP4MOE_FC1_GEMV={f1} NVFP4MOE_FC2_GEMV={f2}")
+    for key in _GEMM_PATHS[2:] + _GEMM_PATHS[:1]:
+        assert_close(outs[key], outs["0", "0"], f"T={T}: {key} against the tcgen05 GEMMs")
 
 
 @pytest.mark.parametrize("T", [7, 32])
-def test_full_shape_crowded_expert_tiles_at_decode(full_model, T):
+@pytest.mark.parametrize("decode", ["default", "forced"])
+def test_full_shape_crowded_expert_tiles_at_decode(full_model, T, decode, monkeypatch):
     """Every token routed to the same 16 experts (in its own order), so each
-    expert tile holds all T tokens: FC1 on the CUDA cores takes ceil(T/4)
-    jobs per W13 tile, the last one ragged at T = 7."""
+    expert tile holds all T tokens: the decode kernels take ceil(T/4) jobs
+    per W13 tile and per group of W2 tiles, the last one ragged at T = 7
+    (forced: the decode kernels at T = 32 too)."""
     minp, m = full_model
+    if decode == "forced":
+        monkeypatch.setenv("NVFP4MOE_FC1_GEMV", "1")
+        monkeypatch.setenv("NVFP4MOE_FC2_GEMV", "1")
     inp = _full_case(minp, T, "uniform", seed=800 + T)
     rs = np.random.default_rng(800 + T)
     experts = rs.choice(inp.E, inp.k, replace=False).astype(np.int32)
@@ -320,7 +333,7 @@ def test_full_shape_crowded_expert_tiles_at_decode(full_model, T):
     out, ws = m.forward_inputs(inp)
     torch.cuda.synchronize()
     assert api.moe_read_status(ws) == (0, 0)
-    assert_close(out_bits(out), cases.run_oracle(inp), f"T={T}, crowded tiles")
+    assert_close(out_bits(out), cases.run_oracle(inp), f"T={T}, crowded tiles, {decode}")
 
 
 @pytest.mark.parametrize("T", [16, 2048])
@@ -439,23 +452,24 @@ def _fc1_abs_sums(inp, toks):
     return out
 
 
-@pytest.mark.parametrize("fc1", ["cuda_cores", "tensor_cores"])
+@pytest.mark.parametrize("fc1", ["decode_kernel", "tcgen05"])
 def test_full_shape_decode_intermediate_codes(full_model, fc1, monkeypatch):
     """The requantized intermediate A of every routed pair at T = 16, read from
-    the workspace, against the oracle's codes, with FC1 on the CUDA cores (the
-    default at this size) and on the tensor cores.  FC1's fp32 sums round in
-    the hardware's order, so a code may differ only where the oracle's SiTU
-    value, moved by at most the fp32 summation error of its pre-activations
-    (57 fp32 roundings of the sum of absolute products: one per K = 64 MMA
-    step and one for the product; the CUDA-core path has fewer in any
-    product's path: 28 group additions per 16-byte chunk, 3 across the
-    chunks, 1 for the product), crosses an E2M1 rounding midpoint -- or
+    the workspace, against the oracle's codes, with FC1 on the decode kernel
+    (the default at this size) and on the tcgen05 GEMM.  FC1's fp32 sums
+    round in the hardware's order, so a code may differ only where the
+    oracle's SiTU value, moved by at most the fp32 summation error of its
+    pre-activations (57 fp32 roundings of the sum of absolute products: one
+    per K = 64 MMA step and one for the product; the decode kernel has fewer
+    in any product's path: 16 MMA steps of a k-block in four chains, their
+    3 sums, 14 k-block sums, the two k-block parities' sum and the product),
+    crosses an E2M1 rounding midpoint -- or
     where the group's block scale itself differs because its amax crosses an
     E4M3 midpoint the same way.  The mismatch rate is reported."""
     minp, m = full_model
     T = 16
     inp = _full_case(minp, T, "uniform", seed=T)
-    if fc1 == "tensor_cores":
+    if fc1 == "tcgen05":
         monkeypatch.setenv("NVFP4MOE_FC1_GEMV", "0")
     out, ws = m.forward_inputs(inp)
     torch.cuda.synchronize()
