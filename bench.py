@@ -300,7 +300,8 @@ def cpu_model():
 
 
 # Sources compiled into the GEMM kernels (the file and everything it includes).
-GEMM_SOURCES = ("nvfp4_routed_moe_gb300/csrc/gemm.cu", "nvfp4_routed_moe_gb300/csrc/nvfp4.cuh",
+GEMM_SOURCES = ("nvfp4_routed_moe_gb300/csrc/gemm.cu", "nvfp4_routed_moe_gb300/csrc/gemv.cu",
+                "nvfp4_routed_moe_gb300/csrc/nvfp4.cuh",
                 "nvfp4_routed_moe_gb300/csrc/ptx.cuh", "nvfp4_routed_moe_gb300/csrc/plan.h",
                 "include/nvfp4moe.h")
 
@@ -647,10 +648,12 @@ def main():
     fp4 = fp4_peak(torch.cuda.get_device_properties(local).multi_processor_count) if world == 1 or rank == 0 \
         else None
     pairs = int(batch["pairs"])
+    decode_kernels = dict(zip(("fc1", "fc2"), api.moe_forward_kernels(shp, T)))
     for kname, (fn, formula) in KERNEL_BYTES.items():
         b_k = fn(T, n_active)
-        traffic = traffic_from_profile(kname, args.workload)
-        r = {"kernel": f"{kname}_kernel", "bound": "hbm", "achieved": None, "peak": peak, "unit": "GB/s",
+        kernel = f"{kname}_gemv" if decode_kernels.get(kname) else kname   # the decode kernel or the tcgen05 GEMM
+        traffic = traffic_from_profile(kernel, args.workload)
+        r = {"kernel": f"{kernel}_kernel", "bound": "hbm", "achieved": None, "peak": peak, "unit": "GB/s",
              "frac": None, "traffic": traffic, "peak_source": peak_src, "bytes_per_launch": b_k,
              "bytes_formula": formula,
              "traffic_over_algorithmic": traffic / b_k if traffic else None}

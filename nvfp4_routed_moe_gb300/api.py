@@ -29,7 +29,7 @@ STREAM_PRODUCER_TIMEOUT = 1
 EXPORTED = ["moe_workspace_size", "moe_prepared_weight_bytes", "moe_prepare_weights", "moe_prepare_workspace",
             "moe_forward", "moe_forward_local_experts", "moe_init_routing", "moe_init_routing_static", "moe_read_status", "moe_status_string", "moe_test_codec_sweep",
             "moe_test_quantize_rows", "moe_test_situ_requant", "moe_test_requant_lanes", "moe_test_mma_fp4", "moe_test_mma_peak",
-            "moe_workspace_layout", "moe_forward_launch_count", "moe_profile_start", "moe_profile_stop",
+            "moe_workspace_layout", "moe_forward_launch_count", "moe_forward_kernels", "moe_profile_start", "moe_profile_stop",
             "moe_stream_ring_size", "moe_stream_ring_init", "moe_stream_begin", "moe_stream_publish",
             "moe_stream_forward", "moe_stream_read_status"]
 
@@ -97,6 +97,7 @@ def lib():
         "moe_test_mma_peak": [i32, i32, i32, i32, i32, P, P, P],
         "moe_workspace_layout": [S, sz, ctypes.POINTER(moe_ws_layout_t)],
         "moe_forward_launch_count": [S, i64, ctypes.POINTER(i32)],
+        "moe_forward_kernels": [S, i64, ctypes.POINTER(i32), ctypes.POINTER(i32)],
         "moe_profile_start": [i32],
         "moe_profile_stop": [ctypes.POINTER(ctypes.c_float), ctypes.POINTER(i32)],
         "moe_stream_ring_size": [S, R, ctypes.POINTER(sz)],
@@ -249,6 +250,14 @@ def moe_workspace_layout(shp, ws_bytes: int) -> moe_ws_layout_t:
     out = moe_ws_layout_t()
     _check(lib().moe_workspace_layout(ctypes.byref(shp), ws_bytes, ctypes.byref(out)), "moe_workspace_layout")
     return out
+
+
+def moe_forward_kernels(shp, num_tokens: int):
+    """(fc1_decode, fc2_decode): True where the forward runs the decode kernel."""
+    a, b = ctypes.c_int32(), ctypes.c_int32()
+    _check(lib().moe_forward_kernels(ctypes.byref(shp), num_tokens, ctypes.byref(a), ctypes.byref(b)),
+           "moe_forward_kernels")
+    return bool(a.value), bool(b.value)
 
 
 def moe_forward_launch_count(shp, num_tokens: int) -> int:

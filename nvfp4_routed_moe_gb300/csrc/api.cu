@@ -1105,6 +1105,17 @@ moe_status_t moe_profile_stop(float* stage_ms, int32_t* calls) {
   return st;
 }
 
+moe_status_t moe_forward_kernels(const moe_shape_t* shape, int64_t num_tokens, int32_t* fc1_decode,
+                                 int32_t* fc2_decode) {
+  moe_status_t st = shape_supported(shape);
+  if (st != MOE_OK) return st;
+  if (!fc1_decode || !fc2_decode || num_tokens < 1) return MOE_ERR_INVALID_ARG;
+  const Shape s = to_shape(shape);
+  *fc1_decode = fc1_gemv(s, num_tokens) ? 1 : 0;
+  *fc2_decode = fc2_gemv(s, num_tokens) ? 1 : 0;
+  return MOE_OK;
+}
+
 moe_status_t moe_forward_launch_count(const moe_shape_t* shape, int64_t num_tokens, int32_t* launches) {
   moe_status_t st = shape_supported(shape);
   if (st != MOE_OK) return st;

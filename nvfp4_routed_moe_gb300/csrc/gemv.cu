@@ -54,8 +54,10 @@ namespace moe {
 
 cudaError_t launch_with_pdl(const void* fn, dim3 grid, dim3 block, size_t smem, cudaStream_t st, void** args);
 
-constexpr int kGvWarps = 16;                      // consumer warps: 16 W13 rows, alternate k-blocks
-constexpr int kGvThreads = (kGvWarps + 1) * 32;   // + the producer warp
+constexpr int kGvWarps = 16;                      // FC2 consumer warps: 16 W2 rows, alternate output tiles
+constexpr int kG1Par = 2;                         // FC1: k-block classes (k-block % kG1Par), 8 warps each
+constexpr int kG1Warps = 8 * kG1Par;              // FC1 consumer warps: 16 W13 rows each
+constexpr int kGvThreads = (kG1Warps + 1) * 32;   // FC1: + the producer warp
 constexpr int kGvTok = 4;                         // tokens per job
 constexpr int kGvStages = 8;
 constexpr int kGvW = 16384;                       // one W13 k-block tile: 128 rows x 128 B
@@ -80,12 +82,12 @@ __host__ __device__ inline int x16_token_words(int H) {
 }
 
 // Shared memory: ring | raw X codes [2][kGvTok][H/2] | raw X scales
-// [2][kGvTok][H/16] | X16 [kGvTok][token words] | z [2 slots][2 k-block
-// parities][kGvTok][128] fp32 | barriers; plus 1 KB for the alignment of the
+// [2][kGvTok][H/16] | X16 [kGvTok][token words] | z [2 slots][kG1Par k-block
+// classes][kGvTok][128] fp32 | barriers; plus 1 KB for the alignment of the
 // base.
 static size_t gv_smem_bytes(int H) {
   return (size_t)kGvStages * kGvStage + (size_t)2 * kGvTok * (H / 2) + (size_t)2 * kGvTok * (H / 16) +
-         (size_t)kGvTok * x16_token_words(H) * 4 + (size_t)4 * kGvTok * 128 * 4 + sizeof(GvBars) + 1024;
+         (size_t)kGvTok * x16_token_words(H) * 4 + (size_t)2 * kG1Par * kGvTok * 128 * 4 + sizeof(GvBars) + 1024;
 }
 
 // ----------------------------------------------------------- shared memory
@@ -241,7 +243,7 @@ __device__ __forceinline__ void gv_kblock(uint32_t st, uint32_t x16, int R0, int
 // consumer warps takes 4-byte words i, i + 256, ...
 __device__ __forceinline__ void gv_fill_x16(uint32_t xs, uint32_t xsc, uint32_t x16, int m, int H, int tid) {
   const int H2 = H / 2, G = H / 16, H8 = H / 8, TW = x16_token_words(H);
-  for (int wi = tid; wi < m * H8; wi += kGvWarps * 32) {
+  for (int wi = tid; wi < m * H8; wi += kG1Warps * 32) {
     const int j = wi / H8, ww = wi - j * H8;
     const uint32_t codes = lds32(xs + j * H2 + 4 * ww);
     const uint32_t s2 = h2_lo2(e4m3x2_to_h2(lds8(xsc + j * G + (ww >> 1))));
@@ -281,21 +283,21 @@ __global__ void __launch_bounds__(kGvThreads, 1)
   uint8_t* xscales = xcodes + 2 * kGvTok * H2;
   uint8_t* x16 = xscales + 2 * kGvTok * G;
   float* zbuf = reinterpret_cast<float*>(x16 + (size_t)kGvTok * x16_token_words(p.H) * 4);
-  GvBars* bars = reinterpret_cast<GvBars*>(zbuf + 4 * kGvTok * 128);
+  GvBars* bars = reinterpret_cast<GvBars*>(zbuf + 2 * kG1Par * kGvTok * 128);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int s = 0; s < kGvStages; ++s) {
       mbar_init(&bars->full[s], 1);
-      mbar_init(&bars->empty[s], kGvWarps / 2);   // the warps of the k-block's parity
+      mbar_init(&bars->empty[s], 8);   // the warps of the k-block's class
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&bars->xfull[b], 1);
-      mbar_init(&bars->xempty[b], kGvWarps);
-      mbar_init(&bars->zready[b], kGvWarps);
-      mbar_init(&bars->zfree[b], kGvWarps);
+      mbar_init(&bars->xempty[b], kG1Warps);
+      mbar_init(&bars->zready[b], kG1Warps);
+      mbar_init(&bars->zfree[b], kG1Warps);
     }
-    mbar_init(&bars->x16ready, kGvWarps);
-    mbar_init(&bars->x16free, kGvWarps);
+    mbar_init(&bars->x16ready, kG1Warps);
+    mbar_init(&bars->x16free, kG1Warps);
     bars->abort_flag = 0;
     fence_barrier_init();
   }
@@ -305,7 +307,7 @@ __global__ void __launch_bounds__(kGvThreads, 1)
   const int num_units = min(max(p.hdr[HDR_NUM_TT], 0), p.max_tiles) * NIT;   // (token tile, W13 tile)
   const int4* tiles = reinterpret_cast<const int4*>(p.tt_list);
 
-  if (warp == kGvWarps) {
+  if (warp == kG1Warps) {
     if (lane == 0) {
       // ---------------------------------------------------------- producer
       tma_prefetch_desc(&tm_w13);
@@ -414,7 +416,7 @@ __global__ void __launch_bounds__(kGvThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ consumers
-    const int g = lane >> 2, t = lane & 3, R0 = 16 * (warp & 7) + g, kp = warp >> 3;
+    const int g = lane >> 2, t = lane & 3, R0 = 16 * (warp & 7) + g, kp = warp >> 3;   // k-block class kp
     const int tid = threadIdx.x, ej = tid >> 6, ef = tid & 63;   // epilogue (tid < 256): token ej, feature ef
     const int TW = x16_token_words(p.H);
     const uint32_t ring_s = smem_u32(ring), x16_s = smem_u32(x16);
@@ -444,7 +446,7 @@ __global__ void __launch_bounds__(kGvThreads, 1)
       const uint32_t x16_lane = x16_s + 4 * (min(g, m - 1) * TW + t * kGvSeg);
       float sum[4] = {0.0f, 0.0f, 0.0f, 0.0f};
       bool ok = true;
-      for (int kb = kp; kb < NKB; kb += 2) {
+      for (int kb = kp; kb < NKB; kb += kG1Par) {
         const uint32_t n = kbase + (uint32_t)kb, stage = n % kGvStages, phase = (n / kGvStages) & 1u;
         if (!gv_wait(&bars->full[stage], phase, bars, p.status)) {
           ok = false;
@@ -461,7 +463,7 @@ __global__ void __launch_bounds__(kGvThreads, 1)
       if (!ok) break;
       // partial z[token][row] of this k-block parity: thread (g, t) holds rows
       // R0, R0 + 8 of tokens 2t, 2t + 1
-      const uint32_t z = smem_u32(zbuf + zb * 2 * kGvTok * 128);
+      const uint32_t z = smem_u32(zbuf + zb * kG1Par * kGvTok * 128);
       const uint32_t zp = z + 4 * kp * kGvTok * 128;
       if (!gv_wait(&bars->zfree[zb], zph ^ 1u, bars, p.status)) break;
       if (2 * t < m) {
@@ -479,9 +481,13 @@ __global__ void __launch_bounds__(kGvThreads, 1)
       // 16 lanes quantize a 16-feature group (the first 8 warps)
       float a = 0.0f;
       if (tid < 256 && ej < m) {
-        const uint32_t z1 = z + 4 * kGvTok * 128;
-        const float zg = lds_f32(z + 4 * (ej * 128 + 2 * ef)) + lds_f32(z1 + 4 * (ej * 128 + 2 * ef));
-        const float zu = lds_f32(z + 4 * (ej * 128 + 2 * ef + 1)) + lds_f32(z1 + 4 * (ej * 128 + 2 * ef + 1));
+        float zg = lds_f32(z + 4 * (ej * 128 + 2 * ef)), zu = lds_f32(z + 4 * (ej * 128 + 2 * ef + 1));
+#pragma unroll
+        for (int c = 1; c < kG1Par; ++c) {
+          const uint32_t zc = z + 4 * c * kGvTok * 128;
+          zg += lds_f32(zc + 4 * (ej * 128 + 2 * ef));
+          zu += lds_f32(zc + 4 * (ej * 128 + 2 * ef + 1));
+        }
         a = situ_f32(__fmul_rn(zg, s13), __fmul_rn(zu, s13), be, 1.0f / be, la, 1.0f / la);
       }
       __syncwarp();

@@ -119,6 +119,20 @@ def test_forward_token_count_alignment_and_capacity_checked_before_launch(L):
     assert fwd(1 << 20) == 3                            # more tokens than the workspace holds
     assert fwd(16) == 4                                 # never prepared
 
+def test_forward_kernel_choice(L, monkeypatch):
+    """The decode kernels run FC1 and FC2 up to 16 tokens, the tcgen05 GEMMs
+    above; the environment overrides either."""
+    full = api.shape(3584, 384, 896, 16)
+    assert api.moe_forward_kernels(full, 1) == (True, True)
+    assert api.moe_forward_kernels(full, 16) == (True, True)
+    assert api.moe_forward_kernels(full, 17) == (False, False)
+    assert api.moe_forward_kernels(full, 16384) == (False, False)
+    monkeypatch.setenv("NVFP4MOE_FC1_GEMV", "0")
+    monkeypatch.setenv("NVFP4MOE_FC2_GEMV", "1")
+    assert api.moe_forward_kernels(full, 4096) == (False, True)
+    assert api.moe_forward_kernels(full, 8) == (False, True)
+
+
 def test_launch_count(L):
     assert api.moe_forward_launch_count(api.shape(3584, 384, 896, 16), 1) == 5
     assert api.moe_forward_launch_count(api.shape(3584, 384, 896, 16), 4096) == 7
