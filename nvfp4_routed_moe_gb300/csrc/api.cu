@@ -329,17 +329,18 @@ static bool fc2_gemv(const Shape& s, int64_t T) {
   return T <= kFc2GemvMaxTokens;
 }
 
-// Output tiles per unit of the decode FC2: about three units per SM for the
-// batch's tile bound, between 2 and half of H (each job's A rows take a few
-// microseconds to arrive, so long units stream best; measured at T = 1..16:
-// 2, 4, 7-8 and 14 tiles).  NVFP4MOE_FC2_GROUP overrides.
+// Output tiles per unit of the decode FC2: long units stream best (each
+// job's A rows take a few microseconds to arrive, and units are claimed one
+// at a time), so about 0.8 units per SM for the batch's tile bound, at most
+// half of H/128 (measured at T = 1, 2, 4, 8, 16: 4, 7, 14, 14-28, 14 tiles).
+// NVFP4MOE_FC2_GROUP overrides.
 static int fc2_gemv_group(const Shape& s, int64_t tiles, int sms) {
   if (const char* v = std::getenv("NVFP4MOE_FC2_GROUP")) {
     const int g = std::atoi(v);
     if (g >= 1) return g;
   }
-  const int64_t nmt = s.H / 128, g = (tiles * nmt + 3 * (int64_t)sms - 1) / (3 * (int64_t)sms);
-  return (int)std::max<int64_t>(1, std::min<int64_t>(std::max<int64_t>(1, nmt / 2), std::max<int64_t>(2, g)));
+  const int64_t nmt = s.H / 128, g = (tiles * nmt * 5 + 4 * (int64_t)sms - 1) / (4 * (int64_t)sms);
+  return (int)std::max<int64_t>(1, std::min<int64_t>(std::max<int64_t>(1, nmt / 2), g));
 }
 
 // Above kSfTwoPassMin pairs the X scales take the token-major + atom pass

@@ -58,7 +58,7 @@ constexpr int kGvWarps = 16;                      // FC2 consumer warps: 16 W2 r
 constexpr int kG1Par = 2;                         // FC1: k-block classes (k-block % kG1Par), 8 warps each
 constexpr int kG1Warps = 8 * kG1Par;              // FC1 consumer warps: 16 W13 rows each
 constexpr int kGvThreads = (kG1Warps + 1) * 32;   // FC1: + the producer warp
-constexpr int kGvTok = 4;                         // tokens per job
+constexpr int kGvTok = 4;                         // tokens (FC1) or pairs (FC2) per job
 constexpr int kGvStages = 8;
 constexpr int kGvW = 16384;                       // one W13 k-block tile: 128 rows x 128 B
 constexpr int kGvStage = kGvW + 2048;             // + its four scale atoms
@@ -685,27 +685,38 @@ __global__ void __launch_bounds__(kG2Threads, 1) fc2_gemv_kernel(const Fc2Args p
           w[j] = in ? __ldg(p.wrow + t.y + r0 + j) : 0.0f;
         }
       };
-      // As in FC1: three units in flight (u0 streamed, u1's tile and its first
-      // job's pairs and route weights, u2 taken).
+      // One unit ahead, taken late: while the last job of the current unit
+      // issues its stages, one step per stage takes the next unit from the
+      // counter, loads its tile descriptor and then its first job's pairs,
+      // so each step's latency hides under the stream and a CTA holds at most
+      // one unit it has not started (the units are few and long here, and
+      // units reserved early would stay with CTAs that fall behind).
       int u0 = take();
       int4 t0 = gv_tile(tiles, u0, NG);
       int f0[kGvTok];
       float w0[kGvTok];
       pairs(t0, 0, f0, w0);
-      int u1 = u0 >= 0 ? take() : -1;
-      int4 t1 = gv_tile(tiles, u1, NG);
-      int u2 = u1 >= 0 ? take() : -1;
+      int nu = -1, step = 0;
+      int4 nt = make_int4(-1, 0, 0, 0);
+      int nf[kGvTok];
+      float nw[kGvTok];
+      auto advance = [&]() {
+        if (step == 0) {
+          nu = take();
+        } else if (step == 1) {
+          nt = gv_tile(tiles, nu, NG);
+        } else if (step == 2) {
+          pairs(nt, 0, nf, nw);
+        }
+        if (step < 3) ++step;
+      };
       while (ok && u0 >= 0) {
-        int f1[kGvTok];
-        float w1[kGvTok];
-        pairs(t1, 0, f1, w1);
-        const int4 t2 = gv_tile(tiles, u2, NG);
-        const int u3 = u2 >= 0 ? take() : -1;
         if (!gv_tile_ok(t0, p.E, p.max_rows)) {
           set_status(p.status, DEVSTAT_BAD_TILE);
         } else {
           const int e = t0.x, mt0 = (u0 % NG) * G, cnt = min(G, NMT - mt0);
           for (int r0 = 0; r0 < t0.z && ok; r0 += kGvTok) {
+            const bool last_job = r0 + kGvTok >= t0.z;
             int f[kGvTok];
             float w[kGvTok];
             if (r0 == 0) {
@@ -767,19 +778,19 @@ __global__ void __launch_bounds__(kG2Threads, 1) fc2_gemv_kernel(const Fc2Args p
                 stage = 0;
                 phase ^= 1u;
               }
+              if (last_job) advance();
             }
           }
         }
-        u0 = u1;
-        t0 = t1;
+        while (step < 3) advance();
+        u0 = nu;
+        t0 = nt;
 #pragma unroll
         for (int j = 0; j < kGvTok; ++j) {
-          f0[j] = f1[j];
-          w0[j] = w1[j];
+          f0[j] = nf[j];
+          w0[j] = nw[j];
         }
-        u1 = u2;
-        t1 = t2;
-        u2 = u3;
+        step = 0;
       }
       if (ok && g2_wait(&bars->xempty[xb], xph ^ 1u, bars, p.status)) {
         job_store(&bars->job[xb][0], make_int4(-1, 0, 0, 0));
