@@ -157,7 +157,8 @@ def next_rows_sweep(shp, flush, dev, w, scales, winp, peak):
     """The widened paths at T = 4096 (uniform ids), each beside the plain
     forward of the same batch: the chunk-ready streaming front end (four
     1024-token chunks through a two-slot ring, publish and forward on one
-    stream), one expert-parallel rank's slice (the first 112 of 896 experts,
+    stream, then on two streams with the forwards held to all but 16 SMs),
+    one expert-parallel rank's slice (the first 112 of 896 experts,
     its own prepared weights), and per-expert SiTU parameters."""
     import torch
     from nvfp4_routed_moe_gb300 import api
@@ -188,7 +189,42 @@ def next_rows_sweep(shp, flush, dev, w, scales, winp, peak):
     assert api.moe_read_status(ws_c) == (0, 0) and api.moe_stream_read_status(ring) == 0
     res["stream"] = {"chunk": C, "slots": S, "ms": round(t_st, 4), "tokens_per_s": T / (t_st * 1e-3),
                      "vs_plain": t_plain / t_st}
-    del ring, ws_c
+    del ring
+
+    # the same chunks with the producer on its own stream and the chunk
+    # forwards held to all but 16 SMs (the ring's SM budget), so that each
+    # publish overlaps the forward of the chunk before it; events order a
+    # publish after the forward that frees its slot, so no device-side wait
+    # ever depends on the other stream
+    budget = max(1, torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count - 16)
+    cfg2 = api.moe_stream_ring_t(S, C, budget)
+    ring2 = torch.empty(api.moe_stream_ring_size(shp, cfg2), dtype=torch.uint8, device="cuda")
+    api.moe_stream_ring_init(shp, cfg2, ring2)
+    prod, cons = torch.cuda.Stream(), torch.cuda.Stream()
+    n_chunks = T // C
+
+    def streamed_two():
+        cur = torch.cuda.current_stream()
+        prod.wait_stream(cur)
+        cons.wait_stream(cur)
+        pub = [torch.cuda.Event() for _ in range(n_chunks)]
+        con = [torch.cuda.Event() for _ in range(n_chunks)]
+        api.moe_stream_begin(shp, cfg2, ring2, stream=prod)
+        for c, base in enumerate(range(0, T, C)):
+            if c >= S:
+                prod.wait_event(con[c - S])
+            api.moe_stream_publish(shp, cfg2, ring2, c, base, C, api.STREAM_ROUTE | api.STREAM_LAYOUT,
+                                   x[base:base + C], ids[base:base + C], rw[base:base + C], stream=prod)
+            pub[c].record(prod)
+            cons.wait_event(pub[c])
+            api.moe_stream_forward(shp, cfg2, ring2, c, *w, qx, *scales, None, None, ws_c, out, stream=cons)
+            con[c].record(cons)
+        cur.wait_stream(cons)
+    t_two = median_ms(streamed_two, flush)
+    assert api.moe_read_status(ws_c) == (0, 0) and api.moe_stream_read_status(ring2) == 0
+    res["stream_two_streams"] = {"chunk": C, "slots": S, "max_sms": budget, "ms": round(t_two, 4),
+                                 "tokens_per_s": T / (t_two * 1e-3), "vs_plain": t_plain / t_two}
+    del ring2, ws_c
 
     EL, lo = shp.num_experts // 8, 0
     shp_l = api.shape(shp.hidden, shp.inter, EL, shp.top_k)

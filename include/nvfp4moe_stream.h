@@ -51,10 +51,15 @@
 extern "C" {
 #endif
 
-/* Ring geometry: 1 <= num_slots <= 64, 1 <= tokens_per_slot. */
+/* Ring geometry: 1 <= num_slots <= 64, 1 <= tokens_per_slot.  max_sms >= 0
+ * caps the SMs that a chunk forward's kernels occupy (its persistent GEMM
+ * grids and its grid-stride kernels are sized to it), leaving the rest of
+ * the GPU to a producer publishing on another stream; 0 (or at least the
+ * device's count): all SMs.  It does not change the ring's size. */
 typedef struct {
   int32_t num_slots;
   int32_t tokens_per_slot;
+  int32_t max_sms;
 } moe_stream_ring_t;
 
 /* Parts of a chunk that moe_stream_publish copies and publishes. */

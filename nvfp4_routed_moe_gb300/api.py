@@ -60,7 +60,7 @@ class moe_ws_layout_t(ctypes.Structure):
 
 
 class moe_stream_ring_t(ctypes.Structure):
-    _fields_ = [("num_slots", ctypes.c_int32), ("tokens_per_slot", ctypes.c_int32)]
+    _fields_ = [("num_slots", ctypes.c_int32), ("tokens_per_slot", ctypes.c_int32), ("max_sms", ctypes.c_int32)]
 
 
 def shape(hidden: int, inter: int, num_experts: int, top_k: int) -> moe_shape_t:

@@ -520,9 +520,10 @@ static moe_status_t forward_impl(const moe_shape_t* shape, int32_t expert_begin,
                                  const uint8_t* w2, const uint8_t* sf2, const float* qX, const float* dX_dW13,
                                  const float* qA, const float* dA_dW2, const float* situ_beta,
                                  const float* situ_linear_beta, void* ws, size_t ws_bytes, void* out,
-                                 cudaStream_t stream, int64_t stream_out_rows = -1) {
+                                 cudaStream_t stream, int64_t stream_out_rows = -1, int max_sms = 0) {
   // stream_out_rows >= 0: a streamed chunk; the finalize writes the chunk's
-  // rows (count and base from the workspace header) into out [stream_out_rows, H]
+  // rows (count and base from the workspace header) into out [stream_out_rows, H].
+  // max_sms > 0: the kernels' grids are sized to at most that many SMs.
   moe_status_t st = shape_supported(shape);
   if (st != MOE_OK) return st;
   if (!x || !expert_ids || !route_weights || !w13 || !sf13 || !w2 || !sf2 || !qX || !dX_dW13 || !qA || !dA_dW2 ||
@@ -538,6 +539,7 @@ static moe_status_t forward_impl(const moe_shape_t* shape, int32_t expert_begin,
   const WsLayout L = make_layout(s, cap);
   int sms = 0;
   MOE_CUDA(device_ready(&sms));
+  if (max_sms > 0 && max_sms < sms) sms = max_sms;
   uint8_t* w = static_cast<uint8_t*>(ws);
   const int64_t T = num_tokens, P = T * s.k;
   const int NIT = s.I / 64, NKB = s.H / kFc1KBlock, NMT = s.H / 128, NKB2 = s.I / kFc2KBlock;
@@ -818,7 +820,8 @@ static moe_status_t ring_check(const moe_shape_t* shape, const moe_stream_ring_t
                                size_t ring_bytes, RingLayout* R) {
   moe_status_t st = shape_supported(shape);
   if (st != MOE_OK) return st;
-  if (!cfg || cfg->num_slots < 1 || cfg->num_slots > 64 || cfg->tokens_per_slot < 1) return MOE_ERR_INVALID_ARG;
+  if (!cfg || cfg->num_slots < 1 || cfg->num_slots > 64 || cfg->tokens_per_slot < 1 || cfg->max_sms < 0)
+    return MOE_ERR_INVALID_ARG;
   if ((int64_t)cfg->tokens_per_slot * shape->top_k >= ((int64_t)1 << 31)) return MOE_ERR_UNSUPPORTED;
   *R = make_ring_layout(to_shape(shape), cfg->num_slots, cfg->tokens_per_slot);
   if (ring) {
@@ -934,7 +937,7 @@ moe_status_t moe_stream_forward(const moe_shape_t* shape, const moe_stream_ring_
   st = forward_impl(shape, 0, shape->num_experts + 1, R.C, reinterpret_cast<uint16_t*>(b + R.x) + slot * R.C * s.H,
                     reinterpret_cast<int32_t*>(b + R.ids) + slot * R.C * s.k,
                     reinterpret_cast<uint16_t*>(b + R.w) + slot * R.C * s.k, w13, sf13, w2, sf2, qX, dX_dW13, qA,
-                    dA_dW2, situ_beta, situ_linear_beta, ws, ws_bytes, out, stream, out_rows);
+                    dA_dW2, situ_beta, situ_linear_beta, ws, ws_bytes, out, stream, out_rows, ring_cfg->max_sms);
   if (st != MOE_OK) return st;
   MOE_CUDA(launch_stream_release(r, ws_hdr, stream));
   return MOE_OK;

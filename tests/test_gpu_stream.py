@@ -23,9 +23,9 @@ SHORT_WAIT_US = 2000   # waits that are meant to run out give up after 2 ms
 class Stream:
     """A ring, a workspace for one chunk and the model's weights."""
 
-    def __init__(self, m: Model, slots: int, tokens_per_slot: int):
+    def __init__(self, m: Model, slots: int, tokens_per_slot: int, max_sms: int = 0):
         self.m = m
-        self.cfg = api.moe_stream_ring_t(slots, tokens_per_slot)
+        self.cfg = api.moe_stream_ring_t(slots, tokens_per_slot, max_sms)
         self.ring = torch.empty(api.moe_stream_ring_size(m.shape, self.cfg), dtype=torch.uint8, device="cuda")
         api.moe_stream_ring_init(m.shape, self.cfg, self.ring)
         self.ws = m.workspace(tokens_per_slot)
@@ -124,6 +124,35 @@ def test_two_streams_ordered_by_events(tiny300):
     assert api.moe_read_status(st.ws) == (0, 0)
     assert api.moe_stream_read_status(st.ring) == 0
     assert_close(out_bits(out), ref, "two streams")
+
+
+@pytest.mark.parametrize("max_sms", [8, 100])
+def test_two_streams_with_an_sm_budget(tiny300, max_sms):
+    """The chunk forwards sized to a budget of SMs (the ring's max_sms), with
+    the producer publishing on its own stream into the rest: the same output
+    as the batch oracle."""
+    inp, m, x, ids, rw, ref = tiny300
+    S, C = 2, 64
+    st = Stream(m, slots=S, tokens_per_slot=C, max_sms=max_sms)
+    out = torch.empty((inp.T, inp.H), dtype=torch.bfloat16, device="cuda")
+    prod, cons = torch.cuda.Stream(), torch.cuda.Stream()
+    torch.cuda.synchronize()
+    st.begin(stream=prod)
+    parts = chunks_of(inp.T, C)
+    published = [torch.cuda.Event() for _ in parts]
+    consumed = [torch.cuda.Event() for _ in parts]
+    for c, (base, n) in enumerate(parts):
+        if c >= S:
+            prod.wait_event(consumed[c - S])
+        st.publish(c, base, n, x, ids, rw, stream=prod)
+        published[c].record(prod)
+        cons.wait_event(published[c])
+        st.forward(c, out, stream=cons)
+        consumed[c].record(cons)
+    torch.cuda.synchronize()
+    assert api.moe_read_status(st.ws) == (0, 0)
+    assert api.moe_stream_read_status(st.ring) == 0
+    assert_close(out_bits(out), ref, f"two streams, max_sms={max_sms}")
 
 
 def test_graph_replay_new_epoch_each_time(tiny300):

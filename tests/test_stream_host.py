@@ -38,6 +38,12 @@ def test_ring_config_validation(L):
     with pytest.raises(api.MoeError) as e:
         api.moe_stream_ring_size(api.shape(3584, 200, 896, 16), api.moe_stream_ring_t(2, 16))
     assert e.value.status == 2
+    # the SM budget: non-negative, and no part of the ring's size
+    with pytest.raises(api.MoeError) as e:
+        api.moe_stream_ring_size(FULL, api.moe_stream_ring_t(2, 16, -1))
+    assert e.value.status == 1
+    assert api.moe_stream_ring_size(FULL, api.moe_stream_ring_t(2, 16, 96)) == \
+        api.moe_stream_ring_size(FULL, api.moe_stream_ring_t(2, 16))
 
 
 def test_calls_rejected_before_the_device(L):
