@@ -343,6 +343,22 @@ static int fc2_gemv_group(const Shape& s, int64_t tiles, int sms) {
   return (int)std::max<int64_t>(1, std::min<int64_t>(std::max<int64_t>(1, nmt / 2), g));
 }
 
+// The tcgen05 FC2's output tiles per unit: its own choice from the tile
+// count (0) unless NVFP4MOE_FC2_GROUP names a divisor of its pass width.
+static int fc2_tc_group() {
+  const char* v = std::getenv("NVFP4MOE_FC2_GROUP");
+  return v ? std::max(0, std::atoi(v)) : 0;
+}
+
+// The tcgen05 FC2's last units (one tile per CTA) are split into parts about
+// 1/kFc2TailDiv as wide, so that its CTAs finish together
+// (NVFP4MOE_FC2_TAIL overrides; 1 = no split).
+constexpr int kFc2TailDiv = 4;
+static int fc2_tail_div() {
+  const char* v = std::getenv("NVFP4MOE_FC2_TAIL");
+  return v ? std::max(1, std::atoi(v)) : kFc2TailDiv;
+}
+
 // Above kSfTwoPassMin pairs the X scales take the token-major + atom pass
 // route, unless FC1 runs on the decode kernel (which reads them token-major).
 static bool sf_atom_pass(const Shape& s, int64_t T) { return T * s.k > kSfTwoPassMin && !fc1_gemv(s, T); }
@@ -670,6 +686,8 @@ static moe_status_t forward_impl(const moe_shape_t* shape, int32_t expert_begin,
     const int64_t units = tt * ((NMT + f2.group - 1) / f2.group);
     MOE_CUDA(launch_fc2_gemv(f2, (int)std::min<int64_t>(sms, units), stream));
   } else {
+    f2.group = fc2_tc_group();
+    f2.tail_div = fc2_tail_div();
     MOE_CUDA(launch_fc2(tm_w2, tm_aq, f2, (int)std::min<int64_t>(sms, tt * NMT), stream));
   }
 

@@ -104,6 +104,7 @@ struct Barriers {
   uint32_t tmem_base;
   volatile int32_t abort_flag;
   int32_t fc2_g;         // FC2: output tiles per work unit, chosen by thread 0 during setup
+  int32_t fc2_gs;        // FC2: output tiles per part of a split tail unit (= fc2_g: no split)
 };
 static_assert(sizeof(Barriers) <= 1024, "barrier block");
 
@@ -246,8 +247,51 @@ __device__ __forceinline__ float4 unit_scalars(const Fc1Args& p, const int4& t) 
 
 // FC2 work unit -> (token tile, group of G consecutive 128-feature tiles);
 // groups outermost, so the groups of one pass over H run together.
-__device__ __forceinline__ int4 fc2_next_tile(const int4* tiles, int unit, int num_units, int ntiles) {
-  return unit < num_units ? tiles[unit % ntiles] : make_int4(-1, 0, 0, 0);
+// FC2's work units.  Unit u < U0 is (tile u % ntiles, output tiles
+// [(u / ntiles) * G, + G)), groups outermost; with Gs < G the last `ntail`
+// tiles of the last group are split into S = G / Gs parts of Gs output tiles
+// each and come last, so that the units taken at the end are short and the
+// CTAs finish together (the parts reload their tile's activations, so the
+// split is kept to one tile per CTA).
+struct Fc2Units {
+  int ntiles, G, NG, S, Gs, ntail, U0, num;
+  __device__ __forceinline__ void init(int nt, int NMT, int G_, int Gs_, int grid) {
+    ntiles = nt;
+    G = G_;
+    NG = NMT / G;
+    Gs = Gs_;
+    S = G / Gs;
+    ntail = (S > 1 && nt > 0) ? min(nt, grid) : 0;
+    U0 = nt * NG - ntail;
+    num = U0 + ntail * S;
+  }
+  __device__ __forceinline__ int tile_index(int u) const {
+    return u < U0 ? u % ntiles : ntiles - ntail + (u - U0) / S;
+  }
+  __device__ __forceinline__ int first_mt(int u) const {
+    return u < U0 ? (u / ntiles) * G : (NG - 1) * G + ((u - U0) % S) * Gs;
+  }
+  __device__ __forceinline__ int width(int u) const { return u < U0 ? G : Gs; }
+  // the unit as the MMA and epilogue warps see it: first output tile << 8 | count (a negative u passes through)
+  __device__ __forceinline__ int code(int u) const { return u < 0 ? u : (first_mt(u) << 8) | width(u); }
+};
+
+// Width of the split tail units: the widest divisor of G that is at most
+// G / tail_div, or G itself (no split) when tail_div <= 1 or the tiles hold
+// fewer than kFc2TailMinRows routed pairs on average (there the weight
+// stream, not the tiles' reductions, sets the units' cost and the extra
+// activation loads of the parts do not pay).
+constexpr int kFc2TailMinRows = 48;
+__device__ __forceinline__ int fc2_tail_width(int G, int tail_div, int ntiles, int64_t pairs) {
+  if (tail_div <= 1 || ntiles <= 0 || pairs < (int64_t)kFc2TailMinRows * ntiles) return G;
+  int gs = 1;
+  for (int d = 2; d <= G; ++d)
+    if (G % d == 0 && d * tail_div <= G) gs = d;
+  return gs;
+}
+
+__device__ __forceinline__ int4 fc2_next_tile(const int4* tiles, int unit, const Fc2Units& us) {
+  return (unit >= 0 && unit < us.num) ? tiles[us.tile_index(unit)] : make_int4(-1, 0, 0, 0);
 }
 
 // Feature tiles per FC2 unit: the divisor G of the pass width npu that
@@ -255,9 +299,10 @@ __device__ __forceinline__ int4 fc2_next_tile(const int4* tiles, int unit, int n
 // unit streams G W2 tiles and costs about two more in activation loads and
 // hand-over.  Small batches get long units (few tiles, overhead dominates);
 // large batches short ones.
+constexpr int kFc2MaxGroup = 255;   // a unit's output-tile count travels in 8 bits
 __device__ __forceinline__ int fc2_group(int ntiles, int NMT, int npu, int grid) {
   int best = 1, best_cost = -1;
-  for (int G = 1; G <= npu; ++G) {
+  for (int G = 1; G <= min(npu, kFc2MaxGroup); ++G) {
     if (npu % G) continue;
     const int units = ntiles * (NMT / G);
     const int cost = (units + grid - 1) / grid * (G + 2);
@@ -618,7 +663,11 @@ __global__ void __launch_bounds__(kFc2Threads, 1)
     // The tile count comes from the routing kernel, which completed before
     // FC1 started, so it is read before waiting for FC1; one thread picks the
     // group size and the setup barrier shares it.
-    bars->fc2_g = fc2_group(clamp_tiles(__ldcg(p.hdr + HDR_NUM_TT), p.max_tiles), NMT, npu, gridDim.x);
+    const int nt = clamp_tiles(__ldcg(p.hdr + HDR_NUM_TT), p.max_tiles);
+    const int g = (p.group > 0 && p.group <= kFc2MaxGroup && npu % p.group == 0) ? p.group
+                                                                                 : fc2_group(nt, NMT, npu, gridDim.x);
+    bars->fc2_g = g;
+    bars->fc2_gs = fc2_tail_width(g, p.tail_div, nt, p.num_pairs);
   }
   gemm_setup<kMaxStages, kFc2EpiWarps>(bars, warp, 1, 1, 1 + kFc2EpiWarps);
   const uint32_t tmem = bars->tmem_base;
@@ -626,7 +675,6 @@ __global__ void __launch_bounds__(kFc2Threads, 1)
   pdl_launch_dependents();
   const int ntiles = clamp_tiles(p.hdr[HDR_NUM_TT], p.max_tiles);
   const int G = bars->fc2_g;
-  const int num_units = ntiles * (NMT / G);
   // Accumulator slots: the 256 accumulator columns split into slots as wide as
   // the widest token tile of this call, at least 32 columns (8 slots when
   // decoding), so that many narrow sub-units can be in flight between MMA and
@@ -647,6 +695,9 @@ __global__ void __launch_bounds__(kFc2Threads, 1)
       // The CTA's units: taken from the work counter (seeded by routing on
       // every call) or by the static stride, each published one unit ahead
       // of the W2 stream that serves it.
+      Fc2Units us;
+      us.init(ntiles, NMT, G, bars->fc2_gs, (int)gridDim.x);
+      const int num_units = us.num;
       int taken = 0;
       auto take = [&]() -> int {
         const int u = p.dynamic ? atomicAdd(p.next, 1) : (int)blockIdx.x + taken * (int)gridDim.x;
@@ -655,12 +706,12 @@ __global__ void __launch_bounds__(kFc2Threads, 1)
       };
       int qj = 0;
       int unit = take();
-      int4 tl = fc2_next_tile(tiles, unit < 0 ? num_units : unit, num_units, ntiles);
-      ok = uq_publish(bars, qj++, unit, tl, p.status);
+      int4 tl = fc2_next_tile(tiles, unit, us);
+      ok = uq_publish(bars, qj++, us.code(unit), tl, p.status);
       while (ok && unit >= 0) {
         const int un = take();
-        const int4 tn = fc2_next_tile(tiles, un < 0 ? num_units : un, num_units, ntiles);
-        if (!uq_publish(bars, qj++, un, tn, p.status)) break;
+        const int4 tn = fc2_next_tile(tiles, un, us);
+        if (!uq_publish(bars, qj++, us.code(un), tn, p.status)) break;
         const int cur = unit;
         const int4 ct = tl;
         unit = un;
@@ -670,7 +721,7 @@ __global__ void __launch_bounds__(kFc2Threads, 1)
           continue;
         }
         const int4 tlc = ct;
-        const int mt0 = (cur / ntiles) * G;
+        const int mt0 = us.first_mt(cur), cnt = us.width(cur);
         const int e = tlc.x, row0 = tlc.y, rows = tlc.z;
         const int nch = (rows + kTokChunk - 1) / kTokChunk;
         // the token tile's activations, once per unit
@@ -683,8 +734,8 @@ __global__ void __launch_bounds__(kFc2Threads, 1)
         for (int kb = 0; kb < NKB; ++kb) load_rows(as + kb * 8192, tm_aq, kb * 64, row0, nch, 1024u, &bars->act_full[slot]);
         bulk_g2s(as + act_sf, p.sfa + (size_t)(row0 >> 7) * NA * 512u, (uint32_t)(NA * 512), &bars->act_full[slot]);
         ++local;
-        // the group's W2 tiles through the ring
-        for (int g = 0; g < G && ok; ++g) {
+        // the unit's W2 tiles through the ring
+        for (int g = 0; g < cnt && ok; ++g) {
           const int mt = mt0 + g;
           for (int kb0 = 0; kb0 < NKB; kb0 += KS) {
             if (!wait_or_abort(&bars->empty[stage], phase ^ 1u, bars, p.status)) {
@@ -729,6 +780,7 @@ __global__ void __launch_bounds__(kFc2Threads, 1)
       int unit = uq_read(bars, 0, tn, p.status);
       while (unit >= 0 && ok) {
         const int4 tl = tn;
+        const int cnt = unit & 0xFF;
         unit = uq_read(bars, qj + 1, tn, p.status);   // the next entry (published already or soon)
         uq_release(bars, qj++);
         if (unit == -2) break;
@@ -743,7 +795,7 @@ __global__ void __launch_bounds__(kFc2Threads, 1)
         const uint32_t sfb = tmem + kFc2SfbCol + slot * (uint32_t)(NA * 4);
         for (int a = 0; a < NA; ++a) tmem_cp_32x128b_x4(sfb + a * 4, sf_desc(as + act_sf + a * 512));
         const uint64_t bd0 = smem_desc(smem_u32(as), 16, 512, kLayoutSW64);   // + 512 per k-block, + 2 per K-step
-        for (int g = 0; g < G && ok; ++g, ++sub) {
+        for (int g = 0; g < cnt && ok; ++g, ++sub) {
           const uint32_t buf = (uint32_t)sub % nslots, use = (uint32_t)sub / nslots;
           if (!wait_or_abort(&bars->tmem_empty[buf], (use & 1u) ^ 1u, bars, p.status)) {
             ok = false;
@@ -840,10 +892,10 @@ __global__ void __launch_bounds__(kFc2Threads, 1)
       if (tile_ok(nxt, p.E, p.max_rows)) columns(nxt, wgt_nxt, tok_nxt);
       else columns(make_int4(-1, 0, 0, 0), wgt_nxt, tok_nxt);
       if (!tile_ok(tl, p.E, p.max_rows)) continue;
-      const int mt0 = (unit / ntiles) * G;
+      const int mt0 = unit >> 8, cnt = unit & 0xFF;
       const int rows = tl.z;
       const int nch = (rows + kTokChunk - 1) / kTokChunk;
-      for (int g = 0; g < G; ++g, ++sub) {
+      for (int g = 0; g < cnt; ++g, ++sub) {
         const uint32_t buf = (uint32_t)sub % nslots, use = (uint32_t)sub / nslots;
         if (!wait_or_abort(&bars->tmem_full[buf], use & 1u, bars, p.status)) {
           ok = false;

@@ -175,7 +175,8 @@ struct Fc2Args {
   int32_t H, I, E, k;
   int32_t nq;               // passes over H (H/128 divisible by nq)
   int32_t kbs_per_stage;    // k-blocks per W2 ring stage: I/128 (a whole output tile) or 1 (selects the kernel)
-  int32_t group;            // output tiles per work unit of the decode kernel
+  int32_t group;            // output tiles per work unit (decode kernel; tcgen05 kernel: 0 = its own choice)
+  int32_t tail_div;         // tcgen05 kernel: the last units split into parts about 1/tail_div as wide (<= 1: none)
   int32_t* next;            // work counter (hdr + HDR_FC2_NEXT): CTAs take units from it when `dynamic`
   int32_t dynamic;          // 1: units by the work counter; 0: the static stride blockIdx.x + i * gridDim.x
   int32_t max_tiles;
