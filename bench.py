@@ -62,6 +62,8 @@ WORKLOADS = {
                     text="T=4096, H=3584, I=384, E=896, top-k=16, Zipf(1.1) ids without replacement"),
     "decode16": dict(T=16, routing="uniform", big_rows_frac=0.0,
                      text="T=16, H=3584, I=384, E=896, top-k=16, uniform distinct ids"),
+    "T1024": dict(T=1024, routing="uniform", big_rows_frac=0.0,
+                  text="T=1024, H=3584, I=384, E=896, top-k=16, uniform distinct ids"),
     # a small case of the same kernels for counter captures (weights 0.3 GB, still larger than L2)
     "small_e128": dict(T=1024, routing="uniform", big_rows_frac=0.0, E=128,
                        text="T=1024, H=3584, I=384, E=128, top-k=16, uniform distinct ids (profiling case)"),
