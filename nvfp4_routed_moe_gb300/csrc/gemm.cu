@@ -79,24 +79,29 @@ constexpr int kFc1Threads = 32 * (kFc1Epi0 + kFc1EpiWarps);
 // is 1 or I/128 (a whole output tile, so that the issuing thread waits,
 // fences and commits once per tile, which pays at small and medium batches);
 // the stage count follows from I and KS.
-constexpr int kMaxStages = 24;
+constexpr int kMaxStages = 20;
 constexpr int kFc2KbBytes = 9216;   // codes (8 KB) + scale atoms (1 KB) of one k-block
 constexpr int kFc2EpiWarps = 16;
-constexpr int kFc2Threads = 64 + 32 * kFc2EpiWarps;
+// FC2 warps: 0 TMA producer, 1 MMA issuer and TMEM owner, 2 .. 2 + kFc2EpiWarps - 1
+// epilogue, then the thread that copies each W2 stage's scale atoms to TMEM.
+constexpr int kFc2CopyWarp = 2 + kFc2EpiWarps;
+constexpr int kFc2Threads = 32 * (kFc2CopyWarp + 1);
 constexpr int kFc2MaxI = 512;
 constexpr uint32_t kFc2SfbCol = 448;   // TMEM column of the activation slots' scale factors
 
-constexpr int kMaxAccSlots = 16;
+constexpr int kMaxAccSlots = 8;
 constexpr int kUnitQueue = 8;   // entries of a CTA's work-unit queue
 
 struct Barriers {
   uint64_t full[kMaxStages];
   uint64_t empty[kMaxStages];
+  uint64_t sready[kMaxStages];    // FC2: the stage's W2 scale atoms are in TMEM (the copy thread's commit)
   uint64_t tmem_full[kMaxAccSlots];
   uint64_t tmem_empty[kMaxAccSlots];
   uint64_t act_full[2];
   uint64_t act_empty[2];
   uint64_t drain;
+  uint64_t drain_cp;              // FC2: the copy thread's last copies complete
   uint64_t uq_full[kUnitQueue];   // work-unit queue: entry published by the producer thread
   uint64_t uq_empty[kUnitQueue];  // ... read by every consuming role
   int4 uq_tile[kUnitQueue];
@@ -158,6 +163,7 @@ __device__ void gemm_setup(Barriers* bars, int warp, int tmem_warp, uint32_t ful
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&bars->full[s], full_arrivals);
       mbar_init(&bars->empty[s], 1);
+      mbar_init(&bars->sready[s], 1);
     }
     for (int b = 0; b < kMaxAccSlots; ++b) {
       mbar_init(&bars->tmem_full[b], 1);
@@ -168,6 +174,7 @@ __device__ void gemm_setup(Barriers* bars, int warp, int tmem_warp, uint32_t ful
       mbar_init(&bars->act_empty[b], 1);
     }
     mbar_init(&bars->drain, 1);
+    mbar_init(&bars->drain_cp, 1);
     for (int q = 0; q < kUnitQueue; ++q) {
       mbar_init(&bars->uq_full[q], 1);
       mbar_init(&bars->uq_empty[q], uq_consumers);
@@ -669,7 +676,7 @@ __global__ void __launch_bounds__(kFc2Threads, 1)
     bars->fc2_g = g;
     bars->fc2_gs = fc2_tail_width(g, p.tail_div, nt, p.num_pairs);
   }
-  gemm_setup<kMaxStages, kFc2EpiWarps>(bars, warp, 1, 1, 1 + kFc2EpiWarps);
+  gemm_setup<kMaxStages, kFc2EpiWarps>(bars, warp, 1, 1, 2 + kFc2EpiWarps);
   const uint32_t tmem = bars->tmem_base;
   pdl_wait();
   pdl_launch_dependents();
@@ -772,7 +779,6 @@ __global__ void __launch_bounds__(kFc2Threads, 1)
       // Ring descriptors of stage 0, moved by their start-address field only
       // (see FC1's issuing thread).
       const uint64_t rd0 = smem_desc(smem_u32(ring), 16, 512, kLayoutSW64);   // + 512 per k-block, + 2 per K-step
-      const uint64_t rs0 = sf_desc(ring + KS * 8192);                          // + 32 per scale atom
       uint32_t soff = 0;                     // (stage * stage_bytes) >> 4
       uint32_t sfc = tmem + 256;             // the stage's scale columns
       int qj = 0;
@@ -804,13 +810,12 @@ __global__ void __launch_bounds__(kFc2Threads, 1)
           tc_fence_after();
           const uint32_t dcol = tmem + buf * slot_cols;
           for (int kb0 = 0; kb0 < NKB && ok; kb0 += KS) {
-            if (!wait_or_abort(&bars->full[stage], phase, bars, p.status)) {
+            // the stage has landed and the copy thread has put its scale atoms in TMEM
+            if (!wait_or_abort(&bars->sready[stage], phase, bars, p.status)) {
               ok = false;
               break;
             }
             tc_fence_after();
-#pragma unroll 2
-            for (int a = 0; a < 2 * KS; ++a) tmem_cp_32x128b_x4(sfc + a * 4, rs0 + soff + a * 32);
 #pragma unroll 1
             for (int j = 0; j < KS; ++j) {
               const int kb = kb0 + j;
@@ -836,6 +841,52 @@ __global__ void __launch_bounds__(kFc2Threads, 1)
       }
       tc_commit(&bars->drain);
       mbar_wait(&bars->drain, 0, p.status);
+    }
+  } else if (warp == kFc2CopyWarp) {
+    if (lane == 0) {
+      // ---------------------------------------------------------- scale copies
+      // Each ring stage's W2 scale atoms go to its TMEM scale columns as soon
+      // as the stage lands, and a commit tells the MMA thread they are there.
+      // Issued from their own thread, the copies are not part of the MMA
+      // thread's commits, so a stage is released once its MMAs are done
+      // rather than once the copies issued for later stages are too.
+      uint32_t stage = 0, phase = 0, soff = 0, sfc = tmem + 256;
+      const uint64_t rs0 = sf_desc(ring + KS * 8192);   // + 32 per scale atom
+      bool ok = true;
+      int qj = 0;
+      int4 tn;
+      int unit = uq_read(bars, 0, tn, p.status);
+      while (unit >= 0 && ok) {
+        const int4 tl = tn;
+        const int cnt = unit & 0xFF;
+        unit = uq_read(bars, qj + 1, tn, p.status);
+        uq_release(bars, qj++);
+        if (unit == -2) break;
+        if (!tile_ok(tl, p.E, p.max_rows)) continue;
+        for (int g = 0; g < cnt && ok; ++g) {
+          for (int kb0 = 0; kb0 < NKB; kb0 += KS) {
+            if (!wait_or_abort(&bars->full[stage], phase, bars, p.status)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+#pragma unroll 2
+            for (int a = 0; a < 2 * KS; ++a) tmem_cp_32x128b_x4(sfc + a * 4, rs0 + soff + a * 32);
+            tc_commit(&bars->sready[stage]);
+            if (++stage == (uint32_t)nstages) {
+              stage = 0;
+              phase ^= 1u;
+              soff = 0;
+              sfc = tmem + 256;
+            } else {
+              soff += (uint32_t)(stage_bytes / 16);
+              sfc += (uint32_t)(KS * 8);
+            }
+          }
+        }
+      }
+      tc_commit(&bars->drain_cp);
+      mbar_wait(&bars->drain_cp, 0, p.status);
     }
   } else {
     // ------------------------------------------------------------ epilogue
