@@ -100,9 +100,9 @@ moe_status_t moe_forward_launch_count(const moe_shape_t* shape, int64_t num_toke
 
 /* Which kernels one moe_forward runs for FC1 and FC2 at this shape and T
  * (host outs): 1 = the decode kernel (weights streamed through a bulk-copy
- * ring, products on warp-level mma.sync; up to 16 tokens by default), 0 =
- * the tcgen05 block-scaled GEMM.  Follows the same environment overrides as
- * the forward (NVFP4MOE_FC1_GEMV, NVFP4MOE_FC2_GEMV). */
+ * ring, products on warp-level mma.sync; by default FC1 up to 32 tokens,
+ * FC2 up to 16), 0 = the tcgen05 block-scaled GEMM.  Follows the same
+ * environment overrides as the forward (NVFP4MOE_FC1_GEMV, NVFP4MOE_FC2_GEMV). */
 moe_status_t moe_forward_kernels(const moe_shape_t* shape, int64_t num_tokens, int32_t* fc1_decode,
                                  int32_t* fc2_decode);
 

@@ -120,12 +120,14 @@ def test_forward_token_count_alignment_and_capacity_checked_before_launch(L):
     assert fwd(16) == 4                                 # never prepared
 
 def test_forward_kernel_choice(L, monkeypatch):
-    """The decode kernels run FC1 and FC2 up to 16 tokens, the tcgen05 GEMMs
-    above; the environment overrides either."""
+    """The decode kernels run FC1 up to 32 tokens and FC2 up to 16, the
+    tcgen05 GEMMs above; the environment overrides either."""
     full = api.shape(3584, 384, 896, 16)
     assert api.moe_forward_kernels(full, 1) == (True, True)
     assert api.moe_forward_kernels(full, 16) == (True, True)
-    assert api.moe_forward_kernels(full, 17) == (False, False)
+    assert api.moe_forward_kernels(full, 17) == (True, False)
+    assert api.moe_forward_kernels(full, 32) == (True, False)
+    assert api.moe_forward_kernels(full, 33) == (False, False)
     assert api.moe_forward_kernels(full, 16384) == (False, False)
     monkeypatch.setenv("NVFP4MOE_FC1_GEMV", "0")
     monkeypatch.setenv("NVFP4MOE_FC2_GEMV", "1")

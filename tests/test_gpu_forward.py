@@ -688,17 +688,21 @@ def test_recycled_workspace_memory_is_refused_on_the_device(tiny):
 
 
 @pytest.mark.parametrize("env", [{"NVFP4MOE_FC1_DYNAMIC": "0", "NVFP4MOE_FC2_DYNAMIC": "0"},
-                                 {"NVFP4MOE_FC2_TILE_STAGES": "0"}, {"NVFP4MOE_FC2_TILE_STAGES": "1"}])
+                                 {"NVFP4MOE_FC2_TILE_STAGES": "0"}, {"NVFP4MOE_FC2_TAIL": "1"},
+                                 {"NVFP4MOE_FC2_TAIL": "8", "NVFP4MOE_FC2_GROUP": "28"},
+                                 {"NVFP4MOE_FC2_GROUP": "4", "NVFP4MOE_FC2_DYNAMIC": "0"}])
 def test_full_shape_scheduling_options(full_model, env, monkeypatch):
     """The GEMMs' scheduling options give the same result: units by the
     routing-seeded work counters or by the static stride, FC2 ring stages of
-    a whole output tile or of one k-block.  T = 1024 (uniform ids; whole-tile
-    stages by default) and T = 16384 with the options of the environment,
-    sampled tile-boundary tokens against the oracle and the whole output
-    against the default configuration within the tolerance."""
+    a whole output tile or of one k-block, FC2's last units split into
+    parts or not, other unit widths.  T = 1024 (uniform ids), Zipf T = 4096
+    (heavy tiles: the split applies by default) and T = 16384 with the
+    options of the environment, sampled tile-boundary tokens against the
+    oracle and the whole output against the default configuration within
+    the tolerance."""
     minp, m = full_model
-    for T in (1024, 16384):
-        inp = _full_case(minp, T, "uniform", seed=300 + T)
+    for T, routing in ((1024, "uniform"), (4096, "zipf"), (16384, "uniform")):
+        inp = _full_case(minp, T, routing, seed=300 + T)
         ref_out, _ = m.forward_inputs(inp)
         torch.cuda.synchronize()
         for k, v in env.items():
@@ -710,8 +714,8 @@ def test_full_shape_scheduling_options(full_model, env, monkeypatch):
         assert api.moe_read_status(ws) == (0, 0)
         ids = inp.expert_ids
         sample = _tile_boundary_tokens(np.where(ids < 32, ids, 10 ** 6).astype(np.int32), 32)[:200]
-        assert_close(out_bits(out)[sample], cases.run_oracle(inp, tokens=sample), f"T={T} {env}")
-        assert_close(out_bits(out), out_bits(ref_out), f"T={T} {env} against the default")
+        assert_close(out_bits(out)[sample], cases.run_oracle(inp, tokens=sample), f"T={T} {routing} {env}")
+        assert_close(out_bits(out), out_bits(ref_out), f"T={T} {routing} {env} against the default")
 
 
 def test_full_shape_zero_and_subnormal_weight_block_scales(full_model):
