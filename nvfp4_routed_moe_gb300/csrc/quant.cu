@@ -95,15 +95,22 @@ __global__ void __launch_bounds__(256) quant_x_kernel(const QuantXArgs a) {
 // its four rows' tokens from the token-major scales and writes the 16-byte
 // chunk l of atoms 4m..4m+3, word c of a chunk from row l + 32c, so a warp
 // store covers one whole 512-byte atom.  Rows past a tile's fill are zero.
-__global__ void __launch_bounds__(256) sf_atoms_kernel(const SfAtomArgs a) {
+__global__ void __launch_bounds__(256, 4) sf_atoms_kernel(const SfAtomArgs a) {
   pdl_wait();
   pdl_launch_dependents();
   const int ntiles = min(a.hdr[HDR_NUM_TT], a.max_tiles);
   const int lane = threadIdx.x & 31, NA4 = a.H / 64, G = a.H / 16, NM = a.H / 256;
   const int4* tiles = reinterpret_cast<const int4*>(a.tt_list);
   uint4* atoms = reinterpret_cast<uint4*>(a.sfx);
+  // Warp w takes the 256-column steps [kB * (w % NH), + kB) of tile w / NH:
+  // a tile's steps are shared by NH warps with few registers each, so that
+  // many warps, and their loads, are in flight on every SM.
+  constexpr int kB = 2;
+  const int NH = (NM + kB - 1) / kB;
   const int64_t nwarps = (int64_t)gridDim.x * 8;
-  for (int64_t tile = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5); tile < ntiles; tile += nwarps) {
+  for (int64_t w = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5); w < (int64_t)ntiles * NH; w += nwarps) {
+    const int64_t tile = w / NH;
+    const int m0 = (int)(w - tile * NH) * kB;
     const int rows = __ldg(&tiles[tile].z);
     const uint4* src[4];
 #pragma unroll
@@ -112,28 +119,25 @@ __global__ void __launch_bounds__(256) sf_atoms_kernel(const SfAtomArgs a) {
       const int f = r < rows ? __ldg(a.prow_pair + tile * kTileRows + r) : -1;
       const bool ok = f >= 0 && f < a.num_pairs;
       src[c] = ok ? reinterpret_cast<const uint4*>(a.sft + (int64_t)(f / a.k) * G) : nullptr;
-      if (ok) a.wrow[tile * kTileRows + r] = bf16_bits_to_f32(__ldg(a.route_w + f));
+      if (ok && m0 == 0) a.wrow[tile * kTileRows + r] = bf16_bits_to_f32(__ldg(a.route_w + f));
     }
     uint4* dst = atoms + tile * NA4 * 32 + lane;
-    // seven 256-column steps (28 gathered 16-byte loads per lane) in flight
+    // kB 256-column steps (4 kB gathered 16-byte loads per lane) in flight
     // before their atoms are written
-    constexpr int kB = 7;
-    for (int m0 = 0; m0 < NM; m0 += kB) {
-      uint4 v[kB][4];
+    uint4 v[kB][4];
 #pragma unroll
-      for (int i = 0; i < kB; ++i)
+    for (int i = 0; i < kB; ++i)
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
-          v[i][c] = (m0 + i < NM && src[c]) ? __ldg(src[c] + m0 + i) : make_uint4(0u, 0u, 0u, 0u);
+      for (int c = 0; c < 4; ++c)
+        v[i][c] = (m0 + i < NM && src[c]) ? __ldg(src[c] + m0 + i) : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
-      for (int i = 0; i < kB; ++i) {
-        if (m0 + i >= NM) break;
-        uint4* d = dst + 4 * (m0 + i) * 32;
-        d[0] = make_uint4(v[i][0].x, v[i][1].x, v[i][2].x, v[i][3].x);
-        d[32] = make_uint4(v[i][0].y, v[i][1].y, v[i][2].y, v[i][3].y);
-        d[64] = make_uint4(v[i][0].z, v[i][1].z, v[i][2].z, v[i][3].z);
-        d[96] = make_uint4(v[i][0].w, v[i][1].w, v[i][2].w, v[i][3].w);
-      }
+    for (int i = 0; i < kB; ++i) {
+      if (m0 + i >= NM) break;
+      uint4* d = dst + 4 * (m0 + i) * 32;
+      d[0] = make_uint4(v[i][0].x, v[i][1].x, v[i][2].x, v[i][3].x);
+      d[32] = make_uint4(v[i][0].y, v[i][1].y, v[i][2].y, v[i][3].y);
+      d[64] = make_uint4(v[i][0].z, v[i][1].z, v[i][2].z, v[i][3].z);
+      d[96] = make_uint4(v[i][0].w, v[i][1].w, v[i][2].w, v[i][3].w);
     }
   }
 }
@@ -306,7 +310,7 @@ cudaError_t launch_quant_x(const QuantXArgs& a, cudaStream_t st) {
 cudaError_t launch_sf_atoms(const SfAtomArgs& a, int64_t max_tiles, int num_sms, cudaStream_t st) {
   SfAtomArgs args = a;
   void* kargs[] = {&args};
-  const int64_t want = (max_tiles + 7) / 8;   // a warp per tile
+  const int64_t want = (max_tiles * ((a.H / 256 + 1) / 2) + 7) / 8;   // a warp per 2 column steps of a tile
   const unsigned blocks = (unsigned)(want < (int64_t)num_sms * 8 ? want : (int64_t)num_sms * 8);
   return launch_with_pdl((const void*)sf_atoms_kernel, dim3(blocks ? blocks : 1), dim3(256), 0, st, kargs);
 }
