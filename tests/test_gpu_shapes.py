@@ -3,7 +3,9 @@ oracle (every output).  Together they reach every supported extreme: the
 smallest hidden size (256) and k = 1; I = 256 and I = 512 (the largest, which
 changes FC1's units per token tile and FC2's stage count); 1024 experts with
 k = 32; experts with several 128-row token tiles and a ragged last tile; H not
-a multiple of 512."""
+a multiple of 512; heavy tiles (256 pairs per expert) in units of two
+output tiles, whose last units FC2 splits into single tiles (also with
+I = 512)."""
 import pytest
 import torch
 
@@ -19,6 +21,8 @@ SHAPES = [  # (H, I, E, k, T)
     (1024, 512, 64, 8, 40),
     (256, 128, 1024, 32, 20),
     (4096, 128, 16, 2, 300),
+    (512, 128, 64, 4, 4096),
+    (512, 512, 20, 4, 1300),
 ]
 
 
