@@ -28,16 +28,20 @@
 // 128.  The epilogue scales by dA*dW2[e] and the route weight and adds each
 // routed pair's 128 outputs into its token's fp32 accumulator row with L2
 // reductions (one coalesced 128-byte reduction per warp and token).  Groups
-// run outermost in nq passes over H, so the accumulator rows of one pass,
-// T x H/nq fp32, stay resident in L2 while they are summed; the per-pair FC2
-// rows never reach memory.  The finalize kernel rounds the sums to BF16.
+// run outermost (in nq passes over H), so the accumulator columns of one
+// group are the reductions' working set; the per-pair FC2 rows never reach
+// memory.  The finalize kernel rounds the sums to BF16.  When the tiles are
+// heavy, the last unit of one tile per CTA is split into narrower parts that
+// are taken last, so that the CTAs finish together.
 //
 // Warp roles (FC2; FC1's are listed with its constants): warp 0 issues TMA,
-// warp 1 owns TMEM and issues MMAs, the remaining warps drain TMEM (each
-// 32-lane quarter by several warps taking alternate 16-column chunks).  In
-// FC1 warps 0 and 1 gather the X rows.  Persistent CTAs stride over the work units;
-// the stage ring and the barrier phases carry across units.  Every wait is
-// bounded.
+// warp 1 owns TMEM and issues MMAs, the next warps drain TMEM (each 32-lane
+// quarter by several warps taking alternate 16-column chunks), and the last
+// one copies each stage's W2 scale atoms to TMEM (outside the MMA thread,
+// whose commits then cover its MMAs alone).  In FC1 warps 0 and 1 gather the
+// X rows.  Persistent CTAs take their work units from a counter that routing
+// seeds; the stage ring and the barrier phases carry across units.  Every
+// wait is bounded.
 #include "nvfp4.cuh"
 #include "plan.h"
 
