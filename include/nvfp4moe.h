@@ -26,10 +26,22 @@
  * are the measured best):
  *  - NVFP4MOE_PDL=0: launch without programmatic dependent launch (each
  *    kernel then starts only after its predecessor has finished); read once.
- *  - NVFP4MOE_FC1_PAIR=1 or 2: W13 tiles per FC1 work unit (default 1 up to
- *    16 tokens, else 2); read at every forward.
+ *  Read at every forward unless noted:
+ *  - NVFP4MOE_FC1_GEMV=0/1, NVFP4MOE_FC2_GEMV=0/1: FC1 / FC2 on the decode
+ *    kernel (warp-level MMAs over the streamed weights) or on the tcgen05
+ *    GEMM (default: the decode kernel up to 32 tokens for FC1, 16 for FC2).
+ *  - NVFP4MOE_FC1_PAIR=1 or 2: W13 tiles per work unit of FC1's tcgen05
+ *    GEMM (default 1 up to 16 tokens, else 2).
+ *  - NVFP4MOE_FC1_DYNAMIC=0, NVFP4MOE_FC2_DYNAMIC=0: the GEMMs' CTAs take
+ *    their units by a static stride instead of the routing-seeded counters.
+ *  - NVFP4MOE_FC2_GROUP=n: output tiles per FC2 work unit (tcgen05: a
+ *    divisor of the pass width, else ignored; decode kernel: any n >= 1).
+ *  - NVFP4MOE_FC2_TAIL=n: FC2's last units split into parts about 1/n as
+ *    wide (default 4; 1 = no split).
+ *  - NVFP4MOE_FC2_TILE_STAGES=0: FC2 ring stages of one k-block instead of a
+ *    whole output tile.
  *  - NVFP4MOE_ACC_PASS_MB=n: L2 budget in MiB of one FC2 pass over H (the
- *    accumulator slice T x H/passes fp32; default 64); read at every forward.
+ *    accumulator slice T x H/passes fp32; default 64).
  */
 #ifndef NVFP4MOE_H_
 #define NVFP4MOE_H_
