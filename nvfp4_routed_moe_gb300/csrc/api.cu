@@ -296,7 +296,7 @@ constexpr int64_t kFc1SingleMaxTokens = 16;
 // W13 tiles per FC1 work unit: two (shared X loads and scale copies) unless
 // the batch is so small that single tiles are needed to keep the SMs busy
 // (NVFP4MOE_FC1_PAIR=1/2 overrides).
-static int fc1_pair(const Shape& s, int64_t T) {
+static int fc1_pair(const Shape&, int64_t T) {
   if (const char* v = std::getenv("NVFP4MOE_FC1_PAIR")) {
     if (v[0] == '1') return 1;
     if (v[0] == '2') return 2;
